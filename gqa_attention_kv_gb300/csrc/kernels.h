@@ -1,0 +1,44 @@
+// kernels.h -- host-side launchers shared between the C ABI and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/attn_kv.h"
+
+namespace gqa {
+
+int device_sm_count();
+
+// Encode a 2D/3D bf16 tensor map with 128-byte swizzle (returns false on failure).
+bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
+
+int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
+                     void *k_cache, void *v_cache, int64_t num_slots, int row_bytes,
+                     int32_t *err, cudaStream_t stream);
+
+// Decode plan: how the grid splits each request's keys.
+struct DecodePlan {
+    int head_dim;
+    int m_tiles;      // 16-row MMA tiles per CTA (1 or 2)
+    int rows;         // q_rows * group
+    int row_blocks;   // CTAs along the query rows of one KV head
+    int nsplit;       // CTAs along the keys of one (request, KV head, row block)
+    size_t workspace; // bytes of fp32 partial states (0 when nsplit == 1)
+};
+
+int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
+                int head_dim, int max_seq_len, int window, DecodePlan *plan);
+
+int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *cache,
+                  const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
+                  int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
+                  void *out, void *workspace, int32_t *err, cudaStream_t stream);
+
+int launch_prefill(const void *q, const void *k, const void *v, int batch, int seq_len,
+                   int window, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                   void *out, int32_t *err, cudaStream_t stream);
+
+}  // namespace gqa

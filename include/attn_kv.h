@@ -1,0 +1,204 @@
+/*
+ * attn_kv.h -- C ABI of the GB300 grouped-query attention library.
+ *
+ * Three operations on one decoder KV cache, each a few kernel launches on the
+ * caller's stream:
+ *
+ *   attn_kv_append  write new K/V rows into the cache slots a slot_mapping names
+ *   attn_decode     causal decode attention, 1..K query rows per request, over a
+ *                   linear, paged (block-table) or ring-buffer (sliding-window)
+ *                   cache, as a split-KV flash-decode plus a merge of the
+ *                   partial softmax states
+ *   attn_prefill    causal (optionally windowed) GQA prefill attention
+ *
+ * Sources for the operations (cited by page title and section):
+ *   - vibevoice.c, "The kernels that matter", "Attention backends", "Paged KV
+ *     cache", "The decode step is one submission": split-KV decode whose
+ *     partial softmax states a second kernel merges, all query heads of a GQA
+ *     group reading a cache position once, a device-side page table, and the
+ *     step's moving parts (where new K/V land, how far attention walks) read
+ *     from device memory so a captured CUDA graph replays.
+ *   - Voxtral Realtime -- Architecture & Design Notes, "KV cache", "SDPA",
+ *     "Attention layout", "Encoder KV cache": [B, S, H, D] caches, GQA by head
+ *     ratio, ring buffers sized 2x the window, the analytic ring position and
+ *     the sliding-window mask  valid = (t >= 0) & (pos - t >= 0) &
+ *     (pos - t < window).
+ *   - talker_multiframe (vLLM-Omni NPU worker), "How a frame advances without
+ *     the host" and the NarrowStep fields: K sequential query rows per request
+ *     with positions, slot_mapping, seq_lens and an unchanged block table.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are bf16 (16-bit words) unless stated otherwise, row-major,
+ *     last dimension contiguous, in DEVICE memory, and owned by the caller.
+ *     Every base pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
+ *   - The library never allocates, frees or synchronises, and launches only on
+ *     the stream it is given (never the legacy default stream unless the
+ *     caller passes 0).
+ *   - Host-checkable problems (null pointers, bad sizes, unsupported shapes,
+ *     too small a workspace) return a nonzero attn_status BEFORE any launch.
+ *   - Data-dependent problems found on the device (a slot, page or position
+ *     outside its buffer) never fault: the offending row or key is skipped and,
+ *     when err_word is not NULL, the first such error code is stored there
+ *     (atomically; a zero word stays zero when nothing went wrong).  Every
+ *     device-side wait is bounded; one that gives up stores ATTN_ERR_TIMEOUT.
+ *     The caller clears *err_word and reads it back when it wants to know.
+ *   - A return of ATTN_ERR_CUDA means a launch was rejected by the runtime.
+ *   - Head mapping: query head h reads KV head h / (n_q_heads / n_kv_heads).
+ *   - head_dim must be 64 or 128.
+ */
+#ifndef GQA_ATTN_KV_H
+#define GQA_ATTN_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *attn_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,        /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = 2,       /* sizes inconsistent or out of range */
+    ATTN_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
+    ATTN_ERR_WORKSPACE = 4,   /* workspace smaller than attn_decode_workspace_size */
+    ATTN_ERR_BOUNDS = 5,      /* device: slot / page / position outside its buffer */
+    ATTN_ERR_TIMEOUT = 6,     /* device: a bounded wait gave up */
+    ATTN_ERR_CUDA = 7,        /* the CUDA runtime rejected a launch */
+    ATTN_ERR_ALIGN = 8        /* a base pointer is not 16-byte aligned */
+} attn_status;
+
+typedef enum {
+    ATTN_CACHE_LINEAR = 0, /* request b, position t -> slot b*slots_per_seq + t */
+    ATTN_CACHE_PAGED = 1,  /* -> block_table[b][t / block_size]*block_size + t % block_size */
+    ATTN_CACHE_RING = 2    /* -> slot b*slots_per_seq + t % slots_per_seq (ring of that size) */
+} attn_cache_kind;
+
+/*
+ * One layer's KV cache.  k and v are [num_slots, n_kv_heads, head_dim] bf16
+ * (the pages' [B, S, H, D] layout with requests and positions flattened into
+ * slots).  The struct itself is read on the host during the call only.
+ *
+ *   LINEAR: slots_per_seq = capacity of each request's window.
+ *   PAGED : block_table is a DEVICE int32 [batch, max_blocks_per_seq] array of
+ *           page ids; page p covers slots p*block_size .. p*block_size +
+ *           block_size - 1.  block_size >= 1.  The table may change between
+ *           calls (a captured graph follows it).
+ *   RING  : slots_per_seq = ring size R; position t of request b lives in slot
+ *           b*R + t % R.  A ring holds the last R positions written.
+ */
+typedef struct {
+    int32_t kind;               /* attn_cache_kind */
+    void *k;                    /* bf16 [num_slots, n_kv_heads, head_dim] */
+    void *v;                    /* bf16 [num_slots, n_kv_heads, head_dim] */
+    int64_t num_slots;
+    int32_t slots_per_seq;      /* LINEAR capacity, RING size; unused for PAGED */
+    const int32_t *block_table; /* PAGED only, device */
+    int32_t block_size;         /* PAGED only */
+    int32_t max_blocks_per_seq; /* PAGED only: row length of block_table */
+} attn_kv_cache;
+
+/*
+ * attn_kv_append -- cache.k[slot_mapping[i]] = k_new[i]; same for v.
+ *
+ * Source: the step writes its new K/V before attention reads them (Voxtral
+ * notes, "Encoder KV cache": writes happen before attention), into the slot the
+ * engine reserved for each new row (talker_multiframe, NarrowStep field
+ * slot_mapping[r]); the slot is a device value so a replayed graph lands each
+ * step's row in its own place (vibevoice.c, "The decode step is one
+ * submission").
+ *
+ *   k_new, v_new  bf16 [n, n_kv_heads, head_dim], device
+ *   slot_mapping  int64 [n], device; a slot outside [0, cache->num_slots) skips
+ *                 its row and stores ATTN_ERR_BOUNDS in *err_word
+ *   n             rows to write (0 is a no-op)
+ * Copies are bit-exact.  With a slot repeated inside one call, which row lands
+ * is unspecified.  Does not read cache->kind: slots are absolute.
+ */
+int attn_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
+                   const attn_kv_cache *cache, int n_kv_heads, int head_dim, int32_t *err_word,
+                   attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
+ * this shape (the fp32 partial softmax states of its cache splits).  The same
+ * arguments must be passed to attn_decode.  0 means no workspace is needed.
+ * Returns (size_t)-1 for arguments attn_decode would reject.
+ */
+size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_rows,
+                                  int n_q_heads, int n_kv_heads, int head_dim, int max_seq_len,
+                                  int window);
+
+/*
+ * attn_decode -- causal decode attention for q_rows query rows per request.
+ *
+ * Source: vibevoice.c, "The kernels that matter" / "Attention backends"
+ * (split-KV decode whose partial softmax states are merged by a second kernel;
+ * the heads of a GQA group read each cache position once); talker_multiframe,
+ * NarrowStep fields (K sequential query rows per request, positions[r],
+ * seq_lens[r] = keys written, the block table); Voxtral notes, "Encoder KV
+ * cache" (the sliding-window mask and the ring).
+ *
+ *   q          bf16 [batch, q_rows, n_q_heads, head_dim], device
+ *   cache      the layer's cache (see attn_kv_cache)
+ *   seq_lens   int32 [batch], device: keys written for each request, this
+ *              step's rows included
+ *   positions  int32 [batch*q_rows], device: absolute position of each query
+ *              row.  Row (b, r) attends key position t iff
+ *                  0 <= t < seq_lens[b],  t <= positions[b*q_rows + r],
+ *                  window <= 0 or positions[...] - t < window,
+ *                  RING: t >= seq_lens[b] - slots_per_seq (still in the ring).
+ *              For LINEAR and PAGED caches a step's rows are normally
+ *              positions seq_len - q_rows + r.
+ *   batch, q_rows   >= 1 (batch 0 is a no-op)
+ *   max_seq_len     host-side upper bound of seq_lens[]; it sizes the grid
+ *              (the split count) only, so a graph captured for one bound
+ *              replays for any seq_lens up to it.  Keys beyond it are not read.
+ *   window     sliding window in positions; <= 0 means none.  RING requires
+ *              window > 0 and slots_per_seq >= window + q_rows - 1.
+ *   scale      multiplies q.k before the natural-base softmax
+ *   out        bf16 [batch, q_rows, n_q_heads, head_dim], device; rounded
+ *              once from fp32 (round to nearest even).  A row with no valid
+ *              key gets zeros.
+ *   workspace  device scratch of at least
+ *              attn_decode_workspace_size(...) bytes (may be NULL when that is
+ *              0), 16-byte aligned; its contents are not needed between calls.
+ */
+int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
+                const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
+                int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,
+                void *workspace, size_t workspace_bytes, int32_t *err_word,
+                attn_stream_t stream);
+
+/*
+ * attn_prefill -- causal GQA self-attention over whole sequences.
+ *
+ * Source: vibevoice.c, "Prefill attention" and "Attention backends" (causal
+ * attention with both contractions on the tensor cores and the heads of a GQA
+ * group sharing K/V tiles); Voxtral notes, "Offline Encoder" (causal SDPA over
+ * the whole input, head_dim 64, and the 750-frame sliding window that only
+ * matters beyond 750 frames).
+ *
+ *   q    bf16 [batch, seq_len, n_q_heads, head_dim], device
+ *   k, v bf16 [batch, seq_len, n_kv_heads, head_dim], device
+ *   Query i of a sequence attends keys t of the same sequence with t <= i and,
+ *   when window > 0, i - t < window.
+ *   out  bf16 [batch, seq_len, n_q_heads, head_dim], device, rounded once.
+ */
+int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,
+                 int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,
+                 int32_t *err_word, attn_stream_t stream);
+
+/* Human-readable name of an attn_status. */
+const char *attn_status_string(int status);
+
+/* Library version string. */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_KV_H */

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/attn_kv.h declares, and refuses bad arguments with
+the documented status before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_kv_gb300 as gq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gqa_attention_kv_gb300 import build
+
+    build.build()
+    return gq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("attn_kv_append", "attn_decode", "attn_decode_workspace_size", "attn_prefill",
+                 "attn_status_string", "attn_version"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert gq.attn_status_string(code) != "unknown status"
+    assert gq.attn_status_string(99) == "unknown status"
+    assert "sm_103a" in gq.attn_version()
+
+
+class FakeTensor:
+    """Pointer + shape stand-in: validation must refuse before touching it."""
+
+    def __init__(self, ptr, shape):
+        self._p, self.shape = ptr, shape
+
+    def data_ptr(self):
+        return self._p
+
+    def numel(self):
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n
+
+    def element_size(self):
+        return 1
+
+
+def cache(kind=gq.LINEAR, Hkv=8, D=128, slots=1024, sps=512, bt=None, bs=0, k=4096, v=8192):
+    return gq.KVCache(kind, FakeTensor(k, (slots, Hkv, D)), FakeTensor(v, (slots, Hkv, D)),
+                      slots_per_seq=sps, block_table=bt, block_size=bs)
+
+
+def decode_rc(lib, c, B=2, R=1, Hq=32, Hkv=8, D=128, L=512, W=0, q=16, out=32, ws=None,
+              ws_bytes=0):
+    cs = c.struct()
+    return lib.attn_decode(q, ctypes.byref(cs), 64, 128, B, R, L, W, Hq, Hkv, D, 0.1, out,
+                           ws, ws_bytes, None, None)
+
+
+def test_decode_validation(lib):
+    assert decode_rc(lib, cache(), Hq=30, Hkv=8) == gq.ATTN_ERR_SHAPE       # 30 % 8 != 0
+    assert decode_rc(lib, cache(), D=96) == gq.ATTN_ERR_UNSUPPORTED
+    assert decode_rc(lib, cache(), R=0) == gq.ATTN_ERR_SHAPE
+    assert decode_rc(lib, cache(sps=600)) == gq.ATTN_ERR_SHAPE              # 2*600 > 1024 slots
+    assert decode_rc(lib, cache(), q=None) == gq.ATTN_ERR_NULL
+    assert decode_rc(lib, cache(), q=17) == gq.ATTN_ERR_ALIGN
+    assert decode_rc(lib, cache(k=4100)) == gq.ATTN_ERR_ALIGN
+    # ring: needs a window and ring >= window + q_rows - 1
+    assert decode_rc(lib, cache(gq.RING, sps=512), W=0) == gq.ATTN_ERR_SHAPE
+    assert decode_rc(lib, cache(gq.RING, sps=512), R=4, W=510) == gq.ATTN_ERR_SHAPE
+    # paged: block table required, and the table must span max_seq_len
+    assert decode_rc(lib, cache(gq.PAGED, sps=0, bs=16), L=512) in (gq.ATTN_ERR_SHAPE,
+                                                                    gq.ATTN_ERR_NULL)
+    bt = FakeTensor(1 << 20, (2, 8))
+    assert decode_rc(lib, cache(gq.PAGED, sps=0, bt=bt, bs=16), L=512) == gq.ATTN_ERR_SHAPE
+    # batch 0 is a no-op
+    assert decode_rc(lib, cache(), B=0) == gq.ATTN_OK
+
+
+def test_decode_workspace_checks(lib):
+    c = cache(slots=4096 * 4, sps=4096)
+    cs = c.struct()
+    need = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 4096, 0)
+    assert need > 0 and need != ctypes.c_size_t(-1).value
+    assert decode_rc(lib, c, L=4096, ws=None, ws_bytes=0) == gq.ATTN_ERR_NULL
+    assert decode_rc(lib, c, L=4096, ws=1 << 20, ws_bytes=need - 1) == gq.ATTN_ERR_WORKSPACE
+    bad = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 30, 8, 128, 4096, 0)
+    assert bad == ctypes.c_size_t(-1).value
+
+
+def test_prefill_validation(lib):
+    f = lib.attn_prefill
+    assert f(16, 32, 48, 1, 100, 0, 30, 8, 128, 0.1, 64, None, None) == gq.ATTN_ERR_SHAPE
+    assert f(16, 32, 48, 1, 100, 0, 32, 8, 80, 0.1, 64, None, None) == gq.ATTN_ERR_UNSUPPORTED
+    assert f(None, 32, 48, 1, 100, 0, 32, 8, 128, 0.1, 64, None, None) == gq.ATTN_ERR_NULL
+    assert f(16, 40, 48, 1, 100, 0, 32, 8, 128, 0.1, 72, None, None) == gq.ATTN_ERR_ALIGN
+    assert f(16, 32, 48, 0, 100, 0, 32, 8, 128, 0.1, 64, None, None) == gq.ATTN_OK
+    assert f(16, 32, 48, 1, 0, 0, 32, 8, 128, 0.1, 64, None, None) == gq.ATTN_OK
+
+
+def test_append_validation(lib):
+    c = cache()
+    cs = c.struct()
+    f = lib.attn_kv_append
+    assert f(16, 32, 48, 0, ctypes.byref(cs), 8, 128, None, None) == gq.ATTN_OK   # n = 0
+    assert f(16, 32, 48, -1, ctypes.byref(cs), 8, 128, None, None) == gq.ATTN_ERR_SHAPE
+    assert f(None, 32, 48, 4, ctypes.byref(cs), 8, 128, None, None) == gq.ATTN_ERR_NULL
+    assert f(16, 33, 48, 4, ctypes.byref(cs), 8, 128, None, None) == gq.ATTN_ERR_ALIGN
+    assert f(16, 32, 48, 4, ctypes.byref(cs), 8, 100, None, None) == gq.ATTN_ERR_UNSUPPORTED
+
+
+def test_product_path_does_not_reach_the_oracle():
+    """The binding and the kernels never import the CPU checker."""
+    pkg = os.path.join(ROOT, "gqa_attention_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_oracle" not in text, f

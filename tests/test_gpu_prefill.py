@@ -1,0 +1,89 @@
+"""Prefill parity: the tcgen05 prefill kernel against the fp64 oracle.
+
+Covers on and off every 128-row tile edge (vibevoice.c, "Attention
+backends": prefill on and off every tile edge), head_dim 64 and 128, GQA
+ratios 1, 4 and 7, sliding windows (Voxtral notes, "Offline Encoder"), and
+batches of several sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gqa_attention_kv_gb300 as gq
+from gqa_attention_kv_gb300 import synth
+from helpers import bits, compare
+
+pytestmark = pytest.mark.gpu
+
+
+def run(p, rows=None):
+    dev = "cuda"
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gq.attn_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), p.window, p.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error word {int(err.item())}"
+    rc, ref = oracle.prefill(bits(p.q), bits(p.k), bits(p.v), p.window, p.scale, rows=rows)
+    assert rc == 0
+    if rows is not None:
+        out = out[:, rows]
+    return out, ref
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 127, 128, 129, 255, 256, 257, 300])
+@pytest.mark.parametrize("D", [64, 128])
+def test_tile_edges(T, D):
+    p = synth.prefill_case(100 + T + D, 2, T, 8, 2, D)
+    out, ref = run(p)
+    compare(out, ref, f"T={T} D={D}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (28, 4), (12, 2), (32, 8)])
+def test_gqa_ratios(Hq, Hkv):
+    p = synth.prefill_case(200 + Hq, 1, 400, Hq, Hkv, 128)
+    out, ref = run(p)
+    compare(out, ref, f"{Hq}/{Hkv}")
+
+
+@pytest.mark.parametrize("T,W", [(300, 1), (300, 17), (300, 128), (600, 200), (1000, 750),
+                                 (257, 300)])
+def test_window(T, W):
+    p = synth.prefill_case(300 + W, 1, T, 8, 8, 64, window=W)
+    out, ref = run(p)
+    compare(out, ref, f"T={T} W={W}")
+
+
+def test_encoder_prefill_full():
+    """The speech-encoder shape at full size: T=750, 32 heads, D=64."""
+    p = synth.encoder_prefill()
+    out, ref = run(p)
+    compare(out, ref, "encoder T=750")
+
+
+def test_encoder_prefill_window_full():
+    """The 1,500-frame variant with the 750-frame window."""
+    p = synth.encoder_prefill(long=True)
+    out, ref = run(p)
+    compare(out, ref, "encoder T=1500 W=750")
+
+
+def test_qwen_prompt_sampled_rows():
+    """The 14,449-token Qwen2-7B prompt, checked on sampled rows: every tile
+    edge, the first and last 64 rows and 64 seeded random rows."""
+    p = synth.qwen_prefill()
+    T = p.q.shape[1]
+    edges = [r for t in range(128, T, 128) for r in (t - 1, t)]
+    g = np.random.default_rng(20263)
+    rows = sorted(set(list(range(64)) + list(range(T - 64, T)) + edges[::9] +
+                      g.integers(0, T, 64).tolist()))
+    out, ref = run(p, rows=rows)
+    compare(out, ref, "qwen prompt (sampled rows)")
+
+
+def test_deterministic():
+    p = synth.prefill_case(400, 1, 700, 28, 4, 128)
+    dev = "cuda"
+    a = gq.attn_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), 0, p.scale)
+    b = gq.attn_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), 0, p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
