@@ -1,0 +1,679 @@
+#!/usr/bin/env python3
+"""Throughput of the GQA attention hot path on one GB300 (or N replicas).
+
+One step of the default workload is one pass of the whole path over the
+Qwen2-7B-shaped decoder (28 q / 4 kv heads, head_dim 128, bf16):
+
+  1. causal prefill of a 14,449-token prompt          (attn_prefill)
+  2. KV append of those 14,449 prompt rows            (attn_kv_append)
+  3. five decode steps of 2 slots x 1 row, at contexts 14,449 / 17,623 /
+     20,797 / 23,971 and the mixed pair (14,449, 23,971), each appending its
+     2 new rows first                                  (attn_kv_append + attn_decode)
+
+Printed metric (one JSON line): decode-attention KV GB/s over the step's
+decode launches (``value``), prefill TFLOP/s over its prefill launch
+(``prefill``), both as fractions of the measured HBM / dense-bf16 peaks.
+Inputs are seeded synthetic tensors; decode caches rotate over copies that
+total more than 4x the L2 so every decode reads DRAM; the prefill inputs and
+output (236 MB) exceed the L2 by themselves.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload qwen|voxtral|voxtral-graph|encoder|encoder-long|ring|paged]
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (the oracle is the only reference implementation there is).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# algorithmic work
+# --------------------------------------------------------------------------
+
+def prefill_flops(T, Hq, D, window=0):
+    """4 * D * Hq * (unmasked query-key pairs): QK^T and PV, 2 flops per MAC."""
+    if window and window > 0:
+        pairs = sum(min(i + 1, window) for i in range(T))
+    else:
+        pairs = T * (T + 1) // 2
+    return 4.0 * D * Hq * pairs
+
+
+def decode_bytes(keys_per_request_head, Hkv, D, B, R, Hq, append_rows):
+    """K+V bytes of the valid keys (each KV head read once) + q + out + the
+    appended rows (read + write)."""
+    kv = 2 * 2 * D * Hkv * keys_per_request_head
+    qo = 2 * 2 * B * R * Hq * D
+    app = 2 * 2 * 2 * append_rows * Hkv * D
+    return kv + qo + app
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[4]), parts[5:9]))
+            except ValueError:
+                continue
+        loaded = [r for r in rows if r[2] >= 50.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[0] for r in loaded]) if loaded else None,
+                "sm_max_mhz": max(r[1] for r in rows) if rows else None,
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# --------------------------------------------------------------------------
+# workloads (device side)
+# --------------------------------------------------------------------------
+
+class Workload:
+    """A step = a fixed sequence of library calls.  Subclasses fill ``groups``:
+    a list of (name, callable) that each issue launches on the current stream;
+    events are recorded around every group."""
+
+    name = ""
+    describe = {}
+    launches_per_step = 0
+
+    def decode_bytes_per_step(self):
+        return 0.0
+
+    def prefill_flops_per_step(self):
+        return 0.0
+
+
+def _l2_bytes():
+    import torch
+
+    try:
+        return int(torch.cuda.get_device_properties(0).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+class QwenWorkload(Workload):
+    name = "qwen2-7b prompt prefill 14449 + decode 2x1 at 14449..23971"
+    CONTEXTS = [(14449, 14449), (17623, 17623), (20797, 20797), (23971, 23971), (14449, 23971)]
+
+    def __init__(self, dev):
+        import torch
+
+        import gqa_attention_kv_gb300 as gq
+        from gqa_attention_kv_gb300 import synth
+
+        self.gq, self.torch = gq, torch
+        Hq, Hkv, D = 28, 4, 128
+        self.Hq, self.Hkv, self.D = Hq, Hkv, D
+        self.T = synth.QWEN_PROMPT
+        p = synth.qwen_prefill(device=dev)
+        self.q, self.k, self.v, self.scale = p.q, p.k, p.v, p.scale
+        self.out = torch.empty_like(self.q)
+        self.cap = max(c for pair in self.CONTEXTS for c in pair)
+        self.B = 2
+        # decode caches: enough copies that consecutive decodes never share one
+        # and the copies together exceed 4x the L2
+        per_copy = 2 * self.B * self.cap * Hkv * D * 2
+        self.ncopy = max(6, math.ceil(4 * _l2_bytes() / per_copy) + 1)
+        g = synth.generator(20263 + 5000, dev)
+        self.caches = []
+        for _ in range(self.ncopy):
+            kc = synth.normal_bf16(g, (self.B * self.cap, Hkv, D), dev)
+            vc = synth.normal_bf16(g, (self.B * self.cap, Hkv, D), dev)
+            self.caches.append(gq.KVCache(synth.LINEAR, kc, vc, slots_per_seq=self.cap))
+        self.prompt_slots = torch.arange(self.T, dtype=torch.int64, device=dev)
+        self.dec = []
+        for i, ctx in enumerate(self.CONTEXTS):
+            c = synth.decode_case(20263 + 100 + i, synth.LINEAR, self.B, 1, Hq, Hkv, D, list(ctx),
+                                  slots_per_seq=self.cap, device=dev)
+            self.dec.append({"q": c.q, "k_new": c.k_new, "v_new": c.v_new,
+                             "slots": c.slot_mapping, "seq": c.seq_lens, "pos": c.positions,
+                             "out": torch.empty_like(c.q), "ctx": ctx})
+        self.max_seq = self.cap
+        self.ws = torch.empty(gq.attn_decode_workspace_size(self.caches[0], self.B, 1, Hq,
+                                                            self.max_seq, 0),
+                              dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_i = 0
+        plan_splits = self.ws.numel() > 0
+        self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * (2 + (1 if plan_splits else 0))
+        self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",
+                         "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D,
+                         "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
+                         "decode_contexts": [list(c) for c in self.CONTEXTS],
+                         "cache": "linear", "decode_cache_copies": self.ncopy,
+                         "l2_defeat": "decode caches rotate over copies > 4x L2; prefill "
+                                      "inputs+output 236 MB > L2"}
+
+    def prefill_flops_per_step(self):
+        return prefill_flops(self.T, self.Hq, self.D)
+
+    def decode_bytes_per_step(self):
+        tot = 0.0
+        for d in self.dec:
+            keys = sum(d["ctx"])
+            tot += decode_bytes(keys, self.Hkv, self.D, self.B, 1, self.Hq, self.B)
+        return tot
+
+    def prompt_append_bytes(self):
+        return 2 * 2 * 2 * self.T * self.Hkv * self.D
+
+    def run_step(self, ev):
+        """Issue one step; ev(name) records an event at a boundary."""
+        gq = self.gq
+        s = self.step_i
+        self.step_i += 1
+        ev("prefill")
+        gq.attn_prefill(self.q, self.k, self.v, 0, self.scale, out=self.out, err=self.err)
+        ev("prompt_append")
+        c0 = self.caches[(s * 6) % self.ncopy]
+        gq.attn_kv_append(self.k[0], self.v[0], self.prompt_slots, c0, err=self.err)
+        ev("decode")
+        for i, d in enumerate(self.dec):
+            c = self.caches[(s * 6 + 1 + i) % self.ncopy]
+            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
+            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
+                           out=d["out"], workspace=self.ws, err=self.err)
+        ev("end")
+
+    # end to end through host buffers ---------------------------------------
+    def setup_host(self):
+        torch = self.torch
+        pin = lambda t: t.detach().to("cpu").pin_memory()
+        self.h = {"q": pin(self.q), "k": pin(self.k), "v": pin(self.v),
+                  "out": torch.empty(self.q.shape, dtype=self.q.dtype).pin_memory(),
+                  "dec": [{k: pin(v) for k, v in d.items() if k in
+                           ("q", "k_new", "v_new", "slots", "seq", "pos")} |
+                          {"out": torch.empty(d["q"].shape, dtype=d["q"].dtype).pin_memory()}
+                          for d in self.dec]}
+        self.h2d_prefill = sum(self.h[k].numel() * self.h[k].element_size() for k in "qkv")
+        self.d2h_prefill = self.h["out"].numel() * self.h["out"].element_size()
+        self.h2d_decode = sum(t.numel() * t.element_size() for d in self.h["dec"]
+                              for k, t in d.items() if k != "out")
+        self.d2h_decode = sum(d["out"].numel() * d["out"].element_size() for d in self.h["dec"])
+
+    def run_step_e2e(self, ev):
+        gq = self.gq
+        h = self.h
+        s = self.step_i
+        self.step_i += 1
+        ev("prefill")
+        self.q.copy_(h["q"], non_blocking=True)
+        self.k.copy_(h["k"], non_blocking=True)
+        self.v.copy_(h["v"], non_blocking=True)
+        gq.attn_prefill(self.q, self.k, self.v, 0, self.scale, out=self.out, err=self.err)
+        h["out"].copy_(self.out, non_blocking=True)
+        ev("prompt_append")
+        c0 = self.caches[(s * 6) % self.ncopy]
+        gq.attn_kv_append(self.k[0], self.v[0], self.prompt_slots, c0, err=self.err)
+        ev("decode")
+        for i, (d, hd) in enumerate(zip(self.dec, h["dec"])):
+            for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
+                d[key].copy_(hd[key], non_blocking=True)
+            c = self.caches[(s * 6 + 1 + i) % self.ncopy]
+            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
+            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
+                           out=d["out"], workspace=self.ws, err=self.err)
+            hd["out"].copy_(d["out"], non_blocking=True)
+        ev("end")
+
+
+class DecodeOnlyWorkload(Workload):
+    """A decode step (append + decode) over rotating cache copies."""
+
+    def __init__(self, dev, which):
+        import torch
+
+        import gqa_attention_kv_gb300 as gq
+        from gqa_attention_kv_gb300 import synth
+
+        self.gq, self.torch = gq, torch
+        make = {"voxtral": synth.voxtral_decode_step, "ring": synth.ring_window_decode,
+                "paged": synth.paged_multirow_decode}[which]
+        base = make(device=dev)
+        self.case = base
+        per_copy = 2 * base.k_cache.numel() * 2
+        self.ncopy = max(2, min(256, math.ceil(4 * _l2_bytes() / per_copy) + 1))
+        g = synth.generator(777, dev)
+        self.caches = [gq.KVCache(base.kind, base.k_cache if i == 0 else
+                                  synth.normal_bf16(g, base.k_cache.shape, dev),
+                                  base.v_cache if i == 0 else
+                                  synth.normal_bf16(g, base.v_cache.shape, dev),
+                                  slots_per_seq=base.slots_per_seq,
+                                  block_table=base.block_table, block_size=base.block_size)
+                       for i in range(self.ncopy)]
+        self.max_seq = base.max_seq_len()
+        self.ws = torch.empty(gq.attn_decode_workspace_size(
+            self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window),
+            dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(base.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_i = 0
+        self.launches_per_step = 2 + (1 if self.ws.numel() > 0 else 0)
+        # valid keys per (request, row) summed over rows' union per request
+        seq = base.seq_lens.cpu().tolist()
+        keys = 0
+        for b, L in enumerate(seq):
+            lo = 0
+            pos = base.positions.cpu().view(base.batch, base.q_rows)[b]
+            if base.window > 0:
+                lo = max(lo, int(pos.min()) - base.window + 1)
+            if base.kind == synth.RING:
+                lo = max(lo, L - base.slots_per_seq)
+            keys += L - lo
+        self.keys = keys
+        self.name = {"voxtral": "voxtral decode step B=1 R=1 32/8 D=128 linear 512 keys",
+                     "ring": "ring window decode B=16 32/8 D=128 ring 16384 window 8192",
+                     "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16"}[which]
+        self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
+                         "l2_defeat": "caches rotate over copies > 4x L2"}
+
+    def decode_bytes_per_step(self):
+        c = self.case
+        return decode_bytes(self.keys, c.n_kv_heads, c.head_dim, c.batch, c.q_rows,
+                            c.n_q_heads, c.batch * c.q_rows)
+
+    def run_step(self, ev):
+        c = self.case
+        cache = self.caches[self.step_i % self.ncopy]
+        self.step_i += 1
+        ev("decode")
+        self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
+        self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq, c.window, c.scale,
+                            out=self.out, workspace=self.ws, err=self.err)
+        ev("end")
+
+
+class PrefillOnlyWorkload(Workload):
+    def __init__(self, dev, long):
+        import torch
+
+        import gqa_attention_kv_gb300 as gq
+        from gqa_attention_kv_gb300 import synth
+
+        self.gq = gq
+        # several copies so consecutive launches do not hit a hot L2
+        n = 8
+        self.cases = [synth.encoder_prefill(long=long, device=dev) for _ in range(1)]
+        base = self.cases[0]
+        g = synth.generator(99, dev)
+        self.inputs = [(base.q, base.k, base.v)] + [
+            tuple(synth.normal_bf16(g, t.shape, dev) for t in (base.q, base.k, base.v))
+            for _ in range(n - 1)]
+        self.window, self.scale = base.window, base.scale
+        self.out = torch.empty_like(base.q)
+        B, T, Hq, Hkv, D = base.shape
+        self.T, self.Hq, self.D = T, Hq, D
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_i = 0
+        self.launches_per_step = 1
+        self.name = ("encoder prefill T=1500 window 750 32 heads D=64" if long
+                     else "encoder prefill T=750 32 heads D=64")
+        self.describe = {"workload": self.name, "input_copies": n}
+
+    def prefill_flops_per_step(self):
+        return prefill_flops(self.T, self.Hq, self.D, self.window)
+
+    def run_step(self, ev):
+        q, k, v = self.inputs[self.step_i % len(self.inputs)]
+        self.step_i += 1
+        ev("prefill")
+        self.gq.attn_prefill(q, k, v, self.window, self.scale, out=self.out, err=self.err)
+        ev("end")
+
+
+def make_workload(name, dev):
+    if name == "qwen":
+        return QwenWorkload(dev)
+    if name in ("voxtral", "ring", "paged"):
+        return DecodeOnlyWorkload(dev, name)
+    if name in ("encoder", "encoder-long"):
+        return PrefillOnlyWorkload(dev, name == "encoder-long")
+    raise SystemExit(f"unknown workload {name}")
+
+
+# --------------------------------------------------------------------------
+# timing
+# --------------------------------------------------------------------------
+
+def timed_steps(wl, steps, warmup, stream, e2e=False):
+    """Run warmup + steps; return per-group summed ms over the timed steps and
+    the total ms (events bracketing the timed region)."""
+    import torch
+
+    run = wl.run_step_e2e if e2e else wl.run_step
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run(lambda name: None)
+    torch.cuda.synchronize()
+    marks = []  # per step: list of (name, event)
+
+    def ev_factory(lst):
+        def ev(name):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            lst.append((name, e))
+        return ev
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            lst = []
+            marks.append(lst)
+            run(ev_factory(lst))
+        stop.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(stop)
+    groups = {}
+    for lst in marks:
+        for (name, e0), (_, e1) in zip(lst[:-1], lst[1:]):
+            groups[name] = groups.get(name, 0.0) + e0.elapsed_time(e1)
+    return groups, total
+
+
+def cpu_sample(workload_name, steps=1, warmup=0, budget_s=None, max_rows=160):
+    """The oracle on a bounded sample of the workload, on the host cores.
+    With budget_s, the prefill rows per step shrink so that warmup + steps
+    samples take about budget_s seconds."""
+    import numpy as np
+
+    import oracle
+    from gqa_attention_kv_gb300 import synth
+
+    oracle.build()
+    bits = oracle.bf16_bits
+    res = {"cores": oracle.threads()}
+    if workload_name == "qwen":
+        # decode: both slots at the first context, the whole computation
+        case = synth.qwen_decode((14449, 14449))
+        kc, vc = bits(case.k_cache).copy(), bits(case.v_cache).copy()
+        cd = {"kind": case.kind, "k": kc, "v": vc, "slots_per_seq": case.slots_per_seq}
+        # prefill: 24 seeded query rows of the prompt (all 28 heads)
+        p = synth.qwen_prefill()
+        all_rows = np.random.default_rng(7).integers(0, p.q.shape[1], max_rows).astype(np.int32)
+        pq, pk, pv = bits(p.q), bits(p.k), bits(p.v)
+        dbytes = decode_bytes(sum((14449, 14449)), 4, 128, 2, 1, 28, 2)
+        n_rows = max_rows
+        if budget_s is not None:
+            # calibrate: one decode and a prefill of 8 rows
+            t0 = time.perf_counter()
+            oracle.decode(bits(case.q), cd, case.seq_lens.numpy(), case.positions.numpy(), 0,
+                          case.scale, 4)
+            t1 = time.perf_counter()
+            oracle.prefill(pq, pk, pv, 0, p.scale, rows=all_rows[:8])
+            t2 = time.perf_counter()
+            per_step = budget_s / max(1, steps + warmup)
+            per_row = (t2 - t1) / 8
+            n_rows = int(max(1, min(max_rows, (per_step - (t1 - t0)) / max(per_row, 1e-9))))
+        rows = np.sort(all_rows[:n_rows])
+        pflops = 4.0 * 128 * 28 * float(np.sum(rows.astype(np.int64) + 1))
+
+        def one():
+            t0 = time.perf_counter()
+            oracle.kv_append(kc, vc, bits(case.k_new), bits(case.v_new), case.slot_mapping.numpy())
+            oracle.decode(bits(case.q), cd, case.seq_lens.numpy(), case.positions.numpy(), 0,
+                          case.scale, 4)
+            t1 = time.perf_counter()
+            oracle.prefill(pq, pk, pv, 0, p.scale, rows=rows)
+            t2 = time.perf_counter()
+            return t1 - t0, t2 - t1
+
+        sample = ("decode: 2 slots x 1 row at context 14,449 (all 28 heads, whole "
+                  f"computation); prefill: {len(rows)} seeded query rows x 28 heads of the "
+                  "14,449-token prompt")
+    else:
+        raise SystemExit("cpu sample defined for the qwen workload only")
+    for _ in range(warmup):
+        one()
+    td = tp = 0.0
+    for _ in range(max(1, steps)):
+        a, b = one()
+        td += a
+        tp += b
+    n = max(1, steps)
+    res.update({"decode_gbs": dbytes * n / td / 1e9, "prefill_tflops": pflops * n / tp / 1e12,
+                "decode_s": td / n, "prefill_s": tp / n, "sample": sample})
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen",
+                    choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks, peak_src = load_peaks()
+    metric = "decode-attn KV GB/s (% of HBM peak); prefill-attn TFLOP/s (% bf16 peak)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        r = cpu_sample(args.workload, steps=args.steps, warmup=warmup, budget_s=150.0)
+        line = {"impl": "reference", "metric": metric, "value": round(r["decode_gbs"], 4),
+                "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
+                "ms_per_step": round(1e3 * (r["decode_s"] + r["prefill_s"]), 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": QwenWorkload.name, "sample": r["sample"]},
+                "prefill": {"value": round(r["prefill_tflops"], 6), "unit": "TFLOP/s"},
+                "cpu_baseline": {"value": round(r["decode_gbs"], 4), "unit": "GB/s",
+                                 "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
+                                 "prefill_tflops": round(r["prefill_tflops"], 6)},
+                "e2e": {"value": round(r["decode_gbs"], 4), "unit": "GB/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+
+    import gqa_attention_kv_gb300 as gq
+    from gqa_attention_kv_gb300 import build
+
+    build.build()
+    gq.lib()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.workload, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier()
+    clocks.start()
+    groups, total_ms = timed_steps(wl, args.steps, warmup, stream)
+    barrier()
+    clk = clocks.stop()
+    err = int(wl.err.item())
+    if err != 0:
+        raise SystemExit(f"device error word {err} ({gq.attn_status_string(err)})")
+
+    def reduce_max(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    K = args.steps
+    total_ms = reduce_max(total_ms)
+    dec_ms = reduce_max(groups.get("decode", 0.0))
+    pre_ms = reduce_max(groups.get("prefill", 0.0))
+    app_ms = reduce_max(groups.get("prompt_append", 0.0))
+    dbytes = wl.decode_bytes_per_step()
+    pflops = wl.prefill_flops_per_step()
+    dec_gbs = world * dbytes * K / (dec_ms / 1e3) / 1e9 if dec_ms > 0 else None
+    pre_tf = world * pflops * K / (pre_ms / 1e3) / 1e12 if pre_ms > 0 else None
+
+    e2e = None
+    if not args.no_e2e and hasattr(wl, "run_step_e2e"):
+        wl.setup_host()
+        barrier()
+        eg, etot = timed_steps(wl, K, warmup, stream, e2e=True)
+        barrier()
+        edec = reduce_max(eg.get("decode", 0.0))
+        epre = reduce_max(eg.get("prefill", 0.0))
+        e2e = {"value": round(world * dbytes * K / (edec / 1e3) / 1e9, 2), "unit": "GB/s",
+               "prefill_tflops": round(world * pflops * K / (epre / 1e3) / 1e12, 2),
+               "h2d_bytes_per_step": wl.h2d_prefill + wl.h2d_decode,
+               "d2h_bytes_per_step": wl.d2h_prefill + wl.d2h_decode,
+               "ms_per_step": round(reduce_max(etot) / K, 4)}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+
+    if pre_tf is not None:
+        dominant = "prefill"
+        ach = pflops / (pre_ms / K / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"kernel": "gqa::pre::prefill_kernel<128>", "bound": "tensor",
+                "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    else:
+        dominant = "decode"
+        ach = dbytes / (dec_ms / K / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": "gqa::dec::decode_split_kernel", "bound": "hbm",
+                "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    line = {"metric": metric,
+            "value": round(dec_gbs, 2) if dec_gbs is not None else round(pre_tf, 2),
+            "unit": "GB/s" if dec_gbs is not None else "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": warmup,
+            "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(wl.describe) | {"parallelism": f"replicas x{world}" if world > 1
+                                            else "single GPU"},
+            "step_ms": {"prefill": round(pre_ms / K, 4), "prompt_append": round(app_ms / K, 4),
+                        "decode": round(dec_ms / K, 4)},
+            "roofline": roof, "gpu_launches": wl.launches_per_step * K, "clocks": clk}
+    if dec_gbs is not None:
+        dach = dbytes / (dec_ms / K / 1e3) / 1e9
+        line["decode"] = {"value": round(dec_gbs, 2), "unit": "GB/s",
+                          "bytes_per_step": int(dbytes),
+                          "frac_of_measured_hbm": round(dach / peaks["hbm_gbs"], 4),
+                          "frac_of_nominal_hbm": round(dach / NOMINAL_HBM_GBS, 4)}
+    if pre_tf is not None:
+        line["prefill"] = {"value": round(pre_tf, 2), "unit": "TFLOP/s",
+                           "flops_per_step": pflops,
+                           "frac_of_measured_bf16": round(pre_tf / world / peaks["bf16_tflops"], 4)}
+    if dec_gbs is not None and pre_tf is not None:
+        line["roofline_decode"] = {"bound": "hbm", "achieved": line["decode"]["value"] / world,
+                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": line["decode"]["frac_of_measured_hbm"]}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline and args.workload == "qwen":
+        r = cpu_sample(args.workload, steps=1, warmup=0)
+        line["cpu_baseline"] = {"value": round(r["decode_gbs"], 4), "unit": "GB/s",
+                                "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
+                                "prefill_tflops": round(r["prefill_tflops"], 6)}
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

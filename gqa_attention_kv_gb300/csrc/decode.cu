@@ -23,7 +23,9 @@
 //   * Four consumer warps each own one chunk of every tile: S = Q K^T and
 //     O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
 //     accumulate), the mask and online softmax in fp32 registers with quad
-//     shuffles, exp2 with log2(e) folded into the scale.
+//     shuffles, exp2 with log2(e) folded into the scale.  P enters P V as
+//     two bf16 halves, hi + lo (vibevoice.c, "Attention backends": one
+//     rounding of P is too coarse), so P keeps ~16 bits.
 //   * The four warps' states are merged in shared memory; the CTA writes the
 //     final bf16 row (one split) or an fp32 partial (O / l, m + log2 l).
 #include <cuda.h>
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                         }
                     }
                 }
-                uint32_t pa[MT][4];
+                uint32_t pa[MT][4], pl[MT][4];  // P as bf16 hi + lo
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -408,10 +410,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                             o[mt][n][hr * 2 + 1] *= alpha;
                         }
                     }
-                    pa[mt][0] = pack_bf16x2(s[mt][0][0], s[mt][0][1]);
-                    pa[mt][1] = pack_bf16x2(s[mt][0][2], s[mt][0][3]);
-                    pa[mt][2] = pack_bf16x2(s[mt][1][0], s[mt][1][1]);
-                    pa[mt][3] = pack_bf16x2(s[mt][1][2], s[mt][1][3]);
+                    split_bf16x2(s[mt][0][0], s[mt][0][1], pa[mt][0], pl[mt][0]);
+                    split_bf16x2(s[mt][0][2], s[mt][0][3], pa[mt][1], pl[mt][1]);
+                    split_bf16x2(s[mt][1][0], s[mt][1][1], pa[mt][2], pl[mt][2]);
+                    split_bf16x2(s[mt][1][2], s[mt][1][3], pa[mt][3], pl[mt][3]);
                 }
                 {
                     const int m = lane >> 3;
@@ -424,6 +426,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                         for (int mt = 0; mt < MT; ++mt) {
                             mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
                             mma_bf16_16816(o[mt][dn * 2 + 1], pa[mt], v2, v3);
+                            mma_bf16_16816(o[mt][dn * 2], pl[mt], v0, v1);
+                            mma_bf16_16816(o[mt][dn * 2 + 1], pl[mt], v2, v3);
                         }
                     }
                 }

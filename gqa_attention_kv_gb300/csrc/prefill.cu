@@ -18,7 +18,9 @@
 //                tile j so the tensor core works while the softmax runs.
 //   warps 2..5   softmax: thread = query row = TMEM lane.  Reads its S row
 //                with tcgen05.ld, masks, keeps the running max / sum in fp32,
-//                writes P (bf16) into a swizzled shared tile, and rescales
+//                writes P into swizzled shared tiles as two bf16 halves,
+//                hi + lo (vibevoice.c, "Attention backends": one rounding of
+//                P is too coarse; PV then runs once per half), and rescales
 //                its O row in TMEM only when the running max grew by more
 //                than 2^8 (the result is the same; rescaling is lazy).
 //                At the end: O / l -> bf16 -> shared -> TMA store.
@@ -39,6 +41,7 @@ constexpr int kThreads = 192;     // 6 warps
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kPLo = kBM * kBN * 2;        // byte offset of the P lo tile after P hi
 
 template <int HD>
 struct Cfg {
@@ -47,7 +50,7 @@ struct Cfg {
     static constexpr int kQBytes = kBM * HD * 2;
     static constexpr int kKBytes = kBN * HD * 2;
     static constexpr int kVBytes = kBN * HD * 2;
-    static constexpr int kPBytes = kBM * kBN * 2;
+    static constexpr int kPBytes = 2 * kBM * kBN * 2;  // P as bf16 hi + lo
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffP = kOffKV + kStages * (kKBytes + kVBytes);
@@ -189,12 +192,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = j % C::kStages;
                 const uint32_t v_addr = smem_u32(sKV + st * (C::kKBytes + C::kVBytes) + C::kKBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t a =
-                        smem_desc_sw128(p_addr + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-                    // V tile: keys are rows (K), head_dim contiguous (N): MN-major.
-                    const uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, kBN * 128, 1024);
-                    tc_mma_ss(tmem_o, a, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int part = 0; part < 2; ++part) {  // P hi, then P lo
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t a = smem_desc_sw128(
+                            p_addr + part * kPLo + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+                        // V tile: keys are rows (K), head_dim contiguous (N): MN-major.
+                        const uint64_t bdesc =
+                            smem_desc_sw128(v_addr + kk * 16 * 128, kBN * 128, 1024);
+                        tc_mma_ss(tmem_o, a, bdesc, idesc_pv,
+                                  (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                    }
                 }
                 tc_commit(o_ready);
                 tc_commit(&kv_empty[st]);
@@ -253,13 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mref = m_use == -INFINITY ? 0.f : m_use;
             float sum = 0.f;
-            uint32_t pk[kBN / 2];
+            uint32_t pk[kBN / 2], pl[kBN / 2];
 #pragma unroll
             for (int c = 0; c < kBN; c += 2) {
                 const float p0 = fast_exp2(s[c] - mref);
                 const float p1 = fast_exp2(s[c + 1] - mref);
                 sum += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
+                split_bf16x2(p0, p1, pk[c / 2], pl[c / 2]);
             }
             l_run = l_run * alpha + sum;
             m_run = m_use;
@@ -288,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *dst = sP + half * (kBM * 128) + row * 128 + ((c8 ^ (row & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) =
                     make_uint4(pk[cc * 4 + 0], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+                *reinterpret_cast<uint4 *>(dst + kPLo) =
+                    make_uint4(pl[cc * 4 + 0], pl[cc * 4 + 1], pl[cc * 4 + 2], pl[cc * 4 + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();

@@ -174,6 +174,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Split two fp32 values into bf16 hi + lo pairs (hi = round(x), lo =
+// round(x - hi)), so a product with hi + lo carries ~16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<uint32_t *>(&h);
+    lo = *reinterpret_cast<uint32_t *>(&l);
+}
+
 // 2^x via the MUFU base-2 exponential (approximate, flushes denormals).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

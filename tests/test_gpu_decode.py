@@ -55,7 +55,7 @@ def test_paged_block_sizes(D, block_size):
 def test_multirow_paged(R, Hq, Hkv):
     """K sequential query rows causal among themselves; rows x group spans
     one 16-row tile, two, or several row blocks."""
-    case = synth.decode_case(4000 + R * Hq, PAGED, 5, R, Hq, Hkv, 128, [64, 100, 4, 1030, 517],
+    case = synth.decode_case(4000 + R * Hq, PAGED, 5, R, Hq, Hkv, 128, [64, 100, max(R, 4), 1030, 517],
                              block_size=16)
     ref, _, _ = oracle_decode(case)
     out, _ = gpu_decode(case)
