@@ -18,7 +18,8 @@ total more than 4x the L2 so every decode reads DRAM; the prefill inputs and
 output (236 MB) exceed the L2 by themselves.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload qwen|voxtral|voxtral-graph|encoder|encoder-long|ring|paged]
+                  [--workload qwen|voxtral|encoder|encoder-long|ring|paged|
+                              qwen-prefill|prefill-8k]
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload (the oracle is the only reference implementation there is).
@@ -228,6 +229,37 @@ class QwenWorkload(Workload):
     def prompt_append_bytes(self):
         return 2 * 2 * 2 * self.T * self.Hkv * self.D
 
+    def _decode_part(self, s, e2e=False):
+        gq = self.gq
+        for i, d in enumerate(self.dec):
+            if e2e:
+                hd = self.h["dec"][i]
+                for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
+                    d[key].copy_(hd[key], non_blocking=True)
+            c = self.caches[(s * 6 + 1 + i) % self.ncopy]
+            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
+            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
+                           out=d["out"], workspace=self.ws, err=self.err)
+            if e2e:
+                self.h["dec"][i]["out"].copy_(d["out"], non_blocking=True)
+
+    def capture(self, stream, e2e=False):
+        """One CUDA graph of the decode part per cache-rotation index (the
+        launches are identical from step to step, as a serving engine replays
+        them; vibevoice.c, 'The decode step is one submission')."""
+        torch = self.torch
+        graphs = []
+        for r in range(self.ncopy):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self._decode_part(r, e2e)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        if e2e:
+            self.graphs_e2e = graphs
+        else:
+            self.graphs = graphs
+
     def run_step(self, ev):
         """Issue one step; ev(name) records an event at a boundary."""
         gq = self.gq
@@ -239,11 +271,10 @@ class QwenWorkload(Workload):
         c0 = self.caches[(s * 6) % self.ncopy]
         gq.attn_kv_append(self.k[0], self.v[0], self.prompt_slots, c0, err=self.err)
         ev("decode")
-        for i, d in enumerate(self.dec):
-            c = self.caches[(s * 6 + 1 + i) % self.ncopy]
-            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
-            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
-                           out=d["out"], workspace=self.ws, err=self.err)
+        if getattr(self, "graphs", None):
+            self.graphs[s % self.ncopy].replay()
+        else:
+            self._decode_part(s)
         ev("end")
 
     # end to end through host buffers ---------------------------------------
@@ -277,14 +308,10 @@ class QwenWorkload(Workload):
         c0 = self.caches[(s * 6) % self.ncopy]
         gq.attn_kv_append(self.k[0], self.v[0], self.prompt_slots, c0, err=self.err)
         ev("decode")
-        for i, (d, hd) in enumerate(zip(self.dec, h["dec"])):
-            for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
-                d[key].copy_(hd[key], non_blocking=True)
-            c = self.caches[(s * 6 + 1 + i) % self.ncopy]
-            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
-            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
-                           out=d["out"], workspace=self.ws, err=self.err)
-            hd["out"].copy_(d["out"], non_blocking=True)
+        if getattr(self, "graphs_e2e", None):
+            self.graphs_e2e[s % self.ncopy].replay()
+        else:
+            self._decode_part(s, e2e=True)
         ev("end")
 
 
@@ -332,40 +359,71 @@ class DecodeOnlyWorkload(Workload):
                 lo = max(lo, L - base.slots_per_seq)
             keys += L - lo
         self.keys = keys
-        self.name = {"voxtral": "voxtral decode step B=1 R=1 32/8 D=128 linear 512 keys",
+        # one step = one decode per decoder layer, each layer its own cache
+        # (Voxtral decoder: 26 layers); bigger workloads: one layer per step
+        self.layers = 26 if which == "voxtral" else 1
+        self.launches_per_step *= self.layers
+        self.name = {"voxtral": "voxtral decode step B=1 R=1 32/8 D=128 linear 512 keys, "
+                                "26 layers",
                      "ring": "ring window decode B=16 32/8 D=128 ring 16384 window 8192",
                      "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16"}[which]
         self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
+                         "layers_per_step": self.layers,
                          "l2_defeat": "caches rotate over copies > 4x L2"}
 
     def decode_bytes_per_step(self):
         c = self.case
-        return decode_bytes(self.keys, c.n_kv_heads, c.head_dim, c.batch, c.q_rows,
-                            c.n_q_heads, c.batch * c.q_rows)
+        return self.layers * decode_bytes(self.keys, c.n_kv_heads, c.head_dim, c.batch,
+                                          c.q_rows, c.n_q_heads, c.batch * c.q_rows)
+
+    def _decode_part(self, s):
+        c = self.case
+        for layer in range(self.layers):
+            cache = self.caches[(s * self.layers + layer) % self.ncopy]
+            self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
+            self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq, c.window,
+                                c.scale, out=self.out, workspace=self.ws, err=self.err)
+
+    def capture(self, stream, e2e=False):
+        torch = self.torch
+        period = self.ncopy // math.gcd(self.ncopy, self.layers)
+        self.graphs = []
+        for r in range(period):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self._decode_part(r)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
 
     def run_step(self, ev):
-        c = self.case
-        cache = self.caches[self.step_i % self.ncopy]
+        s = self.step_i
         self.step_i += 1
         ev("decode")
-        self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
-        self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq, c.window, c.scale,
-                            out=self.out, workspace=self.ws, err=self.err)
+        if getattr(self, "graphs", None):
+            self.graphs[s % len(self.graphs)].replay()
+        else:
+            self._decode_part(s)
         ev("end")
 
 
 class PrefillOnlyWorkload(Workload):
-    def __init__(self, dev, long):
+    def __init__(self, dev, which):
         import torch
 
         import gqa_attention_kv_gb300 as gq
         from gqa_attention_kv_gb300 import synth
 
         self.gq = gq
-        # several copies so consecutive launches do not hit a hot L2
-        n = 8
-        self.cases = [synth.encoder_prefill(long=long, device=dev) for _ in range(1)]
-        base = self.cases[0]
+        if which == "encoder":
+            base = synth.encoder_prefill(device=dev)
+        elif which == "encoder-long":
+            base = synth.encoder_prefill(long=True, device=dev)
+        elif which == "qwen-prefill":
+            base = synth.qwen_prefill(device=dev)
+        else:  # prefill-8k: the Qwen shape at 8,192 tokens (inputs + output > L2)
+            base = synth.prefill_case(20263, 1, 8192, 28, 4, 128, device=dev)
+        # several input copies so consecutive launches do not hit a hot L2
+        n = 8 if which.startswith("encoder") else 1
         g = synth.generator(99, dev)
         self.inputs = [(base.q, base.k, base.v)] + [
             tuple(synth.normal_bf16(g, t.shape, dev) for t in (base.q, base.k, base.v))
@@ -377,8 +435,10 @@ class PrefillOnlyWorkload(Workload):
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
         self.launches_per_step = 1
-        self.name = ("encoder prefill T=1500 window 750 32 heads D=64" if long
-                     else "encoder prefill T=750 32 heads D=64")
+        self.name = {"encoder": "encoder prefill T=750 32 heads D=64",
+                     "encoder-long": "encoder prefill T=1500 window 750 32 heads D=64",
+                     "qwen-prefill": "qwen2-7b prompt prefill T=14449 28/4 D=128",
+                     "prefill-8k": "qwen2-7b-shaped prefill T=8192 28/4 D=128"}[which]
         self.describe = {"workload": self.name, "input_copies": n}
 
     def prefill_flops_per_step(self):
@@ -397,8 +457,8 @@ def make_workload(name, dev):
         return QwenWorkload(dev)
     if name in ("voxtral", "ring", "paged"):
         return DecodeOnlyWorkload(dev, name)
-    if name in ("encoder", "encoder-long"):
-        return PrefillOnlyWorkload(dev, name == "encoder-long")
+    if name in ("encoder", "encoder-long", "qwen-prefill", "prefill-8k"):
+        return PrefillOnlyWorkload(dev, name)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -416,6 +476,11 @@ def timed_steps(wl, steps, warmup, stream, e2e=False):
         for _ in range(warmup):
             run(lambda name: None)
     torch.cuda.synchronize()
+    if hasattr(wl, "capture"):
+        wl.capture(stream, e2e=e2e)
+        with torch.cuda.stream(stream):
+            run(lambda name: None)  # one replay before timing
+        torch.cuda.synchronize()
     marks = []  # per step: list of (name, event)
 
     def ev_factory(lst):
@@ -515,7 +580,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen",
-                    choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged"])
+                    choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged",
+                             "qwen-prefill", "prefill-8k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -623,7 +689,8 @@ def main():
         dominant = "prefill"
         ach = pflops / (pre_ms / K / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
-        roof = {"kernel": "gqa::pre::prefill_kernel<128>", "bound": "tensor",
+        roof = {"kernel": f"gqa::pre::prefill_kernel<{getattr(wl, 'D', 128)}>",
+                "bound": "tensor",
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "traffic": None,
                 "peak_source": f"{peak_src} bf16_tflops (burst)"}
