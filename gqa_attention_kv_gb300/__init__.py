@@ -181,3 +181,29 @@ def attn_prefill(q, k, v, window, scale, out=None, err=None, stream=None):
                             float(scale), _ptr(out), _ptr(err), _stream(stream))
     _check(rc, "attn_prefill")
     return out
+
+
+def attn_decode_noalloc(q, cache: KVCache, seq_lens, positions, max_seq_len, window, scale,
+                        out=None, err=None, stream=None):
+    """attn_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed scratch array
+    (ATTN_DECODE_NOALLOC_SCRATCH_BYTES per GPU).  Calls that overlap on the
+    GPU share that array and race; order them on one stream."""
+    import torch
+
+    L = lib()
+    f = L.attn_decode_noalloc
+    if f.restype is not ctypes.c_int:
+        p, i32 = ctypes.c_void_p, ctypes.c_int
+        f.argtypes = [p, ctypes.POINTER(_Cache), p, p, i32, i32, i32, i32, i32, i32, i32,
+                      ctypes.c_float, p, p, p]
+        f.restype = i32
+    B, R, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    c = cache.struct()
+    rc = f(_ptr(q), ctypes.byref(c), _ptr(seq_lens), _ptr(positions), B, R, int(max_seq_len),
+           int(window), Hq, cache.n_kv_heads, D, float(scale), _ptr(out), _ptr(err),
+           _stream(stream))
+    _check(rc, "attn_decode_noalloc")
+    return out

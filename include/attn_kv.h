@@ -173,6 +173,33 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
                 attn_stream_t stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to it.
+ *
+ * attn_decode asks the caller for scratch space.  A caller that has no device
+ * allocator (it receives only its input and output tensors from its host), or
+ * that must never call cudaMalloc in its decode loop (an allocation can
+ * synchronise the whole device), calls this instead: same arguments without
+ * the workspace; the scratch is a fixed device array of
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU
+ * that loads the library until the process exits.  Nothing is allocated.
+ *
+ *   Returns ATTN_ERR_WORKSPACE, before any launch, when
+ *   attn_decode_workspace_size(...) for these arguments exceeds that size;
+ *   otherwise the same statuses as attn_decode.
+ *   The first call on a device looks up the array's device address; make it
+ *   before capturing a stream into a CUDA graph.
+ *   All calls share the array: calls whose kernels overlap on the GPU race
+ *   and give wrong results, so order them (one stream, or events).  No part
+ *   of the array has to start at zero.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int attn_decode_noalloc(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
+                        const int32_t *positions, int batch, int q_rows, int max_seq_len,
+                        int window, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                        void *out, int32_t *err_word, attn_stream_t stream);
+
+/*
  * attn_prefill -- causal GQA self-attention over whole sequences.
  *
  * Source: vibevoice.c, "Prefill attention" and "Attention backends" (causal

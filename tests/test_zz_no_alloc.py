@@ -1,0 +1,89 @@
+"""attn_decode_noalloc: the decode entry point for callers that cannot allocate.
+
+Callers without a device allocator of their own, or that must not call
+cudaMalloc inside their decode loop, use attn_decode_noalloc: it takes no
+workspace and uses the library's fixed scratch array instead.  Its answers must
+match attn_decode's (which uses caller scratch) within the parity tolerance,
+on two calls in a row (the second call finds the first call's leftovers in the
+shared array).
+
+This file is named so that pytest collects it last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import gqa_attention_kv_gb300 as gq
+from gqa_attention_kv_gb300 import synth
+from helpers import MAX_ABS, REL_L2
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_via_cabi(q, cache, seq, pos, max_seq, window, scale, out, err):
+    """Call the C entry point directly, with ctypes, on the current stream."""
+    f = gq.lib().attn_decode_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.POINTER(gq._Cache), ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    B, R, Hq, D = q.shape
+    c = cache.struct()
+    rc = f(q.data_ptr(), ctypes.byref(c), seq.data_ptr(), pos.data_ptr(), B, R, max_seq, window,
+           Hq, cache.n_kv_heads, D, scale, out.data_ptr(), err.data_ptr(),
+           torch.cuda.current_stream().cuda_stream)
+    return rc
+
+
+def _close(a, b):
+    a = a.double()
+    b = b.double()
+    max_abs = float((a - b).abs().max())
+    rel = float((a - b).norm() / b.norm())
+    return max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+
+
+def test_noalloc_matches_attn_decode_twice():
+    dev = "cuda"
+    case = synth.decode_case(9101, synth.PAGED, 8, 4, 32, 8, 128,
+                             [4096, 1500, 37, 2049, 700, 4, 3333, 128], block_size=16)
+    cache = gq.KVCache(case.kind, case.k_cache.to(dev), case.v_cache.to(dev),
+                       block_table=case.block_table.to(dev), block_size=case.block_size)
+    gq.attn_kv_append(case.k_new.to(dev), case.v_new.to(dev), case.slot_mapping.to(dev), cache)
+    q, seq, pos = case.q.to(dev), case.seq_lens.to(dev), case.positions.to(dev)
+    max_seq = case.max_seq_len()
+    need = gq.attn_decode_workspace_size(cache, 8, 4, 32, max_seq, 0)
+    assert 0 < need <= (32 << 20), "the case must use the scratch and fit in it"
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    want = gq.attn_decode(q, cache, seq, pos, max_seq, 0, case.scale, err=err)
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        rc = _noalloc_via_cabi(q, cache, seq, pos, max_seq, 0, case.scale, out, err)
+        assert rc == gq.ATTN_OK, gq.attn_status_string(rc)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ok, (max_abs, rel) = _close(out.cpu(), want.cpu())
+        assert ok, f"call {call}: max-abs {max_abs:.3e} rel-L2 {rel:.3e}"
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    dev = "cuda"
+    # 1024 requests x 8 KV heads over 32k keys needs more partial state than
+    # the fixed array holds: refused before any launch.
+    k = torch.zeros(16, 8, 128, dtype=torch.bfloat16, device=dev)
+    cache = gq.KVCache(synth.LINEAR, k, k, slots_per_seq=16)
+    big = gq.KVCache(synth.PAGED, k, k,
+                     block_table=torch.zeros(1024, 2048, dtype=torch.int32, device=dev),
+                     block_size=16)
+    need = gq.attn_decode_workspace_size(big, 1024, 4, 32, 32768, 0)
+    assert need > (32 << 20)
+    q = torch.zeros(1024, 4, 32, 128, dtype=torch.bfloat16, device=dev)
+    seq = torch.full((1024,), 16, dtype=torch.int32, device=dev)
+    pos = torch.zeros(4096, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = _noalloc_via_cabi(q, big, seq, pos, 32768, 0, 0.1, out, err)
+    assert rc == gq.ATTN_ERR_WORKSPACE
+    del cache
