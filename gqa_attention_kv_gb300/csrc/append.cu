@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
                                                         uint4 *__restrict__ v_cache,
                                                         int64_t num_slots, int pieces_per_row,
                                                         int32_t *err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t per_row = 2ll * pieces_per_row;
     const int64_t total = n * per_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -51,10 +53,11 @@ int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_m
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+    const cudaError_t e = launch_pdl(
+        kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, n,
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots, pieces, err);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace gqa

@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     const int row0 = rb * RB;
     const int row1 = min(p.rows, row0 + RB);
 
+    pdl_wait();  // the cache, positions and seq_lens may come from the previous kernel
+    pdl_launch_dependents();
     const SplitRange sr = split_range(p, b, row0, row1, split, threadIdx.x == 0 && split == 0);
     const int n_chunks = sr.c_end - sr.c_begin;
     const int n_tiles = (n_chunks + kWarps - 1) / kWarps;
@@ -515,48 +517,81 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     __syncthreads();  // producer's side of barrier (1)
 }
 
-// Merge the splits' partial states: one warp per (request, query row, head).
+// Merge the splits' partial states.  One CTA per (request, KV head, query
+// row of the group); its warps take the splits round-robin, each keeping an
+// online (max, sum, output) state, and the warps' states are combined in a
+// fixed order, so the result does not depend on timing.
+constexpr int kMergeWarps = 8;
+
 template <int HD, int RB>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const Params p) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int total = p.batch * p.rows * p.n_kv_heads;
-    if (warp >= total) return;
-    const int b = warp / (p.rows * p.n_kv_heads);
-    const int rem = warp - b * p.rows * p.n_kv_heads;
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Params p) {
+    constexpr int PER = HD / 32;
+    __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
+    __shared__ __align__(16) float sm_o[kMergeWarps][HD];
+    pdl_wait();  // the partial states come from the split kernel
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int b = cta / (p.rows * p.n_kv_heads);
+    const int rem = cta - b * p.rows * p.n_kv_heads;
     const int kvh = rem / p.rows;
     const int i = rem - kvh * p.rows;
     const int rb = i / RB, row = i - rb * RB;
     const int64_t unit = ((int64_t)b * p.n_kv_heads + kvh) * p.row_blocks + rb;
     const int64_t base = unit * p.nsplit * RB + row;  // slot of split s: base + s*RB
-    float M = -INFINITY;
-    for (int s = lane; s < p.nsplit; s += 32) M = fmaxf(M, p.ws_lse[base + (int64_t)s * RB]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    constexpr int PER = HD / 32;
+    float m = -INFINITY, l = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int s = warp; s < p.nsplit; s += kMergeWarps) {
+        const int64_t slot = base + (int64_t)s * RB;
+        const float lse = p.ws_lse[slot];
+        float v[PER];
+        const float *src = p.ws_o + slot * HD + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            v[0] = t.x; v[1] = t.y;
+        }
+        if (lse == -INFINITY) continue;
+        if (lse > m) {
+            const float f = fast_exp2(m - lse);
+            l *= f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] *= f;
+            m = lse;
+        }
+        const float f = fast_exp2(lse - m);
+        l += f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += f * v[e];
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) sm_o[warp][lane * PER + e] = acc[e];
+    __syncthreads();
+    if (warp != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm_m[w]);
     float L = 0.f;
+    float o[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < p.nsplit; ++s) {
-            const int64_t slot = base + (int64_t)s * RB;
-            const float lse = p.ws_lse[slot];
-            if (lse == -INFINITY) continue;
-            const float f = fast_exp2(lse - M);
-            L += f;
-            const float *src = p.ws_o + slot * HD + lane * PER;
-            if constexpr (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] += f * v.x;
-                acc[1] += f * v.y;
-                acc[2] += f * v.z;
-                acc[3] += f * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] += f * v.x;
-                acc[1] += f * v.y;
-            }
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            if (sm_m[w] == -INFINITY) continue;
+            const float f = fast_exp2(sm_m[w] - M);
+            L += f * sm_l[w];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) o[e] += f * sm_o[w][lane * PER + e];
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -565,11 +600,11 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const Params p) {
         p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + lane * PER;
     if constexpr (PER == 4) {
         uint2 packed;
-        packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        packed.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+        packed.y = pack_bf16x2(o[2] * inv, o[3] * inv);
         *reinterpret_cast<uint2 *>(dst) = packed;
     } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
     }
 }
 
@@ -597,13 +632,13 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
         configured_device = dev;
     }
     dim3 grid(p.nsplit, p.n_kv_heads * p.row_blocks, p.batch);
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_pdl(kern, grid, dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     if (p.nsplit > 1) {
-        const int64_t warps = (int64_t)p.batch * p.rows * p.n_kv_heads;
-        const int blocks = (int)((warps * 32 + 255) / 256);
-        decode_merge_kernel<HD, 16 * MT><<<blocks, 256, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
+        if (launch_pdl(decode_merge_kernel<HD, 16 * MT>, dim3(ctas), dim3(kMergeWarps * 32), 0,
+                       stream, p) != cudaSuccess)
+            return ATTN_ERR_CUDA;
     }
     return ATTN_OK;
 }

@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();  // q, k, v may come from the previous kernel; out may be read by it
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_s0 = tmem, tmem_s1 = tmem + 128, tmem_o = tmem + 256;
 
@@ -359,8 +360,10 @@ int launch(const Params &p, const CUtensorMap &tq, const CUtensorMap &tk, const 
         configured_device = dev;
     }
     const unsigned grid = (unsigned)p.n_qtiles * p.n_q_heads * p.batch;
-    kern<<<grid, kThreads, Cfg<HD>::kSmem, stream>>>(tq, tk, tv, to, p);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg<HD>::kSmem, stream, tq, tk, tv, to,
+                      p) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
 }
 
 }  // namespace pre

@@ -86,6 +86,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return true;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Block until the grids this one depends on have completed and their memory
+// is visible.  Every kernel of the library calls it before touching memory a
+// previous kernel on the stream may write or read.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream to begin launching (it still waits in
+// pdl_wait until this grid completes).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
