@@ -32,8 +32,11 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
+        extra = ""
+        if status == 7:  # ATTN_ERR_CUDA
+            extra = f": {lib().attn_last_cuda_error().decode()}"
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
-                         f"({attn_status_string(status)})")
+                         f"({attn_status_string(status)}{extra})")
 
 
 class _Cache(ctypes.Structure):
@@ -68,6 +71,7 @@ def lib():
             L.attn_status_string.argtypes = [i32]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_version.restype = ctypes.c_char_p
+            L.attn_last_cuda_error.restype = ctypes.c_char_p
             _lib = L
     return _lib
 

@@ -12,6 +12,15 @@
 
 namespace gqa {
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+void note_cuda_error(cudaError_t e) {
+    g_last_cuda_error = e;
+    cudaGetLastError();  // launch errors are not sticky; clear the runtime's copy
+}
+
+cudaError_t last_cuda_error() { return g_last_cuda_error; }
+
 int device_sm_count() {
     static std::atomic<int> counts[64];
     int dev = 0;
@@ -199,5 +208,9 @@ const char *attn_status_string(int status) {
 }
 
 const char *attn_version(void) { return "gqa_attention_kv_gb300 0.1.0 (sm_103a)"; }
+
+const char *attn_last_cuda_error(void) {
+    return cudaGetErrorString(gqa::last_cuda_error());
+}
 
 }  // extern "C"

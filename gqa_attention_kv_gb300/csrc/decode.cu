@@ -626,9 +626,12 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
             return ATTN_ERR_CUDA;
+        }
         configured_device = dev;
     }
     dim3 grid(p.nsplit, p.n_kv_heads * p.row_blocks, p.batch);

@@ -11,6 +11,10 @@ namespace gqa {
 
 int device_sm_count();
 
+// The last CUDA runtime error a launch in this thread ran into (cudaSuccess if
+// none); attn_last_cuda_error() reports it to the caller.
+void note_cuda_error(cudaError_t e);
+
 // Launch with programmatic stream serialisation: the kernel may begin while
 // its predecessor on the stream finishes; it must call pdl_wait() before
 // touching memory the predecessor writes.
@@ -27,7 +31,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+    if (e != cudaSuccess) note_cuda_error(e);
+    return e;
 }
 
 // Encode a 2D/3D bf16 tensor map with 128-byte swizzle (returns false on failure).

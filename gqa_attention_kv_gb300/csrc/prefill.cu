@@ -20,7 +20,8 @@
 //                 S_a = Q_a K^T            M=128 N=128 K=D   A, B from smem
 //                 O_a += P_a V (hi, lo)    M=128 N=D   K=128 A from TMEM
 //               TMEM columns: S_a/P_a at 128a, O_a at 256 + D a.
-//   warps 2..5  softmax for Q0, warps 6..9 for Q1.  Thread = query row = TMEM
+//   warps 2..3  idle (they complete the first warpgroup).
+//   warps 4..7  softmax for Q0, warps 8..11 for Q1.  Thread = query row = TMEM
 //               lane.  tcgen05.ld of its S row, mask (only on tiles that
 //               cross the diagonal or the window edge), running max / sum in
 //               fp32, P written back over its S columns as two bf16 halves
@@ -47,7 +48,14 @@ namespace pre {
 
 constexpr int kBM = 128;          // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 320;     // 10 warps
+constexpr int kThreads = 384;     // 3 warpgroups
+// Registers: launched at 168 per thread (384 x 168 = 64,512; three warps of
+// 168 fit one SM sub-partition's 16,384).  The TMA/MMA warpgroup then drops
+// to 56 and the two softmax warpgroups rise to 224: 4x32x56 + 8x32x224 =
+// 64,512, exactly the launch total, and 56 + 224 + 224 <= 512 per
+// sub-partition lane slot.
+constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsSoftmax = 224;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -75,7 +83,7 @@ struct Params {
 };
 
 template <int HD>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const Params p) {
@@ -140,6 +148,10 @@ __global__ void __maxnreg__(200)
     pdl_wait();  // q, k, v may come from the previous kernel; out may be read by it
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    // Each role's registers are set inside its own branch: code after a join
+    // of different setmaxnreg values is compiled for the smaller one.
+    setmaxnreg_dec<kRegsControl>();
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -245,9 +257,11 @@ __global__ void __maxnreg__(200)
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, p.err);
         }
+    }
     } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // ---------------------------------------------------------- softmax
-        const int a = (warp - 2) >> 2;        // which query tile
+        const int a = (warp - 4) >> 2;        // which query tile
         const int quad = warp & 3;            // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;     // row inside the tile
         const int qa0 = q0 + a * kBM;
@@ -388,9 +402,12 @@ int launch(const Params &p, const CUtensorMap &tq, const CUtensorMap &tk, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)Cfg<HD>::kSmem) != cudaSuccess)
+        const cudaError_t e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<HD>::kSmem);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
             return ATTN_ERR_CUDA;
+        }
         configured_device = dev;
     }
     const unsigned grid = (unsigned)p.n_pairs * p.n_q_heads * p.batch;

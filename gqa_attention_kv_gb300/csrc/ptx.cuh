@@ -86,6 +86,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return true;
 }
 
+// ------------------------------------------------------ register reallocation
+// Every warp of a warpgroup executes these together.  The launch's register
+// total must cover the sum of the warpgroups' new shares.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------- programmatic dependent launch
 // Block until the grids this one depends on have completed and their memory
 // is visible.  Every kernel of the library calls it before touching memory a

@@ -224,6 +224,10 @@ const char *attn_status_string(int status);
 /* Library version string. */
 const char *attn_version(void);
 
+/* Text of the last CUDA runtime error that made a call of this thread return
+ * ATTN_ERR_CUDA ("no error" if there was none). */
+const char *attn_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
