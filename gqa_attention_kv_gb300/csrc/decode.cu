@@ -4,33 +4,41 @@
 // backends"; talker_multiframe, NarrowStep fields; Voxtral Realtime notes,
 // "Encoder KV cache"): for every request b, query row r and query head h,
 // softmax(scale * q . k_t) over the valid key positions t, applied to v_t.
-// The keys of each request are cut into splits; each split keeps an online
-// softmax state (running max m, sum l, output O) and a second kernel merges
-// the splits' states.  Both are exact reformulations of the softmax.
+// The keys of each (request, KV head) are cut into pieces; each piece keeps
+// an online softmax state (running max m, sum l, output O) and the pieces'
+// states are merged in a fixed order.  Both are exact reformulations.
 //
 // GB300 mapping:
-//   * One CTA = (split, KV head, row block, request).  All query rows of the
-//     GQA group (q_rows x group rows, padded to 16 or 32) are the M dimension
-//     of one mma.sync tile, so every cache position is read from HBM once for
-//     the whole group.
-//   * A producer warp streams the split's keys in tiles of 64 positions (four
-//     16-position chunks) into a multi-stage shared-memory ring.  A chunk
+//   * Work unit = (request, KV head, row block): all query rows of the GQA
+//     group (q_rows x group, padded to 16 or 32) are the M dimension of one
+//     mma.sync tile, so every cache position is read from HBM once per group.
+//   * The kernel is persistent: one CTA per SM.  Every CTA computes, from the
+//     device-side seq_lens and positions, how many 16-key chunks each unit
+//     needs, and takes an equal contiguous share of all units' chunks laid end
+//     to end.  The share is balanced whatever the lengths are (ragged batches
+//     included), and each CTA streams its share through one deep TMA ring,
+//     paying the pipeline ramp once.  A CTA's share covers pieces ("segments")
+//     of one or more units; a unit wholly inside one CTA is written straight
+//     to the output, the others leave fp32 partial states in the workspace
+//     for the merge kernel.
+//   * A producer warp streams 64-key tiles (four 16-key chunks).  A chunk
 //     whose 16 slots are consecutive (linear cache; a page of >= 16 slots; a
 //     ring away from its wrap point) is one 2D TMA box per 64 columns, landing
 //     128-byte-swizzled; any other chunk is gathered row by row with 16-byte
-//     cp.async into the same swizzled layout.  Completion is tracked by an
-//     mbarrier per stage (TMA bytes + one arrival per producer lane).
+//     cp.async into the same layout.  Page ids are fetched 32 at a time, one
+//     per lane, ahead of the tiles that use them.
 //   * Four consumer warps each own one chunk of every tile: S = Q K^T and
 //     O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
 //     accumulate), the mask and online softmax in fp32 registers with quad
-//     shuffles, exp2 with log2(e) folded into the scale.  P enters P V as
-//     two bf16 halves, hi + lo (vibevoice.c, "Attention backends": one
-//     rounding of P is too coarse), so P keeps ~16 bits.
-//   * The four warps' states are merged in shared memory; the CTA writes the
-//     final bf16 row (one split) or an fp32 partial (O / l, m + log2 l).
+//     shuffles, exp2 with log2(e) folded into the scale.  P enters P V as two
+//     bf16 halves, hi + lo (vibevoice.c, "Attention backends": one rounding
+//     of P is too coarse), so P keeps ~16 bits.  At the end of a segment the
+//     four warps merge through shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <algorithm>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -38,13 +46,11 @@
 namespace gqa {
 namespace dec {
 
-constexpr int kChunk = 16;                        // key positions per chunk
-constexpr int kWarps = 4;                         // consumer warps = chunks per tile
-constexpr int kThreads = (kWarps + 1) * 32;       // + one producer warp
+constexpr int kChunk = 16;                   // key positions per chunk
+constexpr int kWarps = 4;                    // consumer warps = chunks per tile
+constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
-constexpr int kMaxStagedPages = 512;              // page-table entries staged per CTA
-constexpr int kMaxChunksPerSplit = 256;
-constexpr int kStages = 3;
+constexpr int kMaxTableEntries = 1024;       // (request, row block) pairs per launch
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -58,22 +64,36 @@ struct Params {
     int max_blocks;
     const int32_t *seq_lens;
     const int32_t *positions;
-    int batch, q_rows, n_q_heads, n_kv_heads, group, rows;
+    int batch;   // requests in this launch
+    int b_base;  // index of this launch's first request (linear / ring slot arithmetic)
+    int q_rows, n_q_heads, n_kv_heads, group, rows;
     int window, max_seq_len;
     float scale_log2;
-    int nsplit, row_blocks;
+    int row_blocks;
+    int grid;  // CTAs of the split kernel
     __nv_bfloat16 *out;
     float *ws_o;
     float *ws_lse;
+    int32_t *ws_meta;  // [0] = total chunks N; [1 .. B+1] = Pb; then cnt[B * row_blocks]
     int32_t *err;
 };
 
-template <int HD>
+template <int HD, int MT>
 struct Geo {
+    static constexpr int RB = 16 * MT;                       // rows per unit
     static constexpr int kHalves = HD / 64;                 // 128-byte column blocks
     static constexpr int kChunkBytes = kHalves * kChunk * 128;
     static constexpr int kTileBytes = kWarps * kChunkBytes;  // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kMergeBytes = kWarps * RB * HD * 4 + 2 * kWarps * RB * 4;
+    static constexpr int kStages = HD == 128 ? (MT == 1 ? 5 : 4) : (MT == 1 ? 10 : 9);
+    static constexpr int kOffMerge = kStages * kStageBytes;
+    static constexpr int kOffBars = kOffMerge + kMergeBytes;
+    static constexpr int kOffInfo = kOffBars + 2 * kStages * 8;
+    static constexpr int kOffTable = kOffInfo + 2 * kStages * kWarps * 4;
+    // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
+    static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
+    static constexpr size_t kSmem = 1024 + kOffTable + kTableBytes;
 };
 
 // Byte offset of 16-byte piece `c16` (0 .. HD/8-1) of row `row` inside a chunk
@@ -83,16 +103,10 @@ __device__ __forceinline__ uint32_t chunk_offset(int row, int c16) {
     return (uint32_t)(half * (kChunk * 128) + row * 128 + ((cc ^ (row & 7)) << 4));
 }
 
-struct SplitRange {
-    int seq_len;
-    int ring_lo;
-    int c_begin, c_end;  // chunk range of this CTA
-};
-
-// Key range of this CTA's split.  Chunk c covers positions 16c .. 16c+15.
-__device__ __forceinline__ SplitRange split_range(const Params &p, int b, int row0, int row1,
-                                                  int split, bool report) {
-    SplitRange s;
+// Key chunk range of unit (request b, row block rb): chunk c covers positions
+// 16c .. 16c+15.  Also returns the request's effective seq_len.
+__device__ __forceinline__ void unit_range(const Params &p, int b, int rb, int &c_lo, int &c_hi,
+                                           int &seq_len_out, bool report) {
     int seq_len = p.seq_lens[b];
     if (seq_len > p.max_seq_len || seq_len < 0 ||
         (p.kind == ATTN_CACHE_LINEAR && seq_len > p.slots_per_seq)) {
@@ -100,62 +114,104 @@ __device__ __forceinline__ SplitRange split_range(const Params &p, int b, int ro
         seq_len = max(0, min(seq_len, p.max_seq_len));
         if (p.kind == ATTN_CACHE_LINEAR) seq_len = min(seq_len, p.slots_per_seq);
     }
+    seq_len_out = seq_len;
+    const int RB = p.rows <= 16 ? 16 : 32;
+    const int row0 = rb * RB, row1 = min(p.rows, row0 + RB);
     int pmin = INT32_MAX, pmax = -1;
     for (int r = row0 / p.group; r <= (row1 - 1) / p.group; ++r) {
         const int pos = p.positions[(int64_t)b * p.q_rows + r];
         pmin = min(pmin, pos);
         pmax = max(pmax, pos);
     }
-    int hi = min(seq_len, pmax + 1);
+    const int hi = min(seq_len, pmax + 1);
     int lo = 0;
     if (p.window > 0) lo = max(lo, pmin - p.window + 1);
-    s.ring_lo = 0;
-    if (p.kind == ATTN_CACHE_RING) {
-        s.ring_lo = seq_len - p.slots_per_seq;
-        lo = max(lo, s.ring_lo);
-    }
-    s.seq_len = seq_len;
+    if (p.kind == ATTN_CACHE_RING) lo = max(lo, seq_len - p.slots_per_seq);
     if (pmin < 0 || hi <= lo) {
-        s.c_begin = s.c_end = 0;
-        return s;
+        c_lo = c_hi = 0;
+        return;
     }
-    const int c0 = lo / kChunk, c1 = (hi + kChunk - 1) / kChunk;
-    const int per = (c1 - c0 + p.nsplit - 1) / p.nsplit;
-    s.c_begin = min(c1, c0 + split * per);
-    s.c_end = min(c1, s.c_begin + per);
-    return s;
+    c_lo = lo / kChunk;
+    c_hi = (hi + kChunk - 1) / kChunk;
 }
 
+// Shared tables every CTA builds: per (request, row block) chunk count and
+// first chunk, per request effective seq_len, and Pb[b] = chunks of all
+// units of requests before b (units ordered (request, KV head, row block)).
+struct Tables {
+    int *cnt, *clo, *seqlen, *Pb;
+};
+
+// One contiguous piece of one unit's chunks handled by this CTA.
+struct Segment {
+    int b, kvh, rb;
+    int c_begin, c_end;  // chunk range inside the unit's key range
+    int unit;
+    bool whole;          // the piece is the whole unit
+};
+
+// The segments of global chunk range [g, g_end), in order.
+struct SegmentWalker {
+    int g, g_end;
+    __device__ bool next(const Params &p, const Tables &t, Segment &s) {
+        if (g >= g_end) return false;
+        const int B = p.batch, RBc = p.row_blocks;
+        // request: the largest b with Pb[b] <= g (requests with no chunks are skipped)
+        int lo = 0, hi = B;  // invariant: Pb[lo] <= g < Pb[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (t.Pb[mid] <= g)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int b = lo;
+        const int per_head = (t.Pb[b + 1] - t.Pb[b]) / p.n_kv_heads;
+        int off = g - t.Pb[b];
+        const int kvh = off / per_head;
+        off -= kvh * per_head;
+        int rb = 0;
+        while (off >= t.cnt[b * RBc + rb]) off -= t.cnt[b * RBc + rb++];
+        const int n_u = t.cnt[b * RBc + rb];
+        const int unit_start = g - off;
+        const int seg_end = min(g_end, unit_start + n_u);
+        s.b = b;
+        s.kvh = kvh;
+        s.rb = rb;
+        s.c_begin = t.clo[b * RBc + rb] + off;
+        s.c_end = s.c_begin + (seg_end - g);
+        s.unit = (b * p.n_kv_heads + kvh) * RBc + rb;
+        s.whole = (off == 0 && seg_end == unit_start + n_u);
+        g = seg_end;
+        return true;
+    }
+};
+
 template <int HD, int MT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    using G = Geo<HD>;
-    constexpr int RB = 16 * MT;  // rows per CTA
+    using G = Geo<HD, MT>;
+    constexpr int RB = G::RB;
+    constexpr int kStages = G::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stages + kStages * G::kStageBytes);
+    float *mo = reinterpret_cast<float *>(smem + G::kOffMerge);  // [kWarps][RB][HD]
+    float *mm = mo + kWarps * RB * HD;                           // [kWarps][RB]
+    float *ml = mm + kWarps * RB;                                // [kWarps][RB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::kOffBars);
     uint64_t *empty = full + kStages;
-    int *info_t0 = reinterpret_cast<int *>(empty + kStages);       // [kStages][kWarps]
+    int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
     uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
-    int *pages = reinterpret_cast<int *>(info_mask + kStages * kWarps);  // [kMaxStagedPages]
+    Tables tb;
+    tb.cnt = reinterpret_cast<int *>(smem + G::kOffTable);
+    tb.clo = tb.cnt + kMaxTableEntries;
+    tb.seqlen = tb.clo + kMaxTableEntries;
+    tb.Pb = tb.seqlen + kMaxTableEntries;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y / p.row_blocks;
-    const int rb = blockIdx.y - kvh * p.row_blocks;
-    const int b = blockIdx.z;
-    const int row0 = rb * RB;
-    const int row1 = min(p.rows, row0 + RB);
-
-    pdl_wait();  // the cache, positions and seq_lens may come from the previous kernel
-    pdl_launch_dependents();
-    const SplitRange sr = split_range(p, b, row0, row1, split, threadIdx.x == 0 && split == 0);
-    const int n_chunks = sr.c_end - sr.c_begin;
-    const int n_tiles = (n_chunks + kWarps - 1) / kWarps;
-
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 32);       // one arrival per producer lane (+ TMA bytes)
@@ -163,7 +219,47 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         }
         fence_barrier_init();
     }
+    pdl_wait();  // the cache, positions and seq_lens may come from the previous kernel
+    pdl_launch_dependents();
+
+    // ---- tables: chunk counts of every (request, row block), then Pb
+    const int B = p.batch, RBc = p.row_blocks;
+    for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
+        const int b = i / RBc, rb = i - (i / RBc) * RBc;
+        int clo, chi, sl;
+        unit_range(p, b, rb, clo, chi, sl, blockIdx.x == 0 && rb == 0);
+        tb.cnt[i] = chi - clo;
+        tb.clo[i] = clo;
+        if (rb == 0) tb.seqlen[b] = sl;
+    }
     __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        if (lane == 0) tb.Pb[0] = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int b = base + lane;
+            int v = 0;
+            if (b < B)
+                for (int rb = 0; rb < RBc; ++rb) v += tb.cnt[b * RBc + rb];
+            v *= p.n_kv_heads;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += n;
+            }
+            if (b < B) tb.Pb[b + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+    const int N = tb.Pb[B];
+    const int L = max(1, (N + p.grid - 1) / p.grid);
+    if (blockIdx.x == 0) {  // for the merge kernel
+        for (int i = threadIdx.x; i <= B; i += kThreads) p.ws_meta[1 + i] = tb.Pb[i];
+        for (int i = threadIdx.x; i < B * RBc; i += kThreads) p.ws_meta[2 + B + i] = tb.cnt[i];
+        if (threadIdx.x == 0) p.ws_meta[0] = N;
+    }
+    const int g0 = min(N, (int)blockIdx.x * L), g1 = min(N, g0 + L);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -172,145 +268,180 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             prefetch_tensormap(&tm_v);
         }
         const bool paged = p.kind == ATTN_CACHE_PAGED;
-        int page0 = 0;
-        bool staged = false;
-        if (paged && n_chunks > 0) {
-            page0 = (sr.c_begin * kChunk) / p.block_size;
-            const int page1 = (sr.c_end * kChunk - 1) / p.block_size;
-            const int np = page1 - page0 + 1;
-            staged = np <= kMaxStagedPages;
-            if (staged) {
-                const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks;
-                for (int i = lane; i < np; i += 32) {
-                    const int pi = page0 + i;
-                    pages[i] = pi < p.max_blocks ? bt[pi] : -1;
-                }
-            }
-            __syncwarp();
-        }
+        const bool paged_tma = paged && (p.block_size % kChunk == 0);
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
-        auto page_of = [&](int t) -> int64_t {  // page id holding position t, or -1
-            const int pi = t / p.block_size;
-            if (pi >= p.max_blocks) return -1;
-            const int v = staged ? pages[pi - page0]
-                                 : p.block_table[(int64_t)b * p.max_blocks + pi];
-            return (v < 0 || v >= num_pages) ? -1 : (int64_t)v;
-        };
-        // slot of position t, or -1 if it is out of bounds
-        auto slot_of = [&](int t) -> int64_t {
-            int64_t s;
-            if (p.kind == ATTN_CACHE_LINEAR) {
-                s = (int64_t)b * p.slots_per_seq + t;
-            } else if (paged) {
-                const int64_t pg = page_of(t);
-                if (pg < 0) return -1;
-                s = pg * p.block_size + t % p.block_size;
-            } else {
-                s = (int64_t)b * p.slots_per_seq + t % p.slots_per_seq;
-            }
-            return (s >= 0 && s < p.num_slots) ? s : -1;
-        };
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
+        SegmentWalker walk{g0, g1};
+        Segment sg;
+        int tile = 0;  // tiles issued by this CTA (stage / phase counter)
         bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            const int st = it % kStages;
-            if (it >= kStages) ok = mbar_wait(&empty[st], ((it / kStages) - 1) & 1, p.err);
-            if (!ok) break;
-            uint8_t *kst = stages + st * G::kStageBytes;
-            uint8_t *vst = kst + G::kTileBytes;
-            // Describe the tile's chunks: a chunk whose 16 slots are
-            // consecutive starts at slot0[c] >= 0 (one TMA box per 64
-            // columns); slot0[c] == -1 marks a contiguous chunk whose page is
-            // out of bounds (the box is aimed outside the tensor, zero-filled,
-            // and its keys masked); slot0[c] == -2 is gathered row by row.
-            int64_t slot0[kWarps];
-            uint32_t tma_bytes = 0;
-            bool issued_cp = false;
-#pragma unroll
-            for (int c = 0; c < kWarps; ++c) {
-                const int chunk = sr.c_begin + it * kWarps + c;
-                slot0[c] = -3;  // absent
-                if (chunk >= sr.c_end) {
-                    if (lane == 0) info_t0[st * kWarps + c] = -1;
-                    continue;
-                }
-                const int t0 = chunk * kChunk;
-                int64_t s0 = -2;
+        while (ok && walk.next(p, tb, sg)) {
+            const int bg = p.b_base + sg.b;  // request index in the whole cache
+            const int32_t *bt = paged ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
+            // page id holding position t (or -1), read straight from the table
+            auto page_of = [&](int t) -> int64_t {
+                const int pi = t / p.block_size;
+                if (pi >= p.max_blocks) return -1;
+                const int v = bt[pi];
+                return (v < 0 || v >= num_pages) ? -1 : (int64_t)v;
+            };
+            auto slot_of = [&](int t) -> int64_t {
+                int64_t s;
                 if (p.kind == ATTN_CACHE_LINEAR) {
-                    s0 = (int64_t)b * p.slots_per_seq + t0;
+                    s = (int64_t)bg * p.slots_per_seq + t;
                 } else if (paged) {
-                    if (p.block_size % kChunk == 0) {
-                        const int64_t pg = page_of(t0);
-                        s0 = pg < 0 ? -1 : pg * p.block_size + t0 % p.block_size;
-                    }
+                    const int64_t pg = page_of(t);
+                    if (pg < 0) return -1;
+                    s = pg * p.block_size + t % p.block_size;
                 } else {
-                    const int j0 = t0 % p.slots_per_seq;
-                    if (j0 + kChunk <= p.slots_per_seq) s0 = (int64_t)b * p.slots_per_seq + j0;
+                    s = (int64_t)bg * p.slots_per_seq + t % p.slots_per_seq;
                 }
-                slot0[c] = s0;
-                uint32_t mask;
-                if (s0 != -2) {
-                    mask = 0xFFFFu;
-                    if (s0 == -1) {
-                        mask = 0;
-                        if (t0 < sr.seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
-                    }
-                    tma_bytes += 2 * G::kChunkBytes;
-                } else {
-                    mask = 0;
-                    for (int r = 0; r < kChunk; ++r) {
-                        const int64_t s = slot_of(t0 + r);
-                        if (s >= 0) mask |= 1u << r;
-                        else if (t0 + r < sr.seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
-                    }
-                    if (lane != 0) {
-                        // lanes 1..31 gather the chunk's K and V rows
-                        constexpr int kPieces = kChunk * (HD / 8);
-                        for (int pc = lane - 1; pc < 2 * kPieces; pc += 31) {
-                            const int tensor = pc / kPieces;
-                            const int rem = pc - tensor * kPieces;
-                            const int r = rem / (HD / 8), c16 = rem % (HD / 8);
-                            int64_t s = slot_of(t0 + r);
-                            if (s < 0) s = 0;  // masked row: read any valid slot
-                            const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
-                                                       s * row_elems + (int64_t)kvh * HD + c16 * 8;
-                            uint8_t *dst =
-                                (tensor ? vst : kst) + c * G::kChunkBytes + chunk_offset(r, c16);
-                            cp_async_16(dst, src);
-                            issued_cp = true;
+                return (s >= 0 && s < p.num_slots) ? s : -1;
+            };
+            const int seq_len = tb.seqlen[sg.b];
+            const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
+            int win_base = -1;  // page index held by lane 0 of the prefetch window
+            int pg_reg = -1;
+            for (int it = 0; it < n_tiles && ok; ++it, ++tile) {
+                const int st = tile % kStages;
+                if (tile >= kStages) ok = mbar_wait(&empty[st], ((tile / kStages) - 1) & 1, p.err);
+                if (!ok) break;
+                uint8_t *kst = stages + st * G::kStageBytes;
+                uint8_t *vst = kst + G::kTileBytes;
+                const int chunk0 = sg.c_begin + it * kWarps;
+                if (paged_tma) {
+                    // refill the per-lane page-id window when this tile leaves it
+                    const int last = min(sg.c_end, chunk0 + kWarps) - 1;
+                    const int pi_first = chunk0 * kChunk / p.block_size;
+                    const int pi_last = last * kChunk / p.block_size;
+                    if (win_base < 0 || pi_last >= win_base + 32) {
+                        win_base = pi_first;
+                        const int pi = win_base + lane;
+                        pg_reg = -1;
+                        if (pi < p.max_blocks) {
+                            const int v = bt[pi];
+                            pg_reg = (v < 0 || v >= num_pages) ? -1 : v;
                         }
                     }
                 }
-                if (lane == 0) {
-                    info_t0[st * kWarps + c] = t0;
-                    info_mask[st * kWarps + c] = mask;
-                }
-            }
-            if (lane == 0) {
-                if (tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
+                // Describe the tile's chunks: slot0[c] >= 0 is the first of 16
+                // consecutive slots (one TMA box per 64 columns); -1 marks a
+                // contiguous chunk whose page is out of bounds (the box is
+                // aimed outside the tensor, zero-filled, keys masked); -2 is
+                // gathered row by row; -3 is absent.
+                int64_t slot0[kWarps];
+                uint32_t tma_bytes = 0;
+                bool issued_cp = false;
 #pragma unroll
                 for (int c = 0; c < kWarps; ++c) {
-                    if (slot0[c] < -1) continue;
-                    const int y = slot0[c] < 0 ? -kChunk : (int)slot0[c];
-#pragma unroll
-                    for (int h = 0; h < G::kHalves; ++h) {
-                        const int x = kvh * HD + h * 64;
-                        tma_load_2d(kst + c * G::kChunkBytes + h * kChunk * 128, &tm_k, x, y,
-                                    &full[st]);
-                        tma_load_2d(vst + c * G::kChunkBytes + h * kChunk * 128, &tm_v, x, y,
-                                    &full[st]);
+                    const int chunk = chunk0 + c;
+                    const int t0 = chunk * kChunk;
+                    int pv = -1;
+                    if (paged_tma) {  // every lane takes part in the shuffle
+                        const int pi = t0 / p.block_size;
+                        pv = __shfl_sync(0xffffffffu, pg_reg, (pi - win_base) & 31);
+                    }
+                    int64_t s0 = -3;
+                    if (chunk < sg.c_end) {
+                        if (p.kind == ATTN_CACHE_LINEAR) {
+                            s0 = (int64_t)bg * p.slots_per_seq + t0;
+                        } else if (paged_tma) {
+                            s0 = pv < 0 ? -1 : (int64_t)pv * p.block_size + t0 % p.block_size;
+                        } else if (paged) {
+                            s0 = -2;
+                        } else {
+                            const int j0 = t0 % p.slots_per_seq;
+                            s0 = (j0 + kChunk <= p.slots_per_seq)
+                                     ? (int64_t)bg * p.slots_per_seq + j0
+                                     : -2;
+                        }
+                    }
+                    slot0[c] = s0;
+                    if (s0 == -3) {
+                        if (lane == 0) info_t0[st * kWarps + c] = -1;
+                        continue;
+                    }
+                    uint32_t mask;
+                    if (s0 != -2) {
+                        mask = 0xFFFFu;
+                        if (s0 == -1) {
+                            mask = 0;
+                            if (t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
+                        }
+                        tma_bytes += 2 * G::kChunkBytes;
+                    } else {
+                        mask = 0;
+                        for (int r = 0; r < kChunk; ++r) {
+                            const int64_t s = slot_of(t0 + r);
+                            if (s >= 0)
+                                mask |= 1u << r;
+                            else if (t0 + r < seq_len)
+                                report_error(p.err, ATTN_ERR_BOUNDS);
+                        }
+                        if (lane != 0) {
+                            // lanes 1..31 gather the chunk's K and V rows
+                            constexpr int kPieces = kChunk * (HD / 8);
+                            for (int pc = lane - 1; pc < 2 * kPieces; pc += 31) {
+                                const int tensor = pc / kPieces;
+                                const int rem = pc - tensor * kPieces;
+                                const int r = rem / (HD / 8), c16 = rem % (HD / 8);
+                                int64_t s = slot_of(t0 + r);
+                                if (s < 0) s = 0;  // masked row: read any valid slot
+                                const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
+                                                           s * row_elems + (int64_t)sg.kvh * HD +
+                                                           c16 * 8;
+                                uint8_t *dst = (tensor ? vst : kst) + c * G::kChunkBytes +
+                                               chunk_offset(r, c16);
+                                cp_async_16(dst, src);
+                                issued_cp = true;
+                            }
+                        }
+                    }
+                    if (lane == 0) {
+                        info_t0[st * kWarps + c] = t0;
+                        info_mask[st * kWarps + c] = mask;
                     }
                 }
-                mbar_arrive(&full[st]);
-            } else if (issued_cp) {
-                cp_async_arrive_noinc(&full[st]);
-            } else {
-                mbar_arrive(&full[st]);
+                if (lane == 0) {
+                    if (tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
+#pragma unroll
+                    for (int c = 0; c < kWarps; ++c) {
+                        if (slot0[c] < -1) continue;
+                        const int y = slot0[c] < 0 ? -kChunk : (int)slot0[c];
+#pragma unroll
+                        for (int h = 0; h < G::kHalves; ++h) {
+                            const int x = sg.kvh * HD + h * 64;
+                            tma_load_2d(kst + c * G::kChunkBytes + h * kChunk * 128, &tm_k, x, y,
+                                        &full[st]);
+                            tma_load_2d(vst + c * G::kChunkBytes + h * kChunk * 128, &tm_v, x, y,
+                                        &full[st]);
+                        }
+                    }
+                    mbar_arrive(&full[st]);
+                } else if (issued_cp) {
+                    cp_async_arrive_noinc(&full[st]);
+                } else {
+                    mbar_arrive(&full[st]);
+                }
             }
         }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const int gq = lane >> 2, tq = lane & 3;
+        // the gathered rows of this thread must land before it leaves
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int gq = lane >> 2, tq = lane & 3;
+    const int ctid = threadIdx.x;  // 0 .. 127
+    SegmentWalker walk{g0, g1};
+    Segment sg;
+    int tile = 0;
+    bool ok = true;
+    while (ok && walk.next(p, tb, sg)) {
+        const int b = sg.b, kvh = sg.kvh;
+        const int row0 = sg.rb * RB;
+        const int row1 = min(p.rows, row0 + RB);
         uint32_t qa[MT][HD / 16][4];
         int rpos[MT][2];
 #pragma unroll
@@ -338,32 +469,38 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             m_run[mt][0] = m_run[mt][1] = -INFINITY;
             l_run[mt][0] = l_run[mt][1] = 0.f;
 #pragma unroll
-            for (int n = 0; n < HD / 8; ++n) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
+            for (int n = 0; n < HD / 8; ++n)
+                o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
         }
-        const int seq_len = sr.seq_len, ring_lo = sr.ring_lo, window = p.window;
-        bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-            const int st = it % kStages;
-            ok = mbar_wait(&full[st], (it / kStages) & 1, p.err);
+        const int seq_len = tb.seqlen[b];
+        const int ring_lo = p.kind == ATTN_CACHE_RING ? seq_len - p.slots_per_seq : 0;
+        const int window = p.window;
+        const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
+        for (int it = 0; it < n_tiles; ++it, ++tile) {
+            const int st = tile % kStages;
+            ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
             __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
             if (!ok) break;
             const int t0 = info_t0[st * kWarps + warp];
             if (t0 >= 0) {
                 const uint32_t mask16 = info_mask[st * kWarps + warp];
-                const uint32_t kbase = smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
+                const uint32_t kbase =
+                    smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
                 const uint32_t vbase = kbase + G::kTileBytes;
                 float s[MT][2][4];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) s[mt][j][0] = s[mt][j][1] = s[mt][j][2] = s[mt][j][3] = 0.f;
+                    for (int j = 0; j < 2; ++j)
+                        s[mt][j][0] = s[mt][j][1] = s[mt][j][2] = s[mt][j][3] = 0.f;
                 {
                     const int m = lane >> 3;
                     const int key = (m >> 1) * 8 + (lane & 7);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         uint32_t b00, b01, b10, b11;
-                        ldmatrix_x4(b00, b01, b10, b11, kbase + chunk_offset(key, kk * 2 + (m & 1)));
+                        ldmatrix_x4(b00, b01, b10, b11,
+                                    kbase + chunk_offset(key, kk * 2 + (m & 1)));
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
                             mma_bf16_16816(s[mt][0], qa[mt][kk], b00, b01);
@@ -384,9 +521,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                             for (int e = 0; e < 2; ++e) {
                                 const int n = j * 8 + tq * 2 + e;
                                 const int t = t0 + n;
-                                const bool valid = ((mask16 >> n) & 1u) && t < seq_len && t <= pos &&
-                                                   t >= ring_lo && (window <= 0 || pos - t < window);
-                                const float v = valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
+                                const bool valid = ((mask16 >> n) & 1u) && t < seq_len &&
+                                                   t <= pos && t >= ring_lo &&
+                                                   (window <= 0 || pos - t < window);
+                                const float v =
+                                    valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
                                 s[mt][j][hr * 2 + e] = v;
                                 mx = fmaxf(mx, v);
                             }
@@ -423,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 #pragma unroll
                     for (int dn = 0; dn < HD / 16; ++dn) {
                         uint32_t v0, v1, v2, v3;
-                        ldmatrix_x4_trans(v0, v1, v2, v3, vbase + chunk_offset(key, dn * 2 + (m >> 1)));
+                        ldmatrix_x4_trans(v0, v1, v2, v3,
+                                          vbase + chunk_offset(key, dn * 2 + (m >> 1)));
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
                             mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
@@ -437,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
-        // quad-reduce the row sums
+        // ---- end of segment: merge the four warps through shared memory
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -447,11 +587,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                 l += __shfl_xor_sync(0xffffffffu, l, 2);
                 l_run[mt][hr] = l;
             }
-        __syncwarp();
-        __syncthreads();  // (1) all stages consumed: the stage memory is free
-        float *mo = reinterpret_cast<float *>(stages);          // [kWarps][RB][HD]
-        float *mm = mo + kWarps * RB * HD;                       // [kWarps][RB]
-        float *ml = mm + kWarps * RB;                            // [kWarps][RB]
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -459,18 +595,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                 const int row = mt * 16 + gq + hr * 8;
                 float *dst = mo + ((size_t)warp * RB + row) * HD;
 #pragma unroll
-                for (int n = 0; n < HD / 8; ++n) {
+                for (int n = 0; n < HD / 8; ++n)
                     *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
                         make_float2(o[mt][n][hr * 2], o[mt][n][hr * 2 + 1]);
-                }
                 if (tq == 0) {
                     mm[warp * RB + row] = m_run[mt][hr];
                     ml[warp * RB + row] = l_run[mt][hr];
                 }
             }
-        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // consumers only
-        // combine the four warps and write the CTA's result
-        const int ctid = threadIdx.x;  // 0 .. 127
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
             const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
             const int i = row0 + row;
@@ -478,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * RB + row]);
-            float L = 0.f;
+            float Lsum = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (M != -INFINITY) {
 #pragma unroll
@@ -486,41 +619,41 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                     const float mw = mm[w * RB + row];
                     if (mw == -INFINITY) continue;
                     const float f = fast_exp2(mw - M);
-                    L += ml[w * RB + row] * f;
-                    const float4 v = *reinterpret_cast<const float4 *>(mo + ((size_t)w * RB + row) * HD + d);
+                    Lsum += ml[w * RB + row] * f;
+                    const float4 v =
+                        *reinterpret_cast<const float4 *>(mo + ((size_t)w * RB + row) * HD + d);
                     acc.x += f * v.x;
                     acc.y += f * v.y;
                     acc.z += f * v.z;
                     acc.w += f * v.w;
                 }
             }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const int r = i / p.group, g = i - (i / p.group) * p.group;
-            if (p.nsplit == 1) {
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            if (sg.whole) {
+                const int r = i / p.group, g = i - (i / p.group) * p.group;
                 __nv_bfloat16 *dst =
-                    p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + d;
+                    p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD +
+                    d;
                 uint2 packed;
                 packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                 packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
                 *reinterpret_cast<uint2 *>(dst) = packed;
             } else {
-                const int64_t unit = ((int64_t)b * p.n_kv_heads + kvh) * p.row_blocks + rb;
-                const int64_t slot = (unit * p.nsplit + split) * RB + row;
+                // partial slot (unit, this CTA): unit + blockIdx.x is unique
+                const int64_t slot = ((int64_t)sg.unit + blockIdx.x) * RB + row;
                 *reinterpret_cast<float4 *>(p.ws_o + slot * HD + d) =
                     make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                if (d == 0) p.ws_lse[slot] = L > 0.f ? M + __log2f(L) : -INFINITY;
+                if (d == 0) p.ws_lse[slot] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
             }
         }
-        return;
     }
-    __syncwarp();
-    __syncthreads();  // producer's side of barrier (1)
 }
 
-// Merge the splits' partial states.  One CTA per (request, KV head, query
-// row of the group); its warps take the splits round-robin, each keeping an
-// online (max, sum, output) state, and the warps' states are combined in a
-// fixed order, so the result does not depend on timing.
+// Merge: one CTA per (request, KV head, query row of the group).  Units whose
+// chunks lie inside one CTA were written by the split kernel; units with no
+// valid key get zeros; the others combine the partial states of the CTAs
+// they span (slots unit + cta), warps taking them round-robin and the warps'
+// states combined in a fixed order, so the result does not depend on timing.
 constexpr int kMergeWarps = 8;
 
 template <int HD, int RB>
@@ -528,7 +661,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     constexpr int PER = HD / 32;
     __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
     __shared__ __align__(16) float sm_o[kMergeWarps][HD];
-    pdl_wait();  // the partial states come from the split kernel
+    pdl_wait();  // the partial states and tables come from the split kernel
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -537,24 +670,49 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int kvh = rem / p.rows;
     const int i = rem - kvh * p.rows;
     const int rb = i / RB, row = i - rb * RB;
-    const int64_t unit = ((int64_t)b * p.n_kv_heads + kvh) * p.row_blocks + rb;
-    const int64_t base = unit * p.nsplit * RB + row;  // slot of split s: base + s*RB
+    const int B = p.batch, RBc = p.row_blocks;
+    const int N = p.ws_meta[0];
+    const int *Pb = p.ws_meta + 1;
+    const int *cnt = p.ws_meta + 2 + B;
+    const int per_head = (Pb[b + 1] - Pb[b]) / p.n_kv_heads;
+    int start = Pb[b] + kvh * per_head;
+    for (int r2 = 0; r2 < rb; ++r2) start += cnt[b * RBc + r2];
+    const int n_u = cnt[b * RBc + rb];
+    const int L = max(1, (N + p.grid - 1) / p.grid);
+    const int r = i / p.group, g = i - r * p.group;
+    __nv_bfloat16 *dst =
+        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + lane * PER;
+    if (n_u == 0) {  // no valid key: zeros
+        if (warp == 0) {
+            if constexpr (PER == 4)
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
+            else
+                *reinterpret_cast<uint32_t *>(dst) = 0u;
+        }
+        return;
+    }
+    const int first = start / L, last = (start + n_u - 1) / L;
+    if (first == last) return;  // written by the split kernel
+    const int unit = (b * p.n_kv_heads + kvh) * RBc + rb;
     float m = -INFINITY, l = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int s = warp; s < p.nsplit; s += kMergeWarps) {
-        const int64_t slot = base + (int64_t)s * RB;
+    for (int c = first + warp; c <= last; c += kMergeWarps) {
+        const int64_t slot = ((int64_t)unit + c) * RB + row;
         const float lse = p.ws_lse[slot];
         float v[PER];
         const float *src = p.ws_o + slot * HD + lane * PER;
         if constexpr (PER == 4) {
             const float4 t = *reinterpret_cast<const float4 *>(src);
-            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+            v[0] = t.x;
+            v[1] = t.y;
+            v[2] = t.z;
+            v[3] = t.w;
         } else {
             const float2 t = *reinterpret_cast<const float2 *>(src);
-            v[0] = t.x; v[1] = t.y;
+            v[0] = t.x;
+            v[1] = t.y;
         }
         if (lse == -INFINITY) continue;
         if (lse > m) {
@@ -580,7 +738,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float L = 0.f;
+    float Lsum = 0.f;
     float o[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) o[e] = 0.f;
@@ -589,15 +747,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
         for (int w = 0; w < kMergeWarps; ++w) {
             if (sm_m[w] == -INFINITY) continue;
             const float f = fast_exp2(sm_m[w] - M);
-            L += f * sm_l[w];
+            Lsum += f * sm_l[w];
 #pragma unroll
             for (int e = 0; e < PER; ++e) o[e] += f * sm_o[w][lane * PER + e];
         }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int r = i / p.group, g = i - r * p.group;
-    __nv_bfloat16 *dst =
-        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + lane * PER;
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     if constexpr (PER == 4) {
         uint2 packed;
         packed.x = pack_bf16x2(o[0] * inv, o[1] * inv);
@@ -608,20 +763,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     }
 }
 
-template <int HD>
-constexpr size_t smem_bytes() {
-    return 1024 + (size_t)kStages * Geo<HD>::kStageBytes + 2 * kStages * sizeof(uint64_t) +
-           2 * kStages * kWarps * sizeof(int) + kMaxStagedPages * sizeof(int);
-}
-
 template <int HD, int MT>
 int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  cudaStream_t stream) {
-    static_assert(kStages * Geo<HD>::kStageBytes >=
-                      (size_t)kWarps * 16 * MT * HD * 4 + 2 * kWarps * 16 * MT * 4,
-                  "merge area must fit in the stage memory");
+    using G = Geo<HD, MT>;
+    static_assert(G::kSmem <= 232448, "shared memory budget");
     auto kern = decode_split_kernel<HD, MT>;
-    const size_t smem = smem_bytes<HD>();
+    const size_t smem = G::kSmem;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -634,15 +782,12 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
         }
         configured_device = dev;
     }
-    dim3 grid(p.nsplit, p.n_kv_heads * p.row_blocks, p.batch);
-    if (launch_pdl(kern, grid, dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
+    if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    if (p.nsplit > 1) {
-        const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
-        if (launch_pdl(decode_merge_kernel<HD, 16 * MT>, dim3(ctas), dim3(kMergeWarps * 32), 0,
-                       stream, p) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-    }
+    const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
+    if (launch_pdl(decode_merge_kernel<HD, G::RB>, dim3(ctas), dim3(kMergeWarps * 32), 0, stream,
+                   p) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 
@@ -650,42 +795,25 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
                 int head_dim, int max_seq_len, int window, DecodePlan *plan) {
+    (void)cache;
+    (void)max_seq_len;
+    (void)window;
     const int group = n_q_heads / n_kv_heads;
     plan->head_dim = head_dim;
     plan->rows = q_rows * group;
     plan->m_tiles = plan->rows <= 16 ? 1 : 2;
     const int rb_rows = 16 * plan->m_tiles;
     plan->row_blocks = (plan->rows + rb_rows - 1) / rb_rows;
-    // Longest key range one request can need.
-    int64_t keys = max_seq_len;
-    if (window > 0) keys = std::min<int64_t>(keys, (int64_t)window + q_rows - 1);
-    if (cache->kind == ATTN_CACHE_RING) keys = std::min<int64_t>(keys, cache->slots_per_seq);
-    const int64_t max_chunks = (keys + dec::kChunk - 1) / dec::kChunk + 1;
-    const int64_t units = (int64_t)batch * n_kv_heads * plan->row_blocks;
-    const int64_t slots = (int64_t)device_sm_count() * 2;  // two CTAs per SM
-    // At least two waves of CTAs, each split >= 4 chunks (64 keys) and
-    // <= kMaxChunksPerSplit chunks; then round up to fill the last wave.
-    int64_t lo = (max_chunks + dec::kMaxChunksPerSplit - 1) / dec::kMaxChunksPerSplit;
-    int64_t hi = std::max<int64_t>(1, max_chunks / 4);
-    hi = std::max(hi, lo);
-    int64_t n = (2 * slots + units - 1) / std::max<int64_t>(units, 1);
-    n = std::min(std::max(n, lo), hi);
-    if (n > 1) {
-        int64_t best = n;
-        double best_eff = 0.0;
-        for (int64_t c = n; c <= std::min<int64_t>(hi, 2 * n); ++c) {
-            const double w = (double)(units * c) / (double)slots;
-            const double eff = w / std::ceil(w);
-            if (eff > best_eff + 1e-9) {
-                best_eff = eff;
-                best = c;
-            }
-        }
-        n = best;
-    }
-    plan->nsplit = (int)n;
-    plan->workspace =
-        n > 1 ? (size_t)units * n * rb_rows * ((size_t)head_dim + 1) * sizeof(float) + 256 : 0;
+    plan->grid = device_sm_count();
+    // Requests per launch: the (request, row block) tables live in shared memory.
+    plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
+    plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
+    const size_t units = (size_t)plan->batch_per_launch * n_kv_heads * plan->row_blocks;
+    // partial slots: unit + cta < units + grid; tables: N, Pb[B+1], cnt[B * row_blocks]
+    const size_t slots = units + plan->grid;
+    const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
+    const size_t meta = (2 + (size_t)plan->batch_per_launch * (plan->row_blocks + 1)) * 4;
+    plan->workspace = ((partial + 255) & ~size_t(255)) + meta + 256;
     return ATTN_OK;
 }
 
@@ -693,53 +821,65 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
                   void *out, void *workspace, int32_t *err, cudaStream_t stream) {
-    dec::Params p;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.k_cache = static_cast<const __nv_bfloat16 *>(cache->k);
-    p.v_cache = static_cast<const __nv_bfloat16 *>(cache->v);
-    p.num_slots = cache->num_slots;
-    p.kind = cache->kind;
-    p.slots_per_seq = cache->slots_per_seq;
-    p.block_table = cache->block_table;
-    p.block_size = cache->block_size;
-    p.max_blocks = cache->max_blocks_per_seq;
-    p.seq_lens = seq_lens;
-    p.positions = positions;
-    p.batch = batch;
-    p.q_rows = q_rows;
-    p.n_q_heads = n_q_heads;
-    p.n_kv_heads = n_kv_heads;
-    p.group = n_q_heads / n_kv_heads;
-    p.rows = plan.rows;
-    p.window = window;
-    p.max_seq_len = max_seq_len;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.nsplit = plan.nsplit;
-    p.row_blocks = plan.row_blocks;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.err = err;
-    p.ws_o = nullptr;
-    p.ws_lse = nullptr;
-    if (plan.nsplit > 1) {
-        const int rb_rows = 16 * plan.m_tiles;
-        const size_t units = (size_t)batch * n_kv_heads * plan.row_blocks;
-        const size_t entries = units * plan.nsplit * rb_rows;
-        p.ws_o = static_cast<float *>(workspace);
-        p.ws_lse = p.ws_o + entries * plan.head_dim;
-    }
     // TMA maps over the caches viewed as [num_slots, n_kv_heads * head_dim].
     CUtensorMap tk, tv;
     const uint64_t dims[2] = {(uint64_t)n_kv_heads * plan.head_dim, (uint64_t)cache->num_slots};
     const uint64_t strides[1] = {(uint64_t)n_kv_heads * plan.head_dim * 2};
     const uint32_t box[2] = {64, (uint32_t)dec::kChunk};
     if (!encode_tensor_map(&tk, cache->k, 2, dims, strides, box, true) ||
-        !encode_tensor_map(&tv, cache->v, 2, dims, strides, box, true))
+        !encode_tensor_map(&tv, cache->v, 2, dims, strides, box, true)) {
+        note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
-    if (plan.head_dim == 128)
-        return plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, stream)
-                                 : dec::launch_split<128, 2>(p, tk, tv, stream);
-    return plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, stream)
-                             : dec::launch_split<64, 2>(p, tk, tv, stream);
+    }
+    const int rb_rows = 16 * plan.m_tiles;
+    const size_t units = (size_t)plan.batch_per_launch * n_kv_heads * plan.row_blocks;
+    const size_t slots = units + plan.grid;
+    const size_t partial = slots * rb_rows * ((size_t)plan.head_dim + 1) * sizeof(float);
+    for (int b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
+        const int nb = std::min(plan.batch_per_launch, batch - b0);
+        const int64_t qo = (int64_t)b0 * q_rows * n_q_heads * plan.head_dim;
+        dec::Params p;
+        p.q = static_cast<const __nv_bfloat16 *>(q) + qo;
+        p.k_cache = static_cast<const __nv_bfloat16 *>(cache->k);
+        p.v_cache = static_cast<const __nv_bfloat16 *>(cache->v);
+        p.num_slots = cache->num_slots;
+        p.kind = cache->kind;
+        p.slots_per_seq = cache->slots_per_seq;
+        p.block_table = cache->block_table
+                            ? cache->block_table + (int64_t)b0 * cache->max_blocks_per_seq
+                            : nullptr;
+        p.block_size = cache->block_size;
+        p.max_blocks = cache->max_blocks_per_seq;
+        p.seq_lens = seq_lens + b0;
+        p.positions = positions + (int64_t)b0 * q_rows;
+        p.batch = nb;
+        p.b_base = b0;
+        p.q_rows = q_rows;
+        p.n_q_heads = n_q_heads;
+        p.n_kv_heads = n_kv_heads;
+        p.group = n_q_heads / n_kv_heads;
+        p.rows = plan.rows;
+        p.window = window;
+        p.max_seq_len = max_seq_len;
+        p.scale_log2 = scale * 1.4426950408889634f;
+        p.row_blocks = plan.row_blocks;
+        p.grid = plan.grid;
+        p.out = static_cast<__nv_bfloat16 *>(out) + qo;
+        p.err = err;
+        p.ws_o = static_cast<float *>(workspace);
+        p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
+        p.ws_meta = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                ((partial + 255) & ~size_t(255)));
+        int rc;
+        if (plan.head_dim == 128)
+            rc = plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, stream)
+                                   : dec::launch_split<128, 2>(p, tk, tv, stream);
+        else
+            rc = plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, stream)
+                                   : dec::launch_split<64, 2>(p, tk, tv, stream);
+        if (rc != ATTN_OK) return rc;
+    }
+    return ATTN_OK;
 }
 
 }  // namespace gqa

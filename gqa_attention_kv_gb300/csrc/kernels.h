@@ -44,14 +44,17 @@ int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_m
                      void *k_cache, void *v_cache, int64_t num_slots, int row_bytes,
                      int32_t *err, cudaStream_t stream);
 
-// Decode plan: how the grid splits each request's keys.
+// Decode plan: a persistent grid of one CTA per SM; requests are processed
+// in launches of at most batch_per_launch (the per-request tables live in
+// shared memory).
 struct DecodePlan {
     int head_dim;
-    int m_tiles;      // 16-row MMA tiles per CTA (1 or 2)
-    int rows;         // q_rows * group
-    int row_blocks;   // CTAs along the query rows of one KV head
-    int nsplit;       // CTAs along the keys of one (request, KV head, row block)
-    size_t workspace; // bytes of fp32 partial states (0 when nsplit == 1)
+    int m_tiles;          // 16-row MMA tiles per unit (1 or 2)
+    int rows;             // q_rows * group
+    int row_blocks;       // units along the query rows of one KV head
+    int grid;             // CTAs of the split kernel
+    int batch_per_launch;
+    size_t workspace;     // bytes of scratch: fp32 partial states + tables
 };
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
