@@ -50,7 +50,7 @@ constexpr int kChunk = 16;                   // key positions per chunk
 constexpr int kWarps = 4;                    // consumer warps = chunks per tile
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
-constexpr int kMaxTableEntries = 1024;       // (request, row block) pairs per launch
+constexpr int kMaxTableEntries = 512;        // (request, row block) pairs per launch
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -70,7 +70,8 @@ struct Params {
     int window, max_seq_len;
     float scale_log2;
     int row_blocks;
-    int grid;  // CTAs of the split kernel
+    int rb_rows;  // query rows per unit (8, 16 or 32)
+    int grid;     // CTAs of the split kernel
     __nv_bfloat16 *out;
     float *ws_o;
     float *ws_lse;
@@ -78,22 +79,30 @@ struct Params {
     int32_t *err;
 };
 
+// MT = 0: up to 8 query rows per unit; keys are the M dimension of the
+//         mma (S^T = K Q^T, O^T = V^T P^T), rows the N dimension of 8.
+// MT = 1, 2: 16 or 32 rows per unit; rows are the M dimension.
 template <int HD, int MT>
 struct Geo {
-    static constexpr int RB = 16 * MT;                       // rows per unit
+    static constexpr int RB = MT == 0 ? 8 : 16 * MT;        // rows per unit
+    static constexpr int kCtasPerSm = MT == 2 ? 1 : 2;
     static constexpr int kHalves = HD / 64;                 // 128-byte column blocks
     static constexpr int kChunkBytes = kHalves * kChunk * 128;
     static constexpr int kTileBytes = kWarps * kChunkBytes;  // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kMergeBytes = kWarps * RB * HD * 4 + 2 * kWarps * RB * 4;
-    static constexpr int kStages = HD == 128 ? (MT == 1 ? 5 : 4) : (MT == 1 ? 10 : 9);
+    static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
+    // as many stages as the shared memory of kCtasPerSm CTAs allows (max 8)
+    static constexpr int kBudget = (kCtasPerSm == 2 ? 115712 : 232448) - 1024 - kMergeBytes -
+                                   kTableBytes - 1024;
+    static constexpr int kStages = kBudget / kStageBytes > 8 ? 8 : kBudget / kStageBytes;
     static constexpr int kOffMerge = kStages * kStageBytes;
     static constexpr int kOffBars = kOffMerge + kMergeBytes;
     static constexpr int kOffInfo = kOffBars + 2 * kStages * 8;
     static constexpr int kOffTable = kOffInfo + 2 * kStages * kWarps * 4;
     // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
-    static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
     static constexpr size_t kSmem = 1024 + kOffTable + kTableBytes;
+    static_assert(kStages >= 2, "at least a double-buffered ring");
 };
 
 // Byte offset of 16-byte piece `c16` (0 .. HD/8-1) of row `row` inside a chunk
@@ -115,8 +124,7 @@ __device__ __forceinline__ void unit_range(const Params &p, int b, int rb, int &
         if (p.kind == ATTN_CACHE_LINEAR) seq_len = min(seq_len, p.slots_per_seq);
     }
     seq_len_out = seq_len;
-    const int RB = p.rows <= 16 ? 16 : 32;
-    const int row0 = rb * RB, row1 = min(p.rows, row0 + RB);
+    const int row0 = rb * p.rb_rows, row1 = min(p.rows, row0 + p.rb_rows);
     int pmin = INT32_MAX, pmax = -1;
     for (int r = row0 / p.group; r <= (row1 - 1) / p.group; ++r) {
         const int pos = p.positions[(int64_t)b * p.q_rows + r];
@@ -188,7 +196,7 @@ struct SegmentWalker {
 };
 
 template <int HD, int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
     using G = Geo<HD, MT>;
@@ -402,21 +410,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         info_mask[st * kWarps + c] = mask;
                     }
                 }
-                if (lane == 0) {
-                    if (tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
+                // lane 0 announces the stage's TMA bytes, then lane c issues
+                // chunk c's boxes (four issuing threads instead of one)
+                if (lane == 0 && tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
+                __syncwarp();
+                int64_t my_slot0 = slot0[0];
 #pragma unroll
-                    for (int c = 0; c < kWarps; ++c) {
-                        if (slot0[c] < -1) continue;
-                        const int y = slot0[c] < 0 ? -kChunk : (int)slot0[c];
+                for (int c = 1; c < kWarps; ++c)
+                    if (lane == c) my_slot0 = slot0[c];
+                if (lane < kWarps && my_slot0 >= -1) {
+                    const int y = my_slot0 < 0 ? -kChunk : (int)my_slot0;
 #pragma unroll
-                        for (int h = 0; h < G::kHalves; ++h) {
-                            const int x = sg.kvh * HD + h * 64;
-                            tma_load_2d(kst + c * G::kChunkBytes + h * kChunk * 128, &tm_k, x, y,
-                                        &full[st]);
-                            tma_load_2d(vst + c * G::kChunkBytes + h * kChunk * 128, &tm_v, x, y,
-                                        &full[st]);
-                        }
+                    for (int h = 0; h < G::kHalves; ++h) {
+                        const int x = sg.kvh * HD + h * 64;
+                        tma_load_2d(kst + lane * G::kChunkBytes + h * kChunk * 128, &tm_k, x, y,
+                                    &full[st]);
+                        tma_load_2d(vst + lane * G::kChunkBytes + h * kChunk * 128, &tm_v, x, y,
+                                    &full[st]);
                     }
+                }
+                __syncwarp();
+                if (lane == 0) {
                     mbar_arrive(&full[st]);
                 } else if (issued_cp) {
                     cp_async_arrive_noinc(&full[st]);
@@ -442,167 +456,301 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = sg.b, kvh = sg.kvh;
         const int row0 = sg.rb * RB;
         const int row1 = min(p.rows, row0 + RB);
-        uint32_t qa[MT][HD / 16][4];
-        int rpos[MT][2];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int i = row0 + mt * 16 + gq + hr * 8;
-                const bool valid = i < row1;
-                const int r = valid ? i / p.group : 0;
-                const int g = valid ? i - r * p.group : 0;
-                rpos[mt][hr] = valid ? p.positions[(int64_t)b * p.q_rows + r] : -1;
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    qa[mt][kk][hr] = valid ? __ldg(qrow + kk * 8 + tq) : 0u;
-                    qa[mt][kk][2 + hr] = valid ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
-                }
-            }
-        }
-        float m_run[MT][2], l_run[MT][2];
-        float o[MT][HD / 8][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            m_run[mt][0] = m_run[mt][1] = -INFINITY;
-            l_run[mt][0] = l_run[mt][1] = 0.f;
-#pragma unroll
-            for (int n = 0; n < HD / 8; ++n)
-                o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
-        }
         const int seq_len = tb.seqlen[b];
         const int ring_lo = p.kind == ATTN_CACHE_RING ? seq_len - p.slots_per_seq : 0;
         const int window = p.window;
         const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
-        for (int it = 0; it < n_tiles; ++it, ++tile) {
-            const int st = tile % kStages;
-            ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
-            __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
-            if (!ok) break;
-            const int t0 = info_t0[st * kWarps + warp];
-            if (t0 >= 0) {
-                const uint32_t mask16 = info_mask[st * kWarps + warp];
-                const uint32_t kbase =
-                    smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
-                const uint32_t vbase = kbase + G::kTileBytes;
-                float s[MT][2][4];
+        if constexpr (MT == 0) {
+            // ---- up to 8 rows: S^T = K Q^T (keys x rows), O^T = V^T P^T (d x rows)
+            // Q^T as the B operand: thread holds row gq, d pairs 2tq (+8) of each k-step
+            uint32_t qb[HD / 16][2];
+            {
+                const int i = row0 + gq;
+                const bool valid = i < row1;
+                const int r = valid ? i / p.group : 0;
+                const int g = valid ? i - r * p.group : 0;
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                    p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    qb[kk][0] = valid ? __ldg(qrow + kk * 8 + tq) : 0u;
+                    qb[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+                }
+            }
+            // this thread's S^T columns are rows 2tq and 2tq+1
+            int cpos[2];
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        s[mt][j][0] = s[mt][j][1] = s[mt][j][2] = s[mt][j][3] = 0.f;
-                {
+            for (int e = 0; e < 2; ++e) {
+                const int i = row0 + 2 * tq + e;
+                cpos[e] = i < row1 ? p.positions[(int64_t)b * p.q_rows + i / p.group] : -1;
+            }
+            float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+            float o[HD / 16][4];  // m-tile md: (d = 16md + gq (+8), rows 2tq, 2tq+1)
+#pragma unroll
+            for (int n = 0; n < HD / 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            for (int it = 0; it < n_tiles; ++it, ++tile) {
+                const int st = tile % kStages;
+                ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
+                __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
+                if (!ok) break;
+                const int t0 = info_t0[st * kWarps + warp];
+                if (t0 >= 0) {
+                    const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const uint32_t kbase =
+                        smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
+                    const uint32_t vbase = kbase + G::kTileBytes;
                     const int m = lane >> 3;
-                    const int key = (m >> 1) * 8 + (lane & 7);
+                    float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
+                    {
+                        const int key = (m & 1) * 8 + (lane & 7);
 #pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        uint32_t b00, b01, b10, b11;
-                        ldmatrix_x4(b00, b01, b10, b11,
-                                    kbase + chunk_offset(key, kk * 2 + (m & 1)));
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            mma_bf16_16816(s[mt][0], qa[mt][kk], b00, b01);
-                            mma_bf16_16816(s[mt][1], qa[mt][kk], b10, b11);
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            uint32_t a[4];
+                            ldmatrix_x4(a[0], a[1], a[2], a[3],
+                                        kbase + chunk_offset(key, kk * 2 + (m >> 1)));
+                            mma_bf16_16816(sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     }
-                }
-                uint32_t pa[MT][4], pl[MT][4];  // P as bf16 hi + lo
+                    float alpha[2];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int pos = rpos[mt][hr];
+                    for (int e = 0; e < 2; ++e) {  // row 2tq + e: elements e (key gq), e+2 (key gq+8)
+                        const int pos = cpos[e];
                         float mx = -INFINITY;
 #pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int n = j * 8 + tq * 2 + e;
-                                const int t = t0 + n;
-                                const bool valid = ((mask16 >> n) & 1u) && t < seq_len &&
-                                                   t <= pos && t >= ring_lo &&
-                                                   (window <= 0 || pos - t < window);
-                                const float v =
-                                    valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
-                                s[mt][j][hr * 2 + e] = v;
-                                mx = fmaxf(mx, v);
-                            }
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                        const float m_new = fmaxf(m_run[mt][hr], mx);
+                        for (int hk = 0; hk < 2; ++hk) {
+                            const int n = gq + hk * 8;
+                            const int t = t0 + n;
+                            const bool valid = ((mask16 >> n) & 1u) && t < seq_len && t <= pos &&
+                                               t >= ring_lo && (window <= 0 || pos - t < window);
+                            const float v = valid ? sacc[e + 2 * hk] * p.scale_log2 : -INFINITY;
+                            sacc[e + 2 * hk] = v;
+                            mx = fmaxf(mx, v);
+                        }
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[e], mx);
                         const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                        const float alpha = fast_exp2(m_run[mt][hr] - m_use);
-                        float sum = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const float pv = fast_exp2(s[mt][j][hr * 2 + e] - m_use);
-                                s[mt][j][hr * 2 + e] = pv;
-                                sum += pv;
-                            }
-                        l_run[mt][hr] = l_run[mt][hr] * alpha + sum;
-                        m_run[mt][hr] = m_new;
-#pragma unroll
-                        for (int n = 0; n < HD / 8; ++n) {
-                            o[mt][n][hr * 2] *= alpha;
-                            o[mt][n][hr * 2 + 1] *= alpha;
-                        }
+                        alpha[e] = fast_exp2(m_run[e] - m_use);
+                        const float p0 = fast_exp2(sacc[e] - m_use);
+                        const float p1 = fast_exp2(sacc[e + 2] - m_use);
+                        sacc[e] = p0;
+                        sacc[e + 2] = p1;
+                        l_run[e] = l_run[e] * alpha[e] + (p0 + p1);
+                        m_run[e] = m_new;
                     }
-                    split_bf16x2(s[mt][0][0], s[mt][0][1], pa[mt][0], pl[mt][0]);
-                    split_bf16x2(s[mt][0][2], s[mt][0][3], pa[mt][1], pl[mt][1]);
-                    split_bf16x2(s[mt][1][0], s[mt][1][1], pa[mt][2], pl[mt][2]);
-                    split_bf16x2(s[mt][1][2], s[mt][1][3], pa[mt][3], pl[mt][3]);
-                }
-                {
-                    const int m = lane >> 3;
-                    const int key = (m & 1) * 8 + (lane & 7);
 #pragma unroll
-                    for (int dn = 0; dn < HD / 16; ++dn) {
-                        uint32_t v0, v1, v2, v3;
-                        ldmatrix_x4_trans(v0, v1, v2, v3,
-                                          vbase + chunk_offset(key, dn * 2 + (m >> 1)));
+                    for (int n = 0; n < HD / 16; ++n) {
+                        o[n][0] *= alpha[0];
+                        o[n][1] *= alpha[1];
+                        o[n][2] *= alpha[0];
+                        o[n][3] *= alpha[1];
+                    }
+                    // P^T fragments: transpose the (key x row) blocks of keys 0-7 and 8-15
+                    uint32_t h0, l0, h1, l1;
+                    split_bf16x2(sacc[0], sacc[1], h0, l0);
+                    split_bf16x2(sacc[2], sacc[3], h1, l1);
+                    const uint32_t bh0 = movmatrix_trans(h0), bl0 = movmatrix_trans(l0);
+                    const uint32_t bh1 = movmatrix_trans(h1), bl1 = movmatrix_trans(l1);
+                    {
+                        const int key = (m >> 1) * 8 + (lane & 7);
 #pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
-                            mma_bf16_16816(o[mt][dn * 2 + 1], pa[mt], v2, v3);
-                            mma_bf16_16816(o[mt][dn * 2], pl[mt], v0, v1);
-                            mma_bf16_16816(o[mt][dn * 2 + 1], pl[mt], v2, v3);
+                        for (int md = 0; md < HD / 16; ++md) {
+                            uint32_t a[4];
+                            ldmatrix_x4_trans(a[0], a[1], a[2], a[3],
+                                              vbase + chunk_offset(key, md * 2 + (m & 1)));
+                            mma_bf16_16816(o[md], a, bh0, bh1);
+                            mma_bf16_16816(o[md], a, bl0, bl1);
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
-        }
-        // ---- end of segment: merge the four warps through shared memory
+            // the row sums are spread over the 8 lanes that share tq
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                float l = l_run[mt][hr];
-                l += __shfl_xor_sync(0xffffffffu, l, 1);
-                l += __shfl_xor_sync(0xffffffffu, l, 2);
-                l_run[mt][hr] = l;
+            for (int e = 0; e < 2; ++e) {
+                float l = l_run[e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                l_run[e] = l;
             }
-        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
+            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+            for (int md = 0; md < HD / 16; ++md)
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = mt * 16 + gq + hr * 8;
-                float *dst = mo + ((size_t)warp * RB + row) * HD;
+                for (int e = 0; e < 4; ++e) {
+                    const int row = 2 * tq + (e & 1);
+                    const int d = md * 16 + gq + (e >> 1) * 8;
+                    mo[((size_t)warp * RB + row) * HD + d] = o[md][e];
+                }
+            if (gq == 0) {
 #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mm[warp * RB + 2 * tq + e] = m_run[e];
+                    ml[warp * RB + 2 * tq + e] = l_run[e];
+                }
+            }
+        } else {
+            uint32_t qa[MT][HD / 16][4];
+            int rpos[MT][2];
+    #pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+    #pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = row0 + mt * 16 + gq + hr * 8;
+                    const bool valid = i < row1;
+                    const int r = valid ? i / p.group : 0;
+                    const int g = valid ? i - r * p.group : 0;
+                    rpos[mt][hr] = valid ? p.positions[(int64_t)b * p.q_rows + r] : -1;
+                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                        p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
+    #pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        qa[mt][kk][hr] = valid ? __ldg(qrow + kk * 8 + tq) : 0u;
+                        qa[mt][kk][2 + hr] = valid ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+                    }
+                }
+            }
+            float m_run[MT][2], l_run[MT][2];
+            float o[MT][HD / 8][4];
+    #pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                m_run[mt][0] = m_run[mt][1] = -INFINITY;
+                l_run[mt][0] = l_run[mt][1] = 0.f;
+    #pragma unroll
                 for (int n = 0; n < HD / 8; ++n)
-                    *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
-                        make_float2(o[mt][n][hr * 2], o[mt][n][hr * 2 + 1]);
-                if (tq == 0) {
-                    mm[warp * RB + row] = m_run[mt][hr];
-                    ml[warp * RB + row] = l_run[mt][hr];
-                }
+                    o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
             }
+            for (int it = 0; it < n_tiles; ++it, ++tile) {
+                const int st = tile % kStages;
+                ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
+                __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
+                if (!ok) break;
+                const int t0 = info_t0[st * kWarps + warp];
+                if (t0 >= 0) {
+                    const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const uint32_t kbase =
+                        smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
+                    const uint32_t vbase = kbase + G::kTileBytes;
+                    float s[MT][2][4];
+    #pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+    #pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            s[mt][j][0] = s[mt][j][1] = s[mt][j][2] = s[mt][j][3] = 0.f;
+                    {
+                        const int m = lane >> 3;
+                        const int key = (m >> 1) * 8 + (lane & 7);
+    #pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            uint32_t b00, b01, b10, b11;
+                            ldmatrix_x4(b00, b01, b10, b11,
+                                        kbase + chunk_offset(key, kk * 2 + (m & 1)));
+    #pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_bf16_16816(s[mt][0], qa[mt][kk], b00, b01);
+                                mma_bf16_16816(s[mt][1], qa[mt][kk], b10, b11);
+                            }
+                        }
+                    }
+                    uint32_t pa[MT][4], pl[MT][4];  // P as bf16 hi + lo
+    #pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+    #pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int pos = rpos[mt][hr];
+                            float mx = -INFINITY;
+    #pragma unroll
+                            for (int j = 0; j < 2; ++j)
+    #pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int n = j * 8 + tq * 2 + e;
+                                    const int t = t0 + n;
+                                    const bool valid = ((mask16 >> n) & 1u) && t < seq_len &&
+                                                       t <= pos && t >= ring_lo &&
+                                                       (window <= 0 || pos - t < window);
+                                    const float v =
+                                        valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
+                                    s[mt][j][hr * 2 + e] = v;
+                                    mx = fmaxf(mx, v);
+                                }
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                            const float m_new = fmaxf(m_run[mt][hr], mx);
+                            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                            const float alpha = fast_exp2(m_run[mt][hr] - m_use);
+                            float sum = 0.f;
+    #pragma unroll
+                            for (int j = 0; j < 2; ++j)
+    #pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const float pv = fast_exp2(s[mt][j][hr * 2 + e] - m_use);
+                                    s[mt][j][hr * 2 + e] = pv;
+                                    sum += pv;
+                                }
+                            l_run[mt][hr] = l_run[mt][hr] * alpha + sum;
+                            m_run[mt][hr] = m_new;
+    #pragma unroll
+                            for (int n = 0; n < HD / 8; ++n) {
+                                o[mt][n][hr * 2] *= alpha;
+                                o[mt][n][hr * 2 + 1] *= alpha;
+                            }
+                        }
+                        split_bf16x2(s[mt][0][0], s[mt][0][1], pa[mt][0], pl[mt][0]);
+                        split_bf16x2(s[mt][0][2], s[mt][0][3], pa[mt][1], pl[mt][1]);
+                        split_bf16x2(s[mt][1][0], s[mt][1][1], pa[mt][2], pl[mt][2]);
+                        split_bf16x2(s[mt][1][2], s[mt][1][3], pa[mt][3], pl[mt][3]);
+                    }
+                    {
+                        const int m = lane >> 3;
+                        const int key = (m & 1) * 8 + (lane & 7);
+    #pragma unroll
+                        for (int dn = 0; dn < HD / 16; ++dn) {
+                            uint32_t v0, v1, v2, v3;
+                            ldmatrix_x4_trans(v0, v1, v2, v3,
+                                              vbase + chunk_offset(key, dn * 2 + (m >> 1)));
+    #pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
+                                mma_bf16_16816(o[mt][dn * 2 + 1], pa[mt], v2, v3);
+                                mma_bf16_16816(o[mt][dn * 2], pl[mt], v0, v1);
+                                mma_bf16_16816(o[mt][dn * 2 + 1], pl[mt], v2, v3);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+            // ---- end of segment: merge the four warps through shared memory
+    #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+    #pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    float l = l_run[mt][hr];
+                    l += __shfl_xor_sync(0xffffffffu, l, 1);
+                    l += __shfl_xor_sync(0xffffffffu, l, 2);
+                    l_run[mt][hr] = l;
+                }
+            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
+    #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+    #pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int row = mt * 16 + gq + hr * 8;
+                    float *dst = mo + ((size_t)warp * RB + row) * HD;
+    #pragma unroll
+                    for (int n = 0; n < HD / 8; ++n)
+                        *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
+                            make_float2(o[mt][n][hr * 2], o[mt][n][hr * 2 + 1]);
+                    if (tq == 0) {
+                        mm[warp * RB + row] = m_run[mt][hr];
+                        ml[warp * RB + row] = l_run[mt][hr];
+                    }
+                }
+        }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
             const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
@@ -767,7 +915,8 @@ template <int HD, int MT>
 int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  cudaStream_t stream) {
     using G = Geo<HD, MT>;
-    static_assert(G::kSmem <= 232448, "shared memory budget");
+    static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
+                  "shared memory budget");
     auto kern = decode_split_kernel<HD, MT>;
     const size_t smem = G::kSmem;
     static int configured_device = -1;
@@ -801,10 +950,11 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     const int group = n_q_heads / n_kv_heads;
     plan->head_dim = head_dim;
     plan->rows = q_rows * group;
-    plan->m_tiles = plan->rows <= 16 ? 1 : 2;
-    const int rb_rows = 16 * plan->m_tiles;
+    plan->m_tiles = plan->rows <= 8 ? 0 : plan->rows <= 16 ? 1 : 2;
+    const int rb_rows = plan->m_tiles == 0 ? 8 : 16 * plan->m_tiles;
     plan->row_blocks = (plan->rows + rb_rows - 1) / rb_rows;
-    plan->grid = device_sm_count();
+    // persistent grid: two CTAs per SM (one when a unit holds 32 rows)
+    plan->grid = device_sm_count() * (plan->m_tiles == 2 ? 1 : 2);
     // Requests per launch: the (request, row block) tables live in shared memory.
     plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
     plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
@@ -831,7 +981,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
-    const int rb_rows = 16 * plan.m_tiles;
+    const int rb_rows = plan.m_tiles == 0 ? 8 : 16 * plan.m_tiles;
     const size_t units = (size_t)plan.batch_per_launch * n_kv_heads * plan.row_blocks;
     const size_t slots = units + plan.grid;
     const size_t partial = slots * rb_rows * ((size_t)plan.head_dim + 1) * sizeof(float);
@@ -863,6 +1013,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.max_seq_len = max_seq_len;
         p.scale_log2 = scale * 1.4426950408889634f;
         p.row_blocks = plan.row_blocks;
+        p.rb_rows = rb_rows;
         p.grid = plan.grid;
         p.out = static_cast<__nv_bfloat16 *>(out) + qo;
         p.err = err;
@@ -872,11 +1023,13 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                                                 ((partial + 255) & ~size_t(255)));
         int rc;
         if (plan.head_dim == 128)
-            rc = plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, stream)
-                                   : dec::launch_split<128, 2>(p, tk, tv, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, stream)
+                                     : dec::launch_split<128, 2>(p, tk, tv, stream);
         else
-            rc = plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, stream)
-                                   : dec::launch_split<64, 2>(p, tk, tv, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, stream)
+                                     : dec::launch_split<64, 2>(p, tk, tv, stream);
         if (rc != ATTN_OK) return rc;
     }
     return ATTN_OK;

@@ -49,7 +49,7 @@ int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_m
 // shared memory).
 struct DecodePlan {
     int head_dim;
-    int m_tiles;          // 16-row MMA tiles per unit (1 or 2)
+    int m_tiles;          // 0: <= 8 rows per unit (keys as MMA rows); 1, 2: 16-row tiles
     int rows;             // q_rows * group
     int row_blocks;       // units along the query rows of one KV head
     int grid;             // CTAs of the split kernel
