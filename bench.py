@@ -201,7 +201,7 @@ class QwenWorkload(Workload):
                              "slots": c.slot_mapping, "seq": c.seq_lens, "pos": c.positions,
                              "out": torch.empty_like(c.q), "ctx": ctx})
         self.max_seq = self.cap
-        self.ws = torch.empty(gq.attn_decode_workspace_size(self.caches[0], self.B, 1, Hq,
+        self.ws = torch.zeros(gq.attn_decode_workspace_size(self.caches[0], self.B, 1, Hq,
                                                             self.max_seq, 0),
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -340,7 +340,7 @@ class DecodeOnlyWorkload(Workload):
                                   block_table=base.block_table, block_size=base.block_size)
                        for i in range(self.ncopy)]
         self.max_seq = base.max_seq_len()
-        self.ws = torch.empty(gq.attn_decode_workspace_size(
+        self.ws = torch.zeros(gq.attn_decode_workspace_size(
             self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window),
             dtype=torch.uint8, device=dev)
         self.out = torch.empty_like(base.q)

@@ -154,8 +154,9 @@ def attn_decode_workspace_size(cache: KVCache, batch, q_rows, n_q_heads, max_seq
 def attn_decode(q, cache: KVCache, seq_lens, positions, max_seq_len, window, scale, out=None,
                 workspace=None, err=None, stream=None):
     """Decode attention.  q bf16 [B, R, Hq, D]; seq_lens int32 [B]; positions int32 [B*R].
-    Returns out (bf16 [B, R, Hq, D]).  A workspace (uint8 device tensor of at
-    least attn_decode_workspace_size bytes) is allocated if not given."""
+    Returns out (bf16 [B, R, Hq, D]).  A workspace (zero-filled uint8 device
+    tensor of at least attn_decode_workspace_size bytes) is allocated if not
+    given; one kept across calls needs no clearing."""
     import torch
 
     B, R, Hq, D = q.shape
@@ -163,7 +164,7 @@ def attn_decode(q, cache: KVCache, seq_lens, positions, max_seq_len, window, sca
         out = torch.empty_like(q)
     need = attn_decode_workspace_size(cache, B, R, Hq, max_seq_len, window)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     c = cache.struct()
     rc = lib().attn_decode(_ptr(q), ctypes.byref(c), _ptr(seq_lens), _ptr(positions), B, R,
                            int(max_seq_len), int(window), Hq, cache.n_kv_heads, D, float(scale),

@@ -19,8 +19,9 @@
 //     included), and each CTA streams its share through one deep TMA ring,
 //     paying the pipeline ramp once.  A CTA's share covers pieces ("segments")
 //     of one or more units; a unit wholly inside one CTA is written straight
-//     to the output, the others leave fp32 partial states in the workspace
-//     for the merge kernel.
+//     to the output; the others leave fp32 partial states in the workspace,
+//     and the CTA that stores a unit's last partial (a per-unit counter tells
+//     it) merges them in CTA order and resets the counter.  One launch.
 //   * A producer warp streams 64-key tiles (four 16-key chunks).  A chunk
 //     whose 16 slots are consecutive (linear cache; a page of >= 16 slots; a
 //     ring away from its wrap point) is one 2D TMA box per 64 columns, landing
@@ -75,7 +76,7 @@ struct Params {
     __nv_bfloat16 *out;
     float *ws_o;
     float *ws_lse;
-    int32_t *ws_meta;  // [0] = total chunks N; [1 .. B+1] = Pb; then cnt[B * row_blocks]
+    int32_t *ws_count;  // per unit: partial states written so far (zero between calls)
     int32_t *err;
 };
 
@@ -99,7 +100,7 @@ struct Geo {
     static constexpr int kOffMerge = kStages * kStageBytes;
     static constexpr int kOffBars = kOffMerge + kMergeBytes;
     static constexpr int kOffInfo = kOffBars + 2 * kStages * 8;
-    static constexpr int kOffTable = kOffInfo + 2 * kStages * kWarps * 4;
+    static constexpr int kOffTable = kOffInfo + 2 * kStages * kWarps * 4 + 16;
     // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
     static constexpr size_t kSmem = 1024 + kOffTable + kTableBytes;
     static_assert(kStages >= 2, "at least a double-buffered ring");
@@ -155,6 +156,7 @@ struct Segment {
     int b, kvh, rb;
     int c_begin, c_end;  // chunk range inside the unit's key range
     int unit;
+    int unit_start, n_u; // the unit's chunks in the global order: [unit_start, +n_u)
     bool whole;          // the piece is the whole unit
 };
 
@@ -189,6 +191,8 @@ struct SegmentWalker {
         s.c_begin = t.clo[b * RBc + rb] + off;
         s.c_end = s.c_begin + (seg_end - g);
         s.unit = (b * p.n_kv_heads + kvh) * RBc + rb;
+        s.unit_start = unit_start;
+        s.n_u = n_u;
         s.whole = (off == 0 && seg_end == unit_start + n_u);
         g = seg_end;
         return true;
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     uint64_t *empty = full + kStages;
     int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
     uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
+    int *s_last = reinterpret_cast<int *>(info_mask + kStages * kWarps);
     Tables tb;
     tb.cnt = reinterpret_cast<int *>(smem + G::kOffTable);
     tb.clo = tb.cnt + kMaxTableEntries;
@@ -262,10 +267,20 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     __syncthreads();
     const int N = tb.Pb[B];
     const int L = max(1, (N + p.grid - 1) / p.grid);
-    if (blockIdx.x == 0) {  // for the merge kernel
-        for (int i = threadIdx.x; i <= B; i += kThreads) p.ws_meta[1 + i] = tb.Pb[i];
-        for (int i = threadIdx.x; i < B * RBc; i += kThreads) p.ws_meta[2 + B + i] = tb.cnt[i];
-        if (threadIdx.x == 0) p.ws_meta[0] = N;
+    if (blockIdx.x == 0) {
+        // units with no valid key get zeros (no CTA visits them)
+        for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
+            if (tb.cnt[i] != 0) continue;
+            const int b = i / RBc, rb = i - (i / RBc) * RBc;
+            for (int row = rb * RB; row < min(p.rows, (rb + 1) * RB); ++row) {
+                const int r = row / p.group, g = row - r * p.group;
+                for (int kvh = 0; kvh < p.n_kv_heads; ++kvh) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
+                    for (int d = 0; d < HD / 8; ++d) dst[d] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
     }
     const int g0 = min(N, (int)blockIdx.x * L), g1 = min(N, g0 + L);
 
@@ -794,120 +809,59 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 if (d == 0) p.ws_lse[slot] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
             }
         }
-    }
-}
-
-// Merge: one CTA per (request, KV head, query row of the group).  Units whose
-// chunks lie inside one CTA were written by the split kernel; units with no
-// valid key get zeros; the others combine the partial states of the CTAs
-// they span (slots unit + cta), warps taking them round-robin and the warps'
-// states combined in a fixed order, so the result does not depend on timing.
-constexpr int kMergeWarps = 8;
-
-template <int HD, int RB>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Params p) {
-    constexpr int PER = HD / 32;
-    __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
-    __shared__ __align__(16) float sm_o[kMergeWarps][HD];
-    pdl_wait();  // the partial states and tables come from the split kernel
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cta = blockIdx.x;
-    const int b = cta / (p.rows * p.n_kv_heads);
-    const int rem = cta - b * p.rows * p.n_kv_heads;
-    const int kvh = rem / p.rows;
-    const int i = rem - kvh * p.rows;
-    const int rb = i / RB, row = i - rb * RB;
-    const int B = p.batch, RBc = p.row_blocks;
-    const int N = p.ws_meta[0];
-    const int *Pb = p.ws_meta + 1;
-    const int *cnt = p.ws_meta + 2 + B;
-    const int per_head = (Pb[b + 1] - Pb[b]) / p.n_kv_heads;
-    int start = Pb[b] + kvh * per_head;
-    for (int r2 = 0; r2 < rb; ++r2) start += cnt[b * RBc + r2];
-    const int n_u = cnt[b * RBc + rb];
-    const int L = max(1, (N + p.grid - 1) / p.grid);
-    const int r = i / p.group, g = i - r * p.group;
-    __nv_bfloat16 *dst =
-        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + lane * PER;
-    if (n_u == 0) {  // no valid key: zeros
-        if (warp == 0) {
-            if constexpr (PER == 4)
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
-            else
-                *reinterpret_cast<uint32_t *>(dst) = 0u;
+        if (!sg.whole) {
+            // The CTA that stores a unit's last partial state merges all of
+            // them: parts in CTA order, online rescaling, one bf16 rounding.
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+            const int first = sg.unit_start / L, last = (sg.unit_start + sg.n_u - 1) / L;
+            if (ctid == 0) {
+                const int prev = atomicAdd(p.ws_count + sg.unit, 1);
+                *s_last = (prev == last - first) ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+            if (*s_last) {
+                __threadfence();
+                for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
+                    const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+                    const int i = row0 + row;
+                    if (i >= row1) continue;
+                    float M = -INFINITY, Lsum = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = first; c <= last; ++c) {
+                        const int64_t slot = ((int64_t)sg.unit + c) * RB + row;
+                        const float lse = __ldcg(p.ws_lse + slot);
+                        if (lse == -INFINITY) continue;
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
+                        if (lse > M) {
+                            const float f = fast_exp2(M - lse);
+                            Lsum *= f;
+                            acc.x *= f;
+                            acc.y *= f;
+                            acc.z *= f;
+                            acc.w *= f;
+                            M = lse;
+                        }
+                        const float f = fast_exp2(lse - M);
+                        Lsum += f;
+                        acc.x += f * v.x;
+                        acc.y += f * v.y;
+                        acc.z += f * v.z;
+                        acc.w += f * v.w;
+                    }
+                    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+                    const int r = i / p.group, g = i - (i / p.group) * p.group;
+                    __nv_bfloat16 *dst =
+                        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD +
+                        d;
+                    uint2 packed;
+                    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2 *>(dst) = packed;
+                }
+                if (ctid == 0) p.ws_count[sg.unit] = 0;  // ready for the next call
+            }
         }
-        return;
-    }
-    const int first = start / L, last = (start + n_u - 1) / L;
-    if (first == last) return;  // written by the split kernel
-    const int unit = (b * p.n_kv_heads + kvh) * RBc + rb;
-    float m = -INFINITY, l = 0.f;
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (int c = first + warp; c <= last; c += kMergeWarps) {
-        const int64_t slot = ((int64_t)unit + c) * RB + row;
-        const float lse = p.ws_lse[slot];
-        float v[PER];
-        const float *src = p.ws_o + slot * HD + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(src);
-            v[0] = t.x;
-            v[1] = t.y;
-            v[2] = t.z;
-            v[3] = t.w;
-        } else {
-            const float2 t = *reinterpret_cast<const float2 *>(src);
-            v[0] = t.x;
-            v[1] = t.y;
-        }
-        if (lse == -INFINITY) continue;
-        if (lse > m) {
-            const float f = fast_exp2(m - lse);
-            l *= f;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] *= f;
-            m = lse;
-        }
-        const float f = fast_exp2(lse - m);
-        l += f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] += f * v[e];
-    }
-    if (lane == 0) {
-        sm_m[warp] = m;
-        sm_l[warp] = l;
-    }
-#pragma unroll
-    for (int e = 0; e < PER; ++e) sm_o[warp][lane * PER + e] = acc[e];
-    __syncthreads();
-    if (warp != 0) return;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float Lsum = 0.f;
-    float o[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) {
-            if (sm_m[w] == -INFINITY) continue;
-            const float f = fast_exp2(sm_m[w] - M);
-            Lsum += f * sm_l[w];
-#pragma unroll
-            for (int e = 0; e < PER; ++e) o[e] += f * sm_o[w][lane * PER + e];
-        }
-    }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    if constexpr (PER == 4) {
-        uint2 packed;
-        packed.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-        packed.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-        *reinterpret_cast<uint2 *>(dst) = packed;
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
     }
 }
 
@@ -933,10 +887,6 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
     }
     if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
-    if (launch_pdl(decode_merge_kernel<HD, G::RB>, dim3(ctas), dim3(kMergeWarps * 32), 0, stream,
-                   p) != cudaSuccess)
-        return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
 
@@ -959,11 +909,12 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
     plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
     const size_t units = (size_t)plan->batch_per_launch * n_kv_heads * plan->row_blocks;
-    // partial slots: unit + cta < units + grid; tables: N, Pb[B+1], cnt[B * row_blocks]
+    // partial slots: unit + cta < units + grid; then one counter per unit
     const size_t slots = units + plan->grid;
     const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
-    const size_t meta = (2 + (size_t)plan->batch_per_launch * (plan->row_blocks + 1)) * 4;
-    plan->workspace = ((partial + 255) & ~size_t(255)) + meta + 256;
+    plan->counter_offset = (partial + 255) & ~size_t(255);
+    plan->counter_bytes = units * sizeof(int32_t);
+    plan->workspace = plan->counter_offset + plan->counter_bytes;
     return ATTN_OK;
 }
 
@@ -984,7 +935,6 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
     const int rb_rows = plan.m_tiles == 0 ? 8 : 16 * plan.m_tiles;
     const size_t units = (size_t)plan.batch_per_launch * n_kv_heads * plan.row_blocks;
     const size_t slots = units + plan.grid;
-    const size_t partial = slots * rb_rows * ((size_t)plan.head_dim + 1) * sizeof(float);
     for (int b0 = 0; b0 < batch; b0 += plan.batch_per_launch) {
         const int nb = std::min(plan.batch_per_launch, batch - b0);
         const int64_t qo = (int64_t)b0 * q_rows * n_q_heads * plan.head_dim;
@@ -1019,8 +969,8 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.err = err;
         p.ws_o = static_cast<float *>(workspace);
         p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
-        p.ws_meta = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                                ((partial + 255) & ~size_t(255)));
+        p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                 plan.counter_offset);
         int rc;
         if (plan.head_dim == 128)
             rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, stream)

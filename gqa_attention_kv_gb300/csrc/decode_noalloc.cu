@@ -20,9 +20,10 @@
 //   * All calls share the one array.  Two calls whose kernels overlap on the
 //     GPU (different streams, no ordering between them) race on it and give
 //     wrong results; order them on one stream or with events.
-//   * Nothing in the array has to start at zero: every partial state the
-//     merge reads is written earlier in the same call, so the contents a
-//     previous call left behind are never read.
+//   * The decode keeps one counter per (request, KV head, row block) in its
+//     scratch, which must start at zero; each call clears them with a stream
+//     memset (no allocation) before its kernel runs.  Everything else a
+//     previous call left in the array is overwritten before it is read.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -82,6 +83,16 @@ extern "C" int attn_decode_noalloc(const void *q, const attn_kv_cache *cache,
     if (need > 0) {
         const int rc = scratch_address(&scratch);
         if (rc != ATTN_OK) return rc;
+        gqa::DecodePlan plan;
+        gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len,
+                         window, &plan);
+        const cudaError_t e =
+            cudaMemsetAsync(static_cast<unsigned char *>(scratch) + plan.counter_offset, 0,
+                            plan.counter_bytes, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            gqa::note_cuda_error(e);
+            return ATTN_ERR_CUDA;
+        }
     }
     return attn_decode(q, cache, seq_lens, positions, batch, q_rows, max_seq_len, window,
                        n_q_heads, n_kv_heads, head_dim, scale, out, scratch,

@@ -54,7 +54,8 @@ struct DecodePlan {
     int row_blocks;       // units along the query rows of one KV head
     int grid;             // CTAs of the split kernel
     int batch_per_launch;
-    size_t workspace;     // bytes of scratch: fp32 partial states + tables
+    size_t workspace;     // bytes of scratch: fp32 partial states + per-unit counters
+    size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
 };
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,

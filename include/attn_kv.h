@@ -123,9 +123,15 @@ int attn_kv_append(const void *k_new, const void *v_new, const int64_t *slot_map
 
 /*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
- * this shape (the fp32 partial softmax states of its cache splits).  The same
- * arguments must be passed to attn_decode.  0 means no workspace is needed.
- * Returns (size_t)-1 for arguments attn_decode would reject.
+ * this shape: fp32 partial softmax states of the keys pieces different CTAs
+ * handle, plus one counter per (request, KV head, row block).  The same
+ * arguments must be passed to attn_decode.  Returns (size_t)-1 for arguments
+ * attn_decode would reject.
+ *
+ * The workspace must be zero-filled before its first use; every call that
+ * completes leaves the counters at zero again, so a workspace kept for later
+ * calls needs no clearing (after a call that reported ATTN_ERR_TIMEOUT,
+ * zero it again).
  */
 size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_rows,
                                   int n_q_heads, int n_kv_heads, int head_dim, int max_seq_len,
@@ -162,9 +168,10 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  *   out        bf16 [batch, q_rows, n_q_heads, head_dim], device; rounded
  *              once from fp32 (round to nearest even).  A row with no valid
  *              key gets zeros.
- *   workspace  device scratch of at least
- *              attn_decode_workspace_size(...) bytes (may be NULL when that is
- *              0), 16-byte aligned; its contents are not needed between calls.
+ *   workspace  device scratch of at least attn_decode_workspace_size(...)
+ *              bytes, 16-byte aligned, zero-filled before its first use (see
+ *              attn_decode_workspace_size).  Calls whose kernels overlap on
+ *              the GPU need separate workspaces.
  */
 int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
                 const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
@@ -190,8 +197,9 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *   The first call on a device looks up the array's device address; make it
  *   before capturing a stream into a CUDA graph.
  *   All calls share the array: calls whose kernels overlap on the GPU race
- *   and give wrong results, so order them (one stream, or events).  No part
- *   of the array has to start at zero.
+ *   and give wrong results, so order them (one stream, or events).  Each
+ *   call clears the part of the array that must start at zero (a stream
+ *   memset, no allocation) before its kernel runs.
  */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int attn_decode_noalloc(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,

@@ -123,7 +123,7 @@ def test_graph_replay_follows_device_state():
     pos = case.positions.to(dev)
     slots = case.slot_mapping.to(dev)
     out = torch.empty_like(q)
-    ws = torch.empty(gq.attn_decode_workspace_size(cache, B, 1, Hq, cap, 0), dtype=torch.uint8,
+    ws = torch.zeros(gq.attn_decode_workspace_size(cache, B, 1, Hq, cap, 0), dtype=torch.uint8,
                      device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     s = torch.cuda.Stream()
