@@ -52,6 +52,7 @@ constexpr int kWarps = 4;                    // consumer warps = chunks per tile
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
 constexpr int kMaxTableEntries = 512;        // (request, row block) pairs per launch
+constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per CTA
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -266,7 +267,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     }
     __syncthreads();
     const int N = tb.Pb[B];
-    const int L = max(1, (N + p.grid - 1) / p.grid);
+    // equal shares, but at least kMinChunksPerCta so small problems do not
+    // spread a few keys over every SM
+    const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
     if (blockIdx.x == 0) {
         // units with no valid key get zeros (no CTA visits them)
         for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
@@ -822,32 +825,47 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
             if (*s_last) {
                 __threadfence();
+                // 1) every part's log-sum-exp of every row into shared memory
+                //    (the merge area is free again), 2) per row the max and the
+                //    weights, 3) the weighted outputs with independent loads.
+                const int parts = last - first + 1;
+                // the merge area holds kWarps * HD parts per row; beyond that
+                // (head_dim 64 and a unit spanning > 256 CTAs) read them directly
+                const bool staged = parts <= kWarps * HD;
+                float *sl = mo;  // [parts][RB]
+                if (staged) {
+                    for (int k = ctid; k < parts * RB; k += kWarps * 32) {
+                        const int c = k / RB, row = k - (k / RB) * RB;
+                        sl[k] = __ldcg(p.ws_lse + ((int64_t)sg.unit + first + c) * RB + row);
+                    }
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+                auto lse_of = [&](int c, int row) -> float {
+                    return staged ? sl[c * RB + row]
+                                  : __ldcg(p.ws_lse + ((int64_t)sg.unit + first + c) * RB + row);
+                };
                 for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
                     const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
                     const int i = row0 + row;
                     if (i >= row1) continue;
-                    float M = -INFINITY, Lsum = 0.f;
+                    float M = -INFINITY;
+                    for (int c = 0; c < parts; ++c) M = fmaxf(M, lse_of(c, row));
+                    float Lsum = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int c = first; c <= last; ++c) {
-                        const int64_t slot = ((int64_t)sg.unit + c) * RB + row;
-                        const float lse = __ldcg(p.ws_lse + slot);
-                        if (lse == -INFINITY) continue;
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
-                        if (lse > M) {
-                            const float f = fast_exp2(M - lse);
-                            Lsum *= f;
-                            acc.x *= f;
-                            acc.y *= f;
-                            acc.z *= f;
-                            acc.w *= f;
-                            M = lse;
+                    if (M != -INFINITY) {
+#pragma unroll 8
+                        for (int c = 0; c < parts; ++c) {
+                            const float lse = lse_of(c, row);
+                            const float f = lse == -INFINITY ? 0.f : fast_exp2(lse - M);
+                            const int64_t slot = ((int64_t)sg.unit + first + c) * RB + row;
+                            const float4 v =
+                                __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
+                            Lsum += f;
+                            acc.x += f * v.x;
+                            acc.y += f * v.y;
+                            acc.z += f * v.z;
+                            acc.w += f * v.w;
                         }
-                        const float f = fast_exp2(lse - M);
-                        Lsum += f;
-                        acc.x += f * v.x;
-                        acc.y += f * v.y;
-                        acc.z += f * v.z;
-                        acc.w += f * v.w;
                     }
                     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
                     const int r = i / p.group, g = i - (i / p.group) * p.group;
