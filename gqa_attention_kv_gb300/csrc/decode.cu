@@ -53,6 +53,8 @@ constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
 constexpr int kMaxTableEntries = 512;        // (request, row block) pairs per launch
 constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per CTA
+constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
+constexpr int kMergeWarps = 8;
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -78,6 +80,7 @@ struct Params {
     float *ws_o;
     float *ws_lse;
     int32_t *ws_count;  // per unit: partial states written so far (zero between calls)
+    int32_t *ws_meta;   // [0] = total chunks N; [1 .. B+1] = Pb; then cnt[B * row_blocks]
     int32_t *err;
 };
 
@@ -271,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     // spread a few keys over every SM
     const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
     if (blockIdx.x == 0) {
+        // tables for the merge kernel
+        for (int i = threadIdx.x; i <= B; i += kThreads) p.ws_meta[1 + i] = tb.Pb[i];
+        for (int i = threadIdx.x; i < B * RBc; i += kThreads) p.ws_meta[2 + B + i] = tb.cnt[i];
+        if (threadIdx.x == 0) p.ws_meta[0] = N;
         // units with no valid key get zeros (no CTA visits them)
         for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
             if (tb.cnt[i] != 0) continue;
@@ -812,12 +819,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 if (d == 0) p.ws_lse[slot] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
             }
         }
-        if (!sg.whole) {
-            // The CTA that stores a unit's last partial state merges all of
-            // them: parts in CTA order, online rescaling, one bf16 rounding.
+        const int first = sg.unit_start / L, last = (sg.unit_start + sg.n_u - 1) / L;
+        if (!sg.whole && last - first < kFusedMaxParts) {
+            // A unit spanning a few CTAs is merged by the CTA that stores its
+            // last partial state: parts in CTA order, one bf16 rounding.
             __threadfence();
             asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-            const int first = sg.unit_start / L, last = (sg.unit_start + sg.n_u - 1) / L;
             if (ctid == 0) {
                 const int prev = atomicAdd(p.ws_count + sg.unit, 1);
                 *s_last = (prev == last - first) ? 1 : 0;
@@ -883,8 +890,111 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     }
 }
 
+// Merge of units that span more than kFusedMaxParts CTAs: one CTA per
+// (request, KV head, query row of the group); its warps take the parts
+// round-robin (online max / sum per warp), and the warps' states are combined
+// in a fixed order, so the result does not depend on timing.
+template <int HD, int RB>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Params p) {
+    constexpr int PER = HD / 32;
+    __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
+    __shared__ __align__(16) float sm_o[kMergeWarps][HD];
+    pdl_wait();  // the partial states and tables come from the split kernel
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int b = cta / (p.rows * p.n_kv_heads);
+    const int rem = cta - b * p.rows * p.n_kv_heads;
+    const int kvh = rem / p.rows;
+    const int i = rem - kvh * p.rows;
+    const int rb = i / RB, row = i - rb * RB;
+    const int B = p.batch, RBc = p.row_blocks;
+    const int N = p.ws_meta[0];
+    const int *Pb = p.ws_meta + 1;
+    const int *cnt = p.ws_meta + 2 + B;
+    const int n_u = cnt[b * RBc + rb];
+    if (n_u == 0) return;  // zero-filled by the split kernel
+    const int per_head = (Pb[b + 1] - Pb[b]) / p.n_kv_heads;
+    int start = Pb[b] + kvh * per_head;
+    for (int r2 = 0; r2 < rb; ++r2) start += cnt[b * RBc + r2];
+    const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
+    const int first = start / L, last = (start + n_u - 1) / L;
+    if (last - first < kFusedMaxParts) return;  // written by the split kernel
+    const int unit = (b * p.n_kv_heads + kvh) * RBc + rb;
+    float m = -INFINITY, l = 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int c = first + warp; c <= last; c += kMergeWarps) {
+        const int64_t slot = ((int64_t)unit + c) * RB + row;
+        const float lse = p.ws_lse[slot];
+        float v[PER];
+        const float *src = p.ws_o + slot * HD + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            v[0] = t.x;
+            v[1] = t.y;
+            v[2] = t.z;
+            v[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            v[0] = t.x;
+            v[1] = t.y;
+        }
+        if (lse == -INFINITY) continue;
+        if (lse > m) {
+            const float f = fast_exp2(m - lse);
+            l *= f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] *= f;
+            m = lse;
+        }
+        const float f = fast_exp2(lse - m);
+        l += f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += f * v[e];
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) sm_o[warp][lane * PER + e] = acc[e];
+    __syncthreads();
+    if (warp != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm_m[w]);
+    float Lsum = 0.f;
+    float o[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            if (sm_m[w] == -INFINITY) continue;
+            const float f = fast_exp2(sm_m[w] - M);
+            Lsum += f * sm_l[w];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) o[e] += f * sm_o[w][lane * PER + e];
+        }
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    const int r = i / p.group, g = i - r * p.group;
+    __nv_bfloat16 *dst =
+        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD + lane * PER;
+    if constexpr (PER == 4) {
+        uint2 packed;
+        packed.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+        packed.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = packed;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
+    }
+}
+
 template <int HD, int MT>
-int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
+int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv, bool merge,
                  cudaStream_t stream) {
     using G = Geo<HD, MT>;
     static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
@@ -905,6 +1015,12 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
     }
     if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    if (merge) {
+        const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
+        if (launch_pdl(decode_merge_kernel<HD, G::RB>, dim3(ctas), dim3(kMergeWarps * 32), 0,
+                       stream, p) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
     return ATTN_OK;
 }
 
@@ -912,9 +1028,6 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
                 int head_dim, int max_seq_len, int window, DecodePlan *plan) {
-    (void)cache;
-    (void)max_seq_len;
-    (void)window;
     const int group = n_q_heads / n_kv_heads;
     plan->head_dim = head_dim;
     plan->rows = q_rows * group;
@@ -932,7 +1045,17 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
     plan->counter_offset = (partial + 255) & ~size_t(255);
     plan->counter_bytes = units * sizeof(int32_t);
-    plan->workspace = plan->counter_offset + plan->counter_bytes;
+    plan->meta_offset = plan->counter_offset + ((plan->counter_bytes + 255) & ~size_t(255));
+    const size_t meta = (2 + (size_t)plan->batch_per_launch * (plan->row_blocks + 1)) * 4;
+    plan->workspace = plan->meta_offset + meta;
+    // Can a unit span more than kFusedMaxParts CTAs?  Its chunks are at most
+    // the key bound / 16 + 1 and every CTA takes at least kMinChunksPerCta.
+    int64_t keys = max_seq_len;
+    if (window > 0) keys = std::min<int64_t>(keys, (int64_t)window + q_rows - 1);
+    if (cache->kind == ATTN_CACHE_RING) keys = std::min<int64_t>(keys, cache->slots_per_seq);
+    const int64_t max_chunks = (keys + dec::kChunk - 1) / dec::kChunk + 1;
+    const int64_t max_parts = (max_chunks + dec::kMinChunksPerCta - 1) / dec::kMinChunksPerCta + 1;
+    plan->merge_kernel = max_parts > dec::kFusedMaxParts;
     return ATTN_OK;
 }
 
@@ -989,15 +1112,17 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
         p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                  plan.counter_offset);
+        p.ws_meta = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                plan.meta_offset);
         int rc;
         if (plan.head_dim == 128)
-            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, stream)
-                                     : dec::launch_split<128, 2>(p, tk, tv, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, plan.merge_kernel, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, plan.merge_kernel, stream)
+                                     : dec::launch_split<128, 2>(p, tk, tv, plan.merge_kernel, stream);
         else
-            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, stream)
-                                     : dec::launch_split<64, 2>(p, tk, tv, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, plan.merge_kernel, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, plan.merge_kernel, stream)
+                                     : dec::launch_split<64, 2>(p, tk, tv, plan.merge_kernel, stream);
         if (rc != ATTN_OK) return rc;
     }
     return ATTN_OK;
