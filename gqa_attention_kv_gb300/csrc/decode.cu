@@ -855,23 +855,33 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
                     const int i = row0 + row;
                     if (i >= row1) continue;
+                    // parts <= kFusedMaxParts: one predicated batch, all loads in flight
+                    float lse[kFusedMaxParts];
+                    float4 v[kFusedMaxParts];
+#pragma unroll
+                    for (int c = 0; c < kFusedMaxParts; ++c) {
+                        lse[c] = -INFINITY;
+                        v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (c < parts) {
+                            const int64_t slot = ((int64_t)sg.unit + first + c) * RB + row;
+                            lse[c] = lse_of(c, row);
+                            v[c] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
+                        }
+                    }
                     float M = -INFINITY;
-                    for (int c = 0; c < parts; ++c) M = fmaxf(M, lse_of(c, row));
+#pragma unroll
+                    for (int c = 0; c < kFusedMaxParts; ++c) M = fmaxf(M, lse[c]);
                     float Lsum = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (M != -INFINITY) {
-#pragma unroll 8
-                        for (int c = 0; c < parts; ++c) {
-                            const float lse = lse_of(c, row);
-                            const float f = lse == -INFINITY ? 0.f : fast_exp2(lse - M);
-                            const int64_t slot = ((int64_t)sg.unit + first + c) * RB + row;
-                            const float4 v =
-                                __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
+#pragma unroll
+                        for (int c = 0; c < kFusedMaxParts; ++c) {
+                            const float f = fast_exp2(lse[c] - M);  // -inf gives 0
                             Lsum += f;
-                            acc.x += f * v.x;
-                            acc.y += f * v.y;
-                            acc.z += f * v.z;
-                            acc.w += f * v.w;
+                            acc.x += f * v[c].x;
+                            acc.y += f * v[c].y;
+                            acc.z += f * v[c].z;
+                            acc.w += f * v[c].w;
                         }
                     }
                     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
@@ -921,38 +931,55 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int first = start / L, last = (start + n_u - 1) / L;
     if (last - first < kFusedMaxParts) return;  // written by the split kernel
     const int unit = (b * p.n_kv_heads + kvh) * RBc + rb;
+    // Each warp takes parts first + warp + 8k; a batch of 8 of them is loaded
+    // at once (all loads in flight), then folded into the warp's state.
     float m = -INFINITY, l = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (int c = first + warp; c <= last; c += kMergeWarps) {
-        const int64_t slot = ((int64_t)unit + c) * RB + row;
-        const float lse = p.ws_lse[slot];
-        float v[PER];
-        const float *src = p.ws_o + slot * HD + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(src);
-            v[0] = t.x;
-            v[1] = t.y;
-            v[2] = t.z;
-            v[3] = t.w;
-        } else {
-            const float2 t = *reinterpret_cast<const float2 *>(src);
-            v[0] = t.x;
-            v[1] = t.y;
-        }
-        if (lse == -INFINITY) continue;
-        if (lse > m) {
-            const float f = fast_exp2(m - lse);
-            l *= f;
+    constexpr int kBatch = 8;
+    for (int c0 = first + warp; c0 <= last; c0 += kBatch * kMergeWarps) {
+        float lse[kBatch];
+        float v[kBatch][PER];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] *= f;
-            m = lse;
-        }
-        const float f = fast_exp2(lse - m);
-        l += f;
+        for (int k = 0; k < kBatch; ++k) {
+            const int c = c0 + k * kMergeWarps;
+            lse[k] = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] += f * v[e];
+            for (int e = 0; e < PER; ++e) v[k][e] = 0.f;
+            if (c <= last) {
+                const int64_t slot = ((int64_t)unit + c) * RB + row;
+                lse[k] = __ldcg(p.ws_lse + slot);
+                const float *src = p.ws_o + slot * HD + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    v[k][0] = t.x;
+                    v[k][1] = t.y;
+                    v[k][2] = t.z;
+                    v[k][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    v[k][0] = t.x;
+                    v[k][1] = t.y;
+                }
+            }
+        }
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, lse[k]);
+        if (mb == -INFINITY) continue;
+        const float fo = fast_exp2(m - mb);  // m == -inf gives 0
+        l *= fo;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] *= fo;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float f = fast_exp2(lse[k] - mb);  // -inf gives 0
+            l += f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] += f * v[k][e];
+        }
+        m = mb;
     }
     if (lane == 0) {
         sm_m[warp] = m;
