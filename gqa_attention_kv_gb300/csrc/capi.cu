@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "kernels.h"
@@ -156,6 +157,7 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
     int rc = check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim,
                                 max_seq_len, window);
     if (rc != ATTN_OK) return rc;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
     if (batch == 0) return ATTN_OK;
     if (!q || !seq_lens || !positions || !out || !cache->k || !cache->v) return ATTN_ERR_NULL;
     if (cache->kind == ATTN_CACHE_PAGED && !cache->block_table) return ATTN_ERR_NULL;
@@ -183,6 +185,7 @@ int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq
             return ATTN_ERR_UNSUPPORTED;
         return ATTN_ERR_SHAPE;
     }
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
     if (batch == 0 || seq_len == 0) return ATTN_OK;
     if (!q || !k || !v || !out) return ATTN_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_ALIGN;

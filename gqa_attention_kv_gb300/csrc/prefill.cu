@@ -297,16 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s[c] = valid ? s[c] : -INFINITY;
                 }
             }
-            // row max of the raw scores, four independent chains
+            // row max of the raw scores: three-input max, four independent chains
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-            for (int c = 4; c < kBN; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int c = 4; c < kBN; c += 8) {
+                mx0 = max3(mx0, s[c], s[c + 1]);
+                mx1 = max3(mx1, s[c + 2], s[c + 3]);
+                mx2 = max3(mx2, s[c + 4], s[c + 5]);
+                mx3 = max3(mx3, s[c + 6], s[c + 7]);
             }
-            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
             // lazy rescale: keep the reference max unless it grew by > 2^8
             float alpha = 1.f;
             if (mx > m_run + kRescaleThreshold || m_run == -INFINITY) {
@@ -334,11 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(s[c0 + 2 * e], sl2, -mref));
-                    const float p1 = fast_exp2(fmaf(s[c0 + 2 * e + 1], sl2, -mref));
-                    sum0 += p0;
-                    sum1 += p1;
-                    split_bf16x2(p0, p1, hi[e], lo[e]);
+                    float x0, x1;
+                    fma2(x0, x1, s[c0 + 2 * e], s[c0 + 2 * e + 1], sl2, sl2, -mref, -mref);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    add2(sum0, sum1, sum0, sum1, p0, p1);
+                    split_trunc_bf16x2(p0, p1, hi[e], lo[e]);
                 }
                 // P over its own S columns: hi at [0, 64), lo at [64, 128)
                 tmem_st_32x32b_x16(s_tmem + c0 / 2, hi);

@@ -216,6 +216,48 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uin
     lo = *reinterpret_cast<uint32_t *>(&l);
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// p0, p1 >= 0 as bf16 hi + lo: hi = the top 16 bits (truncation), lo =
+// round(p - hi).  hi + lo carries ~16 significant bits.
+__device__ __forceinline__ void split_trunc_bf16x2(float p0, float p1, uint32_t &hi,
+                                                   uint32_t &lo) {
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    hi = __byte_perm(b0, b1, 0x7632);  // upper halves: p0 -> low 16 bits, p1 -> high
+    float r0, r1;
+    sub2(r0, r1, p0, p1, __uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u));
+    lo = pack_bf16x2(r0, r1);
+}
+
 // 2^x via the MUFU base-2 exponential (approximate, flushes denormals).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

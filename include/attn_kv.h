@@ -164,7 +164,7 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  *              replays for any seq_lens up to it.  Keys beyond it are not read.
  *   window     sliding window in positions; <= 0 means none.  RING requires
  *              window > 0 and slots_per_seq >= window + q_rows - 1.
- *   scale      multiplies q.k before the natural-base softmax
+ *   scale      multiplies q.k before the natural-base softmax; finite and > 0
  *   out        bf16 [batch, q_rows, n_q_heads, head_dim], device; rounded
  *              once from fp32 (round to nearest even).  A row with no valid
  *              key gets zeros.
@@ -219,7 +219,7 @@ int attn_decode_noalloc(const void *q, const attn_kv_cache *cache, const int32_t
  *   q    bf16 [batch, seq_len, n_q_heads, head_dim], device
  *   k, v bf16 [batch, seq_len, n_kv_heads, head_dim], device
  *   Query i of a sequence attends keys t of the same sequence with t <= i and,
- *   when window > 0, i - t < window.
+ *   when window > 0, i - t < window.  scale (finite, > 0) multiplies q.k.
  *   out  bf16 [batch, seq_len, n_q_heads, head_dim], device, rounded once.
  */
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,

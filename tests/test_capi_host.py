@@ -95,6 +95,10 @@ def test_decode_validation(lib):
     assert decode_rc(lib, cache(gq.PAGED, sps=0, bt=bt, bs=16), L=512) == gq.ATTN_ERR_SHAPE
     # batch 0 is a no-op
     assert decode_rc(lib, cache(), B=0) == gq.ATTN_OK
+    # the scale must be finite and positive
+    cs = cache().struct()
+    assert lib.attn_decode(16, ctypes.byref(cs), 64, 128, 2, 1, 512, 0, 32, 8, 128, -1.0, 32,
+                           None, 0, None, None) == gq.ATTN_ERR_SHAPE
 
 
 def test_decode_workspace_checks(lib):
@@ -116,6 +120,9 @@ def test_prefill_validation(lib):
     assert f(16, 40, 48, 1, 100, 0, 32, 8, 128, 0.1, 72, None, None) == gq.ATTN_ERR_ALIGN
     assert f(16, 32, 48, 0, 100, 0, 32, 8, 128, 0.1, 64, None, None) == gq.ATTN_OK
     assert f(16, 32, 48, 1, 0, 0, 32, 8, 128, 0.1, 64, None, None) == gq.ATTN_OK
+    assert f(16, 32, 48, 1, 100, 0, 32, 8, 128, 0.0, 64, None, None) == gq.ATTN_ERR_SHAPE
+    assert f(16, 32, 48, 1, 100, 0, 32, 8, 128, -0.1, 64, None, None) == gq.ATTN_ERR_SHAPE
+    assert f(16, 32, 48, 1, 100, 0, 32, 8, 128, float("inf"), 64, None, None) == gq.ATTN_ERR_SHAPE
 
 
 def test_append_validation(lib):
