@@ -28,8 +28,10 @@
 //               (hi + lo, vibevoice.c "Attention backends": one rounding of P
 //               is too coarse), O rescaled in TMEM only when the running max
 //               grew by more than 2^8 (the result is unchanged; rescaling is
-//               lazy).  Epilogue: O / l -> bf16 -> shared (over Q_a) -> TMA
-//               store, clipped at the sequence end.
+//               lazy).  P is released in two halves of 64 keys, so PV on
+//               the first half runs while the second is exponentiated.
+//               Epilogue: O / l -> bf16 -> shared (over Q_a) -> TMA store,
+//               clipped at the sequence end.
 //
 // Ordering facts the schedule relies on: tcgen05.mma operations of one thread
 // execute in issue order, so S_a(j+1) = Q_a K^T, issued after O_a += P_a(j) V,
@@ -71,7 +73,7 @@ struct Cfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
     static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 8;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 10;
     static constexpr size_t kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 };
 
@@ -101,8 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *v_empty = v_full + C::kVStages;         // [kVStages]
     uint64_t *q_full = v_empty + C::kVStages;
     uint64_t *s_full = q_full + 1;                    // [2]
-    uint64_t *p_full = s_full + 2;                    // [2]
-    uint64_t *o_done = p_full + 2;
+    uint64_t *p_full = s_full + 2;                    // [2 tiles][2 key halves]
+    uint64_t *o_done = p_full + 4;
     uint64_t *mma_done = o_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
 
@@ -132,8 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
-        mbar_init(&p_full[0], 128);
-        mbar_init(&p_full[1], 128);
+        for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 128);
         mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -208,14 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&s_full[a]);
             };
-            auto issue_pv = [&](int a, int j) {
+            // O_a += P_a V for keys 64h .. 64h+63 of the tile (P hi, then P lo)
+            auto issue_pv_half = [&](int a, int j, int hh) {
                 const uint32_t v_addr = smem_u32(sV + (j % C::kVStages) * C::kVBytes);
                 const uint32_t p_tmem = tmem + a * 128;
                 const uint32_t o_tmem = tmem + 256 + a * HD;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)  // P hi, then P lo
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                        const int kk = hh * (kBN / 32) + k4;
                         // V tile: keys are rows (K), head_dim contiguous (N): MN-major.
                         const uint64_t bdesc =
                             smem_desc_sw128(v_addr + kk * 16 * 128, kBN * 128, 1024);
@@ -234,10 +237,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, p.err);
                 const bool more = j + 1 < n_kt;
                 for (int a = 0; a < 2 && ok; ++a) {
-                    ok = mbar_wait(&p_full[a], j & 1, p.err);
+                    // each half of P as soon as the softmax has written it
+                    for (int hh = 0; hh < 2 && ok; ++hh) {
+                        ok = mbar_wait(&p_full[a * 2 + hh], j & 1, p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv_half(a, j, hh);
+                    }
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(a, j);
                     if (a == 1) tc_commit(&v_empty[j % C::kVStages]);
                     if (more) {
                         if (a == 0) {
@@ -344,11 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P over its own S columns: hi at [0, 64), lo at [64, 128)
                 tmem_st_32x32b_x16(s_tmem + c0 / 2, hi);
                 tmem_st_32x32b_x16(s_tmem + 64 + c0 / 2, lo);
+                if (c0 == kBN / 2 - 32 || c0 == kBN - 32) {
+                    // keys of this half are in TMEM: let PV start on them
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&p_full[a * 2 + (c0 >= kBN / 2 ? 1 : 0)]);
+                }
             }
             l_run = l_run * alpha + (sum0 + sum1);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[a]);
         }
         // epilogue: wait for the last PV, normalise, store through shared memory
         if (ok) ok = mbar_wait(o_done, 0, p.err);
