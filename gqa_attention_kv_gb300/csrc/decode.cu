@@ -22,11 +22,12 @@
 //     to the output; the others leave fp32 partial states in the workspace,
 //     and the CTA that stores a unit's last partial (a per-unit counter tells
 //     it) merges them in CTA order and resets the counter.  One launch.
-//   * A producer warp streams 64-key tiles (four 16-key chunks).  A chunk
-//     whose 16 slots are consecutive (linear cache; a page of >= 16 slots; a
-//     ring away from its wrap point) is one 2D TMA box per 64 columns, landing
-//     128-byte-swizzled; any other chunk is gathered row by row with 16-byte
-//     cp.async into the same layout.  Page ids are fetched 32 at a time, one
+//   * A producer warp streams 64-key tiles (four 16-key chunks).  A tile
+//     whose 64 slots are consecutive (linear cache; a ring away from its wrap
+//     point) is one 2D TMA box of 64 rows per 64 columns; otherwise a chunk
+//     whose 16 slots are consecutive (a page of >= 16 slots) is a 16-row box;
+//     any other chunk is gathered row by row with 16-byte cp.async.  All land
+//     in the same 128-byte-swizzled [half][64 rows][128 B] tile layout.  Page ids are fetched 32 at a time, one
 //     per lane, ahead of the tiles that use them.
 //   * Four consumer warps each own one chunk of every tile: S = Q K^T and
 //     O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
@@ -110,11 +111,15 @@ struct Geo {
     static_assert(kStages >= 2, "at least a double-buffered ring");
 };
 
-// Byte offset of 16-byte piece `c16` (0 .. HD/8-1) of row `row` inside a chunk
-// laid out as [half][16 rows][128 B] with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t chunk_offset(int row, int c16) {
+constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
+
+// Byte offset of 16-byte piece `c16` (0 .. HD/8-1) of row `row` (0 .. 63)
+// inside a K or V tile laid out as [half][64 rows][128 B] with the 128-byte
+// swizzle; chunk c owns rows 16c .. 16c+15.  A 16-row TMA box fills one
+// chunk's rows of one half, a 64-row box a whole half.
+__device__ __forceinline__ uint32_t tile_offset(int row, int c16) {
     const int half = c16 >> 3, cc = c16 & 7;
-    return (uint32_t)(half * (kChunk * 128) + row * 128 + ((cc ^ (row & 7)) << 4));
+    return (uint32_t)(half * (kTileRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4));
 }
 
 // Key chunk range of unit (request b, row block rb): chunk c covers positions
@@ -206,7 +211,9 @@ struct SegmentWalker {
 template <int HD, int MT>
 __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_k64,
+                        const __grid_constant__ CUtensorMap tm_v64, const Params p) {
     using G = Geo<HD, MT>;
     constexpr int RB = G::RB;
     constexpr int kStages = G::kStages;
@@ -299,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_k64);
+            prefetch_tensormap(&tm_v64);
         }
         const bool paged = p.kind == ATTN_CACHE_PAGED;
         const bool paged_tma = paged && (p.block_size % kChunk == 0);
@@ -423,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                                 const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
                                                            s * row_elems + (int64_t)sg.kvh * HD +
                                                            c16 * 8;
-                                uint8_t *dst = (tensor ? vst : kst) + c * G::kChunkBytes +
-                                               chunk_offset(r, c16);
+                                uint8_t *dst =
+                                    (tensor ? vst : kst) + tile_offset(c * kChunk + r, c16);
                                 cp_async_16(dst, src);
                                 issued_cp = true;
                             }
@@ -435,23 +444,35 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         info_mask[st * kWarps + c] = mask;
                     }
                 }
-                // lane 0 announces the stage's TMA bytes, then lane c issues
-                // chunk c's boxes (four issuing threads instead of one)
+                // A tile whose 64 slots are consecutive is one 64-row box per
+                // 64 columns; otherwise lane c issues chunk c's 16-row boxes.
+                bool whole_tile = slot0[0] >= 0;
+#pragma unroll
+                for (int c = 1; c < kWarps; ++c) whole_tile = whole_tile && slot0[c] == slot0[0] + c * kChunk;
                 if (lane == 0 && tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
                 __syncwarp();
-                int64_t my_slot0 = slot0[0];
+                if (whole_tile) {
+                    // lanes 0 .. 2*kHalves-1: (tensor, half)
+                    if (lane < 2 * G::kHalves) {
+                        const int tensor = lane / G::kHalves, h = lane % G::kHalves;
+                        tma_load_2d((tensor ? vst : kst) + h * (kTileRows * 128),
+                                    tensor ? &tm_v64 : &tm_k64, sg.kvh * HD + h * 64,
+                                    (int)slot0[0], &full[st]);
+                    }
+                } else {
+                    int64_t my_slot0 = slot0[0];
 #pragma unroll
-                for (int c = 1; c < kWarps; ++c)
-                    if (lane == c) my_slot0 = slot0[c];
-                if (lane < kWarps && my_slot0 >= -1) {
-                    const int y = my_slot0 < 0 ? -kChunk : (int)my_slot0;
+                    for (int c = 1; c < kWarps; ++c)
+                        if (lane == c) my_slot0 = slot0[c];
+                    if (lane < kWarps && my_slot0 >= -1) {
+                        const int y = my_slot0 < 0 ? -kChunk : (int)my_slot0;
 #pragma unroll
-                    for (int h = 0; h < G::kHalves; ++h) {
-                        const int x = sg.kvh * HD + h * 64;
-                        tma_load_2d(kst + lane * G::kChunkBytes + h * kChunk * 128, &tm_k, x, y,
-                                    &full[st]);
-                        tma_load_2d(vst + lane * G::kChunkBytes + h * kChunk * 128, &tm_v, x, y,
-                                    &full[st]);
+                        for (int h = 0; h < G::kHalves; ++h) {
+                            const int x = sg.kvh * HD + h * 64;
+                            const uint32_t off = h * (kTileRows * 128) + lane * (kChunk * 128);
+                            tma_load_2d(kst + off, &tm_k, x, y, &full[st]);
+                            tma_load_2d(vst + off, &tm_v, x, y, &full[st]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -472,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
 
     // ---------------------------------------------------------------- consumers
     const int gq = lane >> 2, tq = lane & 3;
+    const int cr0 = warp * kChunk;  // this warp's chunk: rows cr0 .. cr0+15 of every tile
     const int ctid = threadIdx.x;  // 0 .. 127
     SegmentWalker walk{g0, g1};
     Segment sg;
@@ -522,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 if (t0 >= 0) {
                     const uint32_t mask16 = info_mask[st * kWarps + warp];
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
+                        smem_u32(stages + st * G::kStageBytes);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     const int m = lane >> 3;
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             uint32_t a[4];
                             ldmatrix_x4(a[0], a[1], a[2], a[3],
-                                        kbase + chunk_offset(key, kk * 2 + (m >> 1)));
+                                        kbase + tile_offset(cr0 + key, kk * 2 + (m >> 1)));
                             mma_bf16_16816(sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     }
@@ -583,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int md = 0; md < HD / 16; ++md) {
                             uint32_t a[4];
                             ldmatrix_x4_trans(a[0], a[1], a[2], a[3],
-                                              vbase + chunk_offset(key, md * 2 + (m & 1)));
+                                              vbase + tile_offset(cr0 + key, md * 2 + (m & 1)));
                             mma_bf16_16816(o[md], a, bh0, bh1);
                             mma_bf16_16816(o[md], a, bl0, bl1);
                         }
@@ -657,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 if (t0 >= 0) {
                     const uint32_t mask16 = info_mask[st * kWarps + warp];
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes + warp * G::kChunkBytes);
+                        smem_u32(stages + st * G::kStageBytes);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     float s[MT][2][4];
     #pragma unroll
@@ -672,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             uint32_t b00, b01, b10, b11;
                             ldmatrix_x4(b00, b01, b10, b11,
-                                        kbase + chunk_offset(key, kk * 2 + (m & 1)));
+                                        kbase + tile_offset(cr0 + key, kk * 2 + (m & 1)));
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_bf16_16816(s[mt][0], qa[mt][kk], b00, b01);
@@ -735,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int dn = 0; dn < HD / 16; ++dn) {
                             uint32_t v0, v1, v2, v3;
                             ldmatrix_x4_trans(v0, v1, v2, v3,
-                                              vbase + chunk_offset(key, dn * 2 + (m >> 1)));
+                                              vbase + tile_offset(cr0 + key, dn * 2 + (m >> 1)));
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
@@ -1021,7 +1043,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
 }
 
 template <int HD, int MT>
-int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv, bool merge,
+int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                 const CUtensorMap &tk64, const CUtensorMap &tv64, bool merge,
                  cudaStream_t stream) {
     using G = Geo<HD, MT>;
     static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
@@ -1040,7 +1063,8 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv, 
         }
         configured_device = dev;
     }
-    if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, p) != cudaSuccess)
+    if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, tk64, tv64, p) !=
+        cudaSuccess)
         return ATTN_ERR_CUDA;
     if (merge) {
         const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
@@ -1095,8 +1119,12 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
     const uint64_t dims[2] = {(uint64_t)n_kv_heads * plan.head_dim, (uint64_t)cache->num_slots};
     const uint64_t strides[1] = {(uint64_t)n_kv_heads * plan.head_dim * 2};
     const uint32_t box[2] = {64, (uint32_t)dec::kChunk};
+    const uint32_t box64[2] = {64, (uint32_t)dec::kTileRows};
+    CUtensorMap tk64, tv64;
     if (!encode_tensor_map(&tk, cache->k, 2, dims, strides, box, true) ||
-        !encode_tensor_map(&tv, cache->v, 2, dims, strides, box, true)) {
+        !encode_tensor_map(&tv, cache->v, 2, dims, strides, box, true) ||
+        !encode_tensor_map(&tk64, cache->k, 2, dims, strides, box64, true) ||
+        !encode_tensor_map(&tv64, cache->v, 2, dims, strides, box64, true)) {
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
@@ -1143,13 +1171,13 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                                                 plan.meta_offset);
         int rc;
         if (plan.head_dim == 128)
-            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, plan.merge_kernel, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, plan.merge_kernel, stream)
-                                     : dec::launch_split<128, 2>(p, tk, tv, plan.merge_kernel, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+                                     : dec::launch_split<128, 2>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream);
         else
-            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, plan.merge_kernel, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, plan.merge_kernel, stream)
-                                     : dec::launch_split<64, 2>(p, tk, tv, plan.merge_kernel, stream);
+            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+                                     : dec::launch_split<64, 2>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream);
         if (rc != ATTN_OK) return rc;
     }
     return ATTN_OK;
