@@ -96,7 +96,12 @@ struct Geo {
     static constexpr int kChunkBytes = kHalves * kChunk * 128;
     static constexpr int kTileBytes = kWarps * kChunkBytes;  // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kMergeBytes = kWarps * RB * HD * 4 + 2 * kWarps * RB * 4;
+    // At the end of a segment each warp parks its O rows (RB x HD fp32) in
+    // its own rows of the stage that held the segment's last tile (K and V,
+    // 2 * kHalves pieces of 16 x 128 B, which it has finished reading); only
+    // 32-row units need a dedicated area.  Row maxima and sums always have one.
+    static constexpr bool kParkInStage = RB * HD * 4 <= 2 * kHalves * kChunk * 128;
+    static constexpr int kMergeBytes = (kParkInStage ? 0 : kWarps * RB * HD * 4) + 2 * kWarps * RB * 4;
     static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
     // as many stages as the shared memory of kCtasPerSm CTAs allows (max 8)
     static constexpr int kBudget = (kCtasPerSm == 2 ? 115712 : 232448) - 1024 - kMergeBytes -
@@ -221,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    float *mo = reinterpret_cast<float *>(smem + G::kOffMerge);  // [kWarps][RB][HD]
-    float *mm = mo + kWarps * RB * HD;                           // [kWarps][RB]
+    float *mo = reinterpret_cast<float *>(smem + G::kOffMerge);  // [kWarps][RB][HD] (if !kParkInStage)
+    float *mm = mo + (G::kParkInStage ? 0 : kWarps * RB * HD);   // [kWarps][RB]
     float *ml = mm + kWarps * RB;                                // [kWarps][RB]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::kOffBars);
     uint64_t *empty = full + kStages;
@@ -499,6 +504,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     Segment sg;
     int tile = 0;
     bool ok = true;
+    // Partial segments merged by this CTA's end-of-share pass (a share cuts
+    // at most its first and its last unit), so that no fence or atomic
+    // stalls the stream in between.
+    Segment pend0, pend1;
+    int n_pend = 0;
     while (ok && walk.next(p, tb, sg)) {
         const int b = sg.b, kvh = sg.kvh;
         const int row0 = sg.rb * RB;
@@ -507,6 +517,21 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const int ring_lo = p.kind == ATTN_CACHE_RING ? seq_len - p.slots_per_seq : 0;
         const int window = p.window;
         const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
+        // the stage of the segment's last tile: its consumers keep it until
+        // the warps' states have been merged through it
+        const int st_last = (tile + n_tiles - 1) % kStages;
+        auto park = [&](int w, int row) -> float * {
+            if constexpr (!G::kParkInStage) {
+                return mo + ((size_t)w * RB + row) * HD;
+            } else {
+                constexpr int kRowsPerPiece = kChunk * 128 / (HD * 4);
+                const int piece = row / kRowsPerPiece;
+                const int tensor = piece / G::kHalves, h = piece - tensor * G::kHalves;
+                uint8_t *base = stages + st_last * G::kStageBytes + tensor * G::kTileBytes +
+                                h * (kTileRows * 128) + w * (kChunk * 128);
+                return reinterpret_cast<float *>(base + (row - piece * kRowsPerPiece) * HD * 4);
+            }
+        };
         if constexpr (MT == 0) {
             // ---- up to 8 rows: S^T = K Q^T (keys x rows), O^T = V^T P^T (d x rows)
             // Q^T as the B operand: thread holds row gq, d pairs 2tq (+8) of each k-step
@@ -612,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);
+                if (lane == 0 && it + 1 < n_tiles) mbar_arrive(&empty[st]);
             }
             // the row sums are spread over the 8 lanes that share tq
 #pragma unroll
@@ -623,14 +648,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 l += __shfl_xor_sync(0xffffffffu, l, 16);
                 l_run[e] = l;
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
+            __syncwarp();  // the warp's reads of the last tile are done
 #pragma unroll
             for (int md = 0; md < HD / 16; ++md)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = 2 * tq + (e & 1);
                     const int d = md * 16 + gq + (e >> 1) * 8;
-                    mo[((size_t)warp * RB + row) * HD + d] = o[md][e];
+                    park(warp, row)[d] = o[md][e];
                 }
             if (gq == 0) {
 #pragma unroll
@@ -769,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);
+                if (lane == 0 && it + 1 < n_tiles) mbar_arrive(&empty[st]);
             }
             // ---- end of segment: merge the four warps through shared memory
     #pragma unroll
@@ -781,13 +806,13 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     l += __shfl_xor_sync(0xffffffffu, l, 2);
                     l_run[mt][hr] = l;
                 }
-            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // merge area free
+            __syncwarp();  // the warp's reads of the last tile are done
     #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
     #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int row = mt * 16 + gq + hr * 8;
-                    float *dst = mo + ((size_t)warp * RB + row) * HD;
+                    float *dst = park(warp, row);
     #pragma unroll
                     for (int n = 0; n < HD / 8; ++n)
                         *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
@@ -816,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const float f = fast_exp2(mw - M);
                     Lsum += ml[w * RB + row] * f;
                     const float4 v =
-                        *reinterpret_cast<const float4 *>(mo + ((size_t)w * RB + row) * HD + d);
+                        *reinterpret_cast<const float4 *>(park(w, row) + d);
                     acc.x += f * v.x;
                     acc.y += f * v.y;
                     acc.z += f * v.z;
@@ -841,84 +866,90 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 if (d == 0) p.ws_lse[slot] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
             }
         }
-        const int first = sg.unit_start / L, last = (sg.unit_start + sg.n_u - 1) / L;
-        if (!sg.whole && last - first < kFusedMaxParts) {
-            // A unit spanning a few CTAs is merged by the CTA that stores its
-            // last partial state: parts in CTA order, one bf16 rounding.
-            __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-            if (ctid == 0) {
-                const int prev = atomicAdd(p.ws_count + sg.unit, 1);
-                *s_last = (prev == last - first) ? 1 : 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-            if (*s_last) {
-                __threadfence();
-                // 1) every part's log-sum-exp of every row into shared memory
-                //    (the merge area is free again), 2) per row the max and the
-                //    weights, 3) the weighted outputs with independent loads.
-                const int parts = last - first + 1;
-                // the merge area holds kWarps * HD parts per row; beyond that
-                // (head_dim 64 and a unit spanning > 256 CTAs) read them directly
-                const bool staged = parts <= kWarps * HD;
-                float *sl = mo;  // [parts][RB]
-                if (staged) {
-                    for (int k = ctid; k < parts * RB; k += kWarps * 32) {
-                        const int c = k / RB, row = k - (k / RB) * RB;
-                        sl[k] = __ldcg(p.ws_lse + ((int64_t)sg.unit + first + c) * RB + row);
-                    }
-                }
-                asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-                auto lse_of = [&](int c, int row) -> float {
-                    return staged ? sl[c * RB + row]
-                                  : __ldcg(p.ws_lse + ((int64_t)sg.unit + first + c) * RB + row);
-                };
-                for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
-                    const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
-                    const int i = row0 + row;
-                    if (i >= row1) continue;
-                    // parts <= kFusedMaxParts: one predicated batch, all loads in flight
-                    float lse[kFusedMaxParts];
-                    float4 v[kFusedMaxParts];
-#pragma unroll
-                    for (int c = 0; c < kFusedMaxParts; ++c) {
-                        lse[c] = -INFINITY;
-                        v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (c < parts) {
-                            const int64_t slot = ((int64_t)sg.unit + first + c) * RB + row;
-                            lse[c] = lse_of(c, row);
-                            v[c] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
-                        }
-                    }
-                    float M = -INFINITY;
-#pragma unroll
-                    for (int c = 0; c < kFusedMaxParts; ++c) M = fmaxf(M, lse[c]);
-                    float Lsum = 0.f;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (M != -INFINITY) {
-#pragma unroll
-                        for (int c = 0; c < kFusedMaxParts; ++c) {
-                            const float f = fast_exp2(lse[c] - M);  // -inf gives 0
-                            Lsum += f;
-                            acc.x += f * v[c].x;
-                            acc.y += f * v[c].y;
-                            acc.z += f * v[c].z;
-                            acc.w += f * v[c].w;
-                        }
-                    }
-                    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-                    const int r = i / p.group, g = i - (i / p.group) * p.group;
-                    __nv_bfloat16 *dst =
-                        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD +
-                        d;
-                    uint2 packed;
-                    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2 *>(dst) = packed;
-                }
-                if (ctid == 0) p.ws_count[sg.unit] = 0;  // ready for the next call
-            }
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // parked rows read
+        if (lane == 0) mbar_arrive(&empty[st_last]);
+        if (!sg.whole && (sg.unit_start + sg.n_u - 1) / L - sg.unit_start / L < kFusedMaxParts) {
+            if (n_pend == 0)
+                pend0 = sg;
+            else
+                pend1 = sg;
+            n_pend = min(n_pend + 1, 2);
         }
+    }
+    if (n_pend == 0) return;
+    // ---- end of share: a unit spanning a few CTAs is merged by the CTA that
+    // stores its last partial state (per-unit counter): parts in CTA order,
+    // one bf16 rounding.  The ring is drained, so the stages are free.
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    if (ctid == 0) {
+        for (int k = 0; k < n_pend; ++k) {
+            const Segment &u = k == 0 ? pend0 : pend1;
+            const int first = u.unit_start / L, last = (u.unit_start + u.n_u - 1) / L;
+            const int prev = atomicAdd(p.ws_count + u.unit, 1);
+            s_last[k] = (prev == last - first) ? 1 : 0;
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    float *sl = reinterpret_cast<float *>(stages);  // [parts][RB] log-sum-exps
+    for (int k = 0; k < n_pend; ++k) {
+        if (!s_last[k]) continue;  // uniform across the consumer warps
+        __threadfence();
+        const Segment &u = k == 0 ? pend0 : pend1;
+        const int first = u.unit_start / L, last = (u.unit_start + u.n_u - 1) / L;
+        const int parts = last - first + 1;  // <= kFusedMaxParts
+        const int row0 = u.rb * RB, row1 = min(p.rows, row0 + RB);
+        // 1) every part's log-sum-exp of every row into shared memory, 2) per
+        // row the max and the weights, 3) the weighted outputs, all loads of
+        // a row in flight at once.
+        for (int i = ctid; i < parts * RB; i += kWarps * 32) {
+            const int c = i / RB, row = i - (i / RB) * RB;
+            sl[i] = __ldcg(p.ws_lse + ((int64_t)u.unit + first + c) * RB + row);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+        for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
+            const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+            const int i = row0 + row;
+            if (i >= row1) continue;
+            float lse[kFusedMaxParts];
+            float4 v[kFusedMaxParts];
+#pragma unroll
+            for (int c = 0; c < kFusedMaxParts; ++c) {
+                lse[c] = -INFINITY;
+                v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < parts) {
+                    const int64_t slot = ((int64_t)u.unit + first + c) * RB + row;
+                    lse[c] = sl[c * RB + row];
+                    v[c] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kFusedMaxParts; ++c) M = fmaxf(M, lse[c]);
+            float Lsum = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int c = 0; c < kFusedMaxParts; ++c) {
+                    const float f = fast_exp2(lse[c] - M);  // -inf gives 0
+                    Lsum += f;
+                    acc.x += f * v[c].x;
+                    acc.y += f * v[c].y;
+                    acc.z += f * v[c].z;
+                    acc.w += f * v[c].w;
+                }
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            const int r = i / p.group, g = i - (i / p.group) * p.group;
+            __nv_bfloat16 *dst =
+                p.out + (((int64_t)u.b * p.q_rows + r) * p.n_q_heads + u.kvh * p.group + g) * HD + d;
+            uint2 packed;
+            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(dst) = packed;
+        }
+        if (ctid == 0) p.ws_count[u.unit] = 0;  // ready for the next call
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // staging reused
     }
 }
 
