@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
+        // Lane c (mod kWarps) describes chunk c of each tile; the warp agrees
+        // on the tile's form with ballots, so a tile costs a few dozen
+        // instructions on the issuing path.
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const bool paged_tma = paged && (p.block_size % kChunk == 0);
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
+        const int c = lane & (kWarps - 1);
         SegmentWalker walk{g0, g1};
         Segment sg;
         int tile = 0;  // tiles issued by this CTA (stage / phase counter)
@@ -325,21 +329,16 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         while (ok && walk.next(p, tb, sg)) {
             const int bg = p.b_base + sg.b;  // request index in the whole cache
             const int32_t *bt = paged ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
-            // page id holding position t (or -1), read straight from the table
-            auto page_of = [&](int t) -> int64_t {
-                const int pi = t / p.block_size;
-                if (pi >= p.max_blocks) return -1;
-                const int v = bt[pi];
-                return (v < 0 || v >= num_pages) ? -1 : (int64_t)v;
-            };
-            auto slot_of = [&](int t) -> int64_t {
+            // raw table entry at page index pi (range-checked when used)
+            auto table_at = [&](int pi) -> int { return pi < p.max_blocks ? bt[pi] : -1; };
+            auto slot_of = [&](int t) -> int64_t {  // slot of position t, or -1
                 int64_t s;
                 if (p.kind == ATTN_CACHE_LINEAR) {
                     s = (int64_t)bg * p.slots_per_seq + t;
                 } else if (paged) {
-                    const int64_t pg = page_of(t);
-                    if (pg < 0) return -1;
-                    s = pg * p.block_size + t % p.block_size;
+                    const int v = table_at(t / p.block_size);
+                    if (v < 0 || v >= num_pages) return -1;
+                    s = (int64_t)v * p.block_size + t % p.block_size;
                 } else {
                     s = (int64_t)bg * p.slots_per_seq + t % p.slots_per_seq;
                 }
@@ -347,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             };
             const int seq_len = tb.seqlen[sg.b];
             const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
-            int win_base = -1;  // page index held by lane 0 of the prefetch window
-            int pg_reg = -1;
+            // page ids of two consecutive 32-page windows, one per lane; the
+            // second is fetched a window ahead of its use
+            int win = -1, pg_cur = -1, pg_next = -1;
             for (int it = 0; it < n_tiles && ok; ++it, ++tile) {
                 const int st = tile % kStages;
                 if (tile >= kStages) ok = mbar_wait(&empty[st], ((tile / kStages) - 1) & 1, p.err);
@@ -356,104 +356,79 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 uint8_t *kst = stages + st * G::kStageBytes;
                 uint8_t *vst = kst + G::kTileBytes;
                 const int chunk0 = sg.c_begin + it * kWarps;
+                const int chunk = chunk0 + c;
+                const int t0 = chunk * kChunk;
+                // slot0 >= 0: first of 16 consecutive slots (TMA box); -1: a
+                // contiguous chunk whose page is out of range (box aimed
+                // outside the tensor, zero-filled, keys masked); -2: gathered
+                // row by row; -3: absent
+                int64_t slot0 = -3;
                 if (paged_tma) {
-                    // refill the per-lane page-id window when this tile leaves it
-                    const int last = min(sg.c_end, chunk0 + kWarps) - 1;
-                    const int pi_first = chunk0 * kChunk / p.block_size;
-                    const int pi_last = last * kChunk / p.block_size;
-                    if (win_base < 0 || pi_last >= win_base + 32) {
-                        win_base = pi_first;
-                        const int pi = win_base + lane;
-                        pg_reg = -1;
-                        if (pi < p.max_blocks) {
-                            const int v = bt[pi];
-                            pg_reg = (v < 0 || v >= num_pages) ? -1 : v;
-                        }
+                    const int pi0 = chunk0 * kChunk / p.block_size;
+                    if (win < 0 || pi0 >= win + 64) {
+                        win = pi0;
+                        pg_cur = table_at(win + lane);
+                        pg_next = table_at(win + 32 + lane);
+                    } else if (pi0 >= win + 32) {
+                        win += 32;
+                        pg_cur = pg_next;
+                        pg_next = table_at(win + 32 + lane);
                     }
-                }
-                // Describe the tile's chunks: slot0[c] >= 0 is the first of 16
-                // consecutive slots (one TMA box per 64 columns); -1 marks a
-                // contiguous chunk whose page is out of bounds (the box is
-                // aimed outside the tensor, zero-filled, keys masked); -2 is
-                // gathered row by row; -3 is absent.
-                int64_t slot0[kWarps];
-                uint32_t tma_bytes = 0;
-                bool issued_cp = false;
-#pragma unroll
-                for (int c = 0; c < kWarps; ++c) {
-                    const int chunk = chunk0 + c;
-                    const int t0 = chunk * kChunk;
-                    int pv = -1;
-                    if (paged_tma) {  // every lane takes part in the shuffle
-                        const int pi = t0 / p.block_size;
-                        pv = __shfl_sync(0xffffffffu, pg_reg, (pi - win_base) & 31);
-                    }
-                    int64_t s0 = -3;
-                    if (chunk < sg.c_end) {
-                        if (p.kind == ATTN_CACHE_LINEAR) {
-                            s0 = (int64_t)bg * p.slots_per_seq + t0;
-                        } else if (paged_tma) {
-                            s0 = pv < 0 ? -1 : (int64_t)pv * p.block_size + t0 % p.block_size;
-                        } else if (paged) {
-                            s0 = -2;
-                        } else {
-                            const int j0 = t0 % p.slots_per_seq;
-                            s0 = (j0 + kChunk <= p.slots_per_seq)
-                                     ? (int64_t)bg * p.slots_per_seq + j0
-                                     : -2;
-                        }
-                    }
-                    slot0[c] = s0;
-                    if (s0 == -3) {
-                        if (lane == 0) info_t0[st * kWarps + c] = -1;
-                        continue;
-                    }
-                    uint32_t mask;
-                    if (s0 != -2) {
-                        mask = 0xFFFFu;
-                        if (s0 == -1) {
-                            mask = 0;
-                            if (t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
-                        }
-                        tma_bytes += 2 * G::kChunkBytes;
+                    const int rel = t0 / p.block_size - win;  // < 64 for a present chunk
+                    const int va = __shfl_sync(0xffffffffu, pg_cur, rel & 31);
+                    const int vb = __shfl_sync(0xffffffffu, pg_next, rel & 31);
+                    const int v = rel < 32 ? va : vb;
+                    if (chunk < sg.c_end)
+                        slot0 = (v < 0 || v >= num_pages)
+                                    ? -1
+                                    : (int64_t)v * p.block_size + t0 % p.block_size;
+                } else if (chunk < sg.c_end) {
+                    if (p.kind == ATTN_CACHE_LINEAR) {
+                        slot0 = (int64_t)bg * p.slots_per_seq + t0;
+                    } else if (paged) {
+                        slot0 = -2;
                     } else {
-                        mask = 0;
-                        for (int r = 0; r < kChunk; ++r) {
-                            const int64_t s = slot_of(t0 + r);
-                            if (s >= 0)
-                                mask |= 1u << r;
-                            else if (t0 + r < seq_len)
-                                report_error(p.err, ATTN_ERR_BOUNDS);
-                        }
-                        if (lane != 0) {
-                            // lanes 1..31 gather the chunk's K and V rows
-                            constexpr int kPieces = kChunk * (HD / 8);
-                            for (int pc = lane - 1; pc < 2 * kPieces; pc += 31) {
-                                const int tensor = pc / kPieces;
-                                const int rem = pc - tensor * kPieces;
-                                const int r = rem / (HD / 8), c16 = rem % (HD / 8);
-                                int64_t s = slot_of(t0 + r);
-                                if (s < 0) s = 0;  // masked row: read any valid slot
-                                const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
-                                                           s * row_elems + (int64_t)sg.kvh * HD +
-                                                           c16 * 8;
-                                uint8_t *dst =
-                                    (tensor ? vst : kst) + tile_offset(c * kChunk + r, c16);
-                                cp_async_16(dst, src);
-                                issued_cp = true;
-                            }
-                        }
-                    }
-                    if (lane == 0) {
-                        info_t0[st * kWarps + c] = t0;
-                        info_mask[st * kWarps + c] = mask;
+                        const int j0 = t0 % p.slots_per_seq;
+                        slot0 = (j0 + kChunk <= p.slots_per_seq)
+                                    ? (int64_t)bg * p.slots_per_seq + j0
+                                    : -2;
                     }
                 }
-                // A tile whose 64 slots are consecutive is one 64-row box per
-                // 64 columns; otherwise lane c issues chunk c's 16-row boxes.
-                bool whole_tile = slot0[0] >= 0;
-#pragma unroll
-                for (int c = 1; c < kWarps; ++c) whole_tile = whole_tile && slot0[c] == slot0[0] + c * kChunk;
+                if (lane < kWarps && slot0 == -1 && t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
+                const unsigned lanes = (1u << kWarps) - 1;
+                const unsigned boxed = __ballot_sync(0xffffffffu, slot0 >= -1) & lanes;
+                const unsigned gathered = __ballot_sync(0xffffffffu, slot0 == -2) & lanes;
+                const int64_t slot00 = __shfl_sync(0xffffffffu, slot0, 0);
+                // a tile whose 64 slots are consecutive is one 64-row box per
+                // 64 columns; otherwise each boxed chunk is a 16-row box
+                const bool whole_tile =
+                    __all_sync(0xffffffffu, slot0 == slot00 + (int64_t)c * kChunk) && slot00 >= 0;
+                // gathered chunks: lane l copies row l % 16 of K (l < 16) or V
+                uint32_t gmask = 0;
+                bool issued_cp = false;
+                for (unsigned bits = gathered; bits; bits &= bits - 1) {
+                    const int gc = __ffs(bits) - 1;
+                    const int gt0 = (chunk0 + gc) * kChunk;
+                    const int r = lane & (kChunk - 1), tensor = lane >> 4;
+                    const int64_t s = slot_of(gt0 + r);
+                    const unsigned valid = __ballot_sync(0xffffffffu, s >= 0) & 0xFFFFu;
+                    if (lane < kChunk && s < 0 && gt0 + r < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
+                    if (lane == gc) gmask = valid;
+                    // a masked row reads slot 0 (any valid slot will do)
+                    const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
+                                               (s < 0 ? 0 : s) * row_elems + (int64_t)sg.kvh * HD;
+                    uint8_t *dst = tensor ? vst : kst;
+#pragma unroll 4
+                    for (int c16 = 0; c16 < HD / 8; ++c16)
+                        cp_async_16(dst + tile_offset(gc * kChunk + r, c16), src + c16 * 8);
+                    issued_cp = true;
+                }
+                if (lane < kWarps) {
+                    info_t0[st * kWarps + lane] = slot0 == -3 ? -1 : t0;
+                    info_mask[st * kWarps + lane] =
+                        slot0 >= 0 ? 0xFFFFu : (slot0 == -1 ? 0u : gmask);
+                }
+                const uint32_t tma_bytes = __popc(boxed) * 2 * G::kChunkBytes;
                 if (lane == 0 && tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
                 __syncwarp();
                 if (whole_tile) {
@@ -462,32 +437,23 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         const int tensor = lane / G::kHalves, h = lane % G::kHalves;
                         tma_load_2d((tensor ? vst : kst) + h * (kTileRows * 128),
                                     tensor ? &tm_v64 : &tm_k64, sg.kvh * HD + h * 64,
-                                    (int)slot0[0], &full[st]);
+                                    (int)slot00, &full[st]);
                     }
-                } else {
-                    int64_t my_slot0 = slot0[0];
+                } else if (lane < kWarps && slot0 >= -1) {
+                    const int y = slot0 < 0 ? -kChunk : (int)slot0;
 #pragma unroll
-                    for (int c = 1; c < kWarps; ++c)
-                        if (lane == c) my_slot0 = slot0[c];
-                    if (lane < kWarps && my_slot0 >= -1) {
-                        const int y = my_slot0 < 0 ? -kChunk : (int)my_slot0;
-#pragma unroll
-                        for (int h = 0; h < G::kHalves; ++h) {
-                            const int x = sg.kvh * HD + h * 64;
-                            const uint32_t off = h * (kTileRows * 128) + lane * (kChunk * 128);
-                            tma_load_2d(kst + off, &tm_k, x, y, &full[st]);
-                            tma_load_2d(vst + off, &tm_v, x, y, &full[st]);
-                        }
+                    for (int h = 0; h < G::kHalves; ++h) {
+                        const int x = sg.kvh * HD + h * 64;
+                        const uint32_t off = h * (kTileRows * 128) + lane * (kChunk * 128);
+                        tma_load_2d(kst + off, &tm_k, x, y, &full[st]);
+                        tma_load_2d(vst + off, &tm_v, x, y, &full[st]);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full[st]);
-                } else if (issued_cp) {
+                if (issued_cp)
                     cp_async_arrive_noinc(&full[st]);
-                } else {
+                else
                     mbar_arrive(&full[st]);
-                }
             }
         }
         // the gathered rows of this thread must land before it leaves
