@@ -24,10 +24,11 @@
 //     it) merges them in CTA order and resets the counter.  One launch.
 //   * A producer warp streams 64-key tiles (four 16-key chunks).  A tile
 //     whose 64 slots are consecutive (linear cache; a ring away from its wrap
-//     point) is one 2D TMA box of 64 rows per 64 columns; otherwise a chunk
-//     whose 16 slots are consecutive (a page of >= 16 slots) is a 16-row box;
-//     any other chunk is gathered row by row with 16-byte cp.async.  All land
-//     in the same 128-byte-swizzled [half][64 rows][128 B] tile layout.  Page ids are fetched 32 at a time, one
+//     point) is one TMA box of 64 rows per tensor; otherwise a chunk whose 16
+//     slots are consecutive (a page of >= 16 slots) is a 16-row box; any
+//     other chunk is gathered row by row with 16-byte cp.async.  Boxes are
+//     3D, {64 columns, rows, halves of the head}, so one box brings a whole
+//     head row; they land 128-byte-swizzled.  Page ids are fetched 32 at a time, one
 //     per lane, ahead of the tiles that use them.
 //   * Four consumer warps each own one chunk of every tile: S = Q K^T and
 //     O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
@@ -55,7 +56,7 @@ constexpr int kProducerWarp = kWarps;
 constexpr int kMaxTableEntries = 512;        // (request, row block) pairs per launch
 constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per CTA
 constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -81,7 +82,7 @@ struct Params {
     float *ws_o;
     float *ws_lse;
     int32_t *ws_count;  // per unit: partial states written so far (zero between calls)
-    int32_t *ws_meta;   // [0] = total chunks N; [1 .. B+1] = Pb; then cnt[B * row_blocks]
+    int2 *ws_parts;     // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     int32_t *err;
 };
 
@@ -110,7 +111,8 @@ struct Geo {
     static constexpr int kOffMerge = kStages * kStageBytes;
     static constexpr int kOffBars = kOffMerge + kMergeBytes;
     static constexpr int kOffInfo = kOffBars + 2 * kStages * 8;
-    static constexpr int kOffTable = kOffInfo + 2 * kStages * kWarps * 4 + 16;
+    // info: t0[kStages][kWarps], mask[kStages][kWarps], whole[kStages], last[4]
+    static constexpr int kOffTable = kOffInfo + ((2 * kStages * kWarps + kStages + 4) * 4 + 15) / 16 * 16;
     // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
     static constexpr size_t kSmem = 1024 + kOffTable + kTableBytes;
     static_assert(kStages >= 2, "at least a double-buffered ring");
@@ -118,13 +120,22 @@ struct Geo {
 
 constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
 
-// Byte offset of 16-byte piece `c16` (0 .. HD/8-1) of row `row` (0 .. 63)
-// inside a K or V tile laid out as [half][64 rows][128 B] with the 128-byte
-// swizzle; chunk c owns rows 16c .. 16c+15.  A 16-row TMA box fills one
-// chunk's rows of one half, a 64-row box a whole half.
-__device__ __forceinline__ uint32_t tile_offset(int row, int c16) {
+// A stage holds the K and V of one 64-key tile, each in one of two
+// 128-byte-swizzled layouts (an 8-row group always spans 1024 aligned bytes):
+//   whole tile (one TMA box of 64 rows): [half][64 rows][128 B]
+//   chunked    (16-row boxes / rows)   : [chunk][half][16 rows][128 B]
+// Chunk c's rows start at chunk_base() and its halves are half_stride() apart.
+template <int HD>
+__device__ __forceinline__ uint32_t chunk_base(bool whole, int c) {
+    return whole ? (uint32_t)c * (kChunk * 128) : (uint32_t)c * ((HD / 64) * kChunk * 128);
+}
+__device__ __forceinline__ uint32_t half_stride(bool whole) {
+    return whole ? (uint32_t)(kTileRows * 128) : (uint32_t)(kChunk * 128);
+}
+// Offset of 16-byte piece c16 (0 .. HD/8-1) of row `key` (0 .. 15) of a chunk.
+__device__ __forceinline__ uint32_t piece_offset(uint32_t hstride, int key, int c16) {
     const int half = c16 >> 3, cc = c16 & 7;
-    return (uint32_t)(half * (kTileRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4));
+    return half * hstride + key * 128 + ((cc ^ (key & 7)) << 4);
 }
 
 // Key chunk range of unit (request b, row block rb): chunk c covers positions
@@ -172,6 +183,7 @@ struct Segment {
     int unit;
     int unit_start, n_u; // the unit's chunks in the global order: [unit_start, +n_u)
     bool whole;          // the piece is the whole unit
+    bool head;           // the piece starts the unit
 };
 
 // The segments of global chunk range [g, g_end), in order.
@@ -208,6 +220,7 @@ struct SegmentWalker {
         s.unit_start = unit_start;
         s.n_u = n_u;
         s.whole = (off == 0 && seg_end == unit_start + n_u);
+        s.head = off == 0;
         g = seg_end;
         return true;
     }
@@ -233,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     uint64_t *empty = full + kStages;
     int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
     uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
-    int *s_last = reinterpret_cast<int *>(info_mask + kStages * kWarps);
+    int *info_whole = reinterpret_cast<int *>(info_mask + kStages * kWarps);  // [kStages]
+    int *s_last = info_whole + kStages;
     Tables tb;
     tb.cnt = reinterpret_cast<int *>(smem + G::kOffTable);
     tb.clo = tb.cnt + kMaxTableEntries;
@@ -247,6 +261,13 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             mbar_init(&empty[s], kWarps);  // one arrival per consumer warp
         }
         fence_barrier_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        // the maps are launch parameters: fetch them while the previous kernel drains
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_k64);
+        prefetch_tensormap(&tm_v64);
     }
     pdl_wait();  // the cache, positions and seq_lens may come from the previous kernel
     pdl_launch_dependents();
@@ -286,14 +307,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     // spread a few keys over every SM
     const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
     if (blockIdx.x == 0) {
-        // tables for the merge kernel
-        for (int i = threadIdx.x; i <= B; i += kThreads) p.ws_meta[1 + i] = tb.Pb[i];
-        for (int i = threadIdx.x; i < B * RBc; i += kThreads) p.ws_meta[2 + B + i] = tb.cnt[i];
-        if (threadIdx.x == 0) p.ws_meta[0] = N;
         // units with no valid key get zeros (no CTA visits them)
         for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
             if (tb.cnt[i] != 0) continue;
             const int b = i / RBc, rb = i - (i / RBc) * RBc;
+            for (int kvh = 0; kvh < p.n_kv_heads; ++kvh)
+                p.ws_parts[(b * p.n_kv_heads + kvh) * RBc + rb] = make_int2(0, -1);
             for (int row = rb * RB; row < min(p.rows, (rb + 1) * RB); ++row) {
                 const int r = row / p.group, g = row - r * p.group;
                 for (int kvh = 0; kvh < p.n_kv_heads; ++kvh) {
@@ -311,12 +330,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         // Lane c (mod kWarps) describes chunk c of each tile; the warp agrees
         // on the tile's form with ballots, so a tile costs a few dozen
         // instructions on the issuing path.
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_k64);
-            prefetch_tensormap(&tm_v64);
-        }
         const bool paged = p.kind == ATTN_CACHE_PAGED;
         const bool paged_tma = paged && (p.block_size % kChunk == 0);
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
@@ -420,9 +433,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     uint8_t *dst = tensor ? vst : kst;
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD / 8; ++c16)
-                        cp_async_16(dst + tile_offset(gc * kChunk + r, c16), src + c16 * 8);
+                        cp_async_16(dst + chunk_base<HD>(false, gc) +
+                                        piece_offset(half_stride(false), r, c16),
+                                    src + c16 * 8);
                     issued_cp = true;
                 }
+                if (lane == 0) info_whole[st] = whole_tile ? 1 : 0;
                 if (lane < kWarps) {
                     info_t0[st * kWarps + lane] = slot0 == -3 ? -1 : t0;
                     info_mask[st * kWarps + lane] =
@@ -431,23 +447,17 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 const uint32_t tma_bytes = __popc(boxed) * 2 * G::kChunkBytes;
                 if (lane == 0 && tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
                 __syncwarp();
+                // boxes {64 columns, rows, halves} of the caches viewed as
+                // [half index = kv head * halves + half][slot][64 columns]
                 if (whole_tile) {
-                    // lanes 0 .. 2*kHalves-1: (tensor, half)
-                    if (lane < 2 * G::kHalves) {
-                        const int tensor = lane / G::kHalves, h = lane % G::kHalves;
-                        tma_load_2d((tensor ? vst : kst) + h * (kTileRows * 128),
-                                    tensor ? &tm_v64 : &tm_k64, sg.kvh * HD + h * 64,
-                                    (int)slot00, &full[st]);
-                    }
+                    if (lane < 2)
+                        tma_load_3d(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, (int)slot00,
+                                    sg.kvh * G::kHalves, &full[st]);
                 } else if (lane < kWarps && slot0 >= -1) {
                     const int y = slot0 < 0 ? -kChunk : (int)slot0;
-#pragma unroll
-                    for (int h = 0; h < G::kHalves; ++h) {
-                        const int x = sg.kvh * HD + h * 64;
-                        const uint32_t off = h * (kTileRows * 128) + lane * (kChunk * 128);
-                        tma_load_2d(kst + off, &tm_k, x, y, &full[st]);
-                        tma_load_2d(vst + off, &tm_v, x, y, &full[st]);
-                    }
+                    const uint32_t off = chunk_base<HD>(false, lane);
+                    tma_load_3d(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st]);
+                    tma_load_3d(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st]);
                 }
                 __syncwarp();
                 if (issued_cp)
@@ -464,7 +474,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
 
     // ---------------------------------------------------------------- consumers
     const int gq = lane >> 2, tq = lane & 3;
-    const int cr0 = warp * kChunk;  // this warp's chunk: rows cr0 .. cr0+15 of every tile
     const int ctid = threadIdx.x;  // 0 .. 127
     SegmentWalker walk{g0, g1};
     Segment sg;
@@ -477,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     int n_pend = 0;
     while (ok && walk.next(p, tb, sg)) {
         const int b = sg.b, kvh = sg.kvh;
+        if (sg.head && ctid == 0)  // for the merge kernel: the CTAs holding the unit
+            p.ws_parts[sg.unit] = make_int2(sg.unit_start / L, (sg.unit_start + sg.n_u - 1) / L);
         const int row0 = sg.rb * RB;
         const int row1 = min(p.rows, row0 + RB);
         const int seq_len = tb.seqlen[b];
@@ -493,8 +504,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 constexpr int kRowsPerPiece = kChunk * 128 / (HD * 4);
                 const int piece = row / kRowsPerPiece;
                 const int tensor = piece / G::kHalves, h = piece - tensor * G::kHalves;
+                const bool wl = info_whole[st_last] != 0;
                 uint8_t *base = stages + st_last * G::kStageBytes + tensor * G::kTileBytes +
-                                h * (kTileRows * 128) + w * (kChunk * 128);
+                                chunk_base<HD>(wl, w) + h * half_stride(wl);
                 return reinterpret_cast<float *>(base + (row - piece * kRowsPerPiece) * HD * 4);
             }
         };
@@ -534,8 +546,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 const int t0 = info_t0[st * kWarps + warp];
                 if (t0 >= 0) {
                     const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const bool whole = info_whole[st] != 0;
+                    const uint32_t hs = half_stride(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     const int m = lane >> 3;
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
@@ -545,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             uint32_t a[4];
                             ldmatrix_x4(a[0], a[1], a[2], a[3],
-                                        kbase + tile_offset(cr0 + key, kk * 2 + (m >> 1)));
+                                        kbase + piece_offset(hs, key, kk * 2 + (m >> 1)));
                             mma_bf16_16816(sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     }
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int md = 0; md < HD / 16; ++md) {
                             uint32_t a[4];
                             ldmatrix_x4_trans(a[0], a[1], a[2], a[3],
-                                              vbase + tile_offset(cr0 + key, md * 2 + (m & 1)));
+                                              vbase + piece_offset(hs, key, md * 2 + (m & 1)));
                             mma_bf16_16816(o[md], a, bh0, bh1);
                             mma_bf16_16816(o[md], a, bl0, bl1);
                         }
@@ -669,8 +683,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 const int t0 = info_t0[st * kWarps + warp];
                 if (t0 >= 0) {
                     const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const bool whole = info_whole[st] != 0;
+                    const uint32_t hs = half_stride(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     float s[MT][2][4];
     #pragma unroll
@@ -685,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             uint32_t b00, b01, b10, b11;
                             ldmatrix_x4(b00, b01, b10, b11,
-                                        kbase + tile_offset(cr0 + key, kk * 2 + (m & 1)));
+                                        kbase + piece_offset(hs, key, kk * 2 + (m & 1)));
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_bf16_16816(s[mt][0], qa[mt][kk], b00, b01);
@@ -748,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int dn = 0; dn < HD / 16; ++dn) {
                             uint32_t v0, v1, v2, v3;
                             ldmatrix_x4_trans(v0, v1, v2, v3,
-                                              vbase + tile_offset(cr0 + key, dn * 2 + (m >> 1)));
+                                              vbase + piece_offset(hs, key, dn * 2 + (m >> 1)));
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_bf16_16816(o[mt][dn * 2], pa[mt], v0, v1);
@@ -937,26 +953,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int kvh = rem / p.rows;
     const int i = rem - kvh * p.rows;
     const int rb = i / RB, row = i - rb * RB;
-    const int B = p.batch, RBc = p.row_blocks;
-    const int N = p.ws_meta[0];
-    const int *Pb = p.ws_meta + 1;
-    const int *cnt = p.ws_meta + 2 + B;
-    const int n_u = cnt[b * RBc + rb];
-    if (n_u == 0) return;  // zero-filled by the split kernel
-    const int per_head = (Pb[b + 1] - Pb[b]) / p.n_kv_heads;
-    int start = Pb[b] + kvh * per_head;
-    for (int r2 = 0; r2 < rb; ++r2) start += cnt[b * RBc + r2];
-    const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
-    const int first = start / L, last = (start + n_u - 1) / L;
-    if (last - first < kFusedMaxParts) return;  // written by the split kernel
-    const int unit = (b * p.n_kv_heads + kvh) * RBc + rb;
-    // Each warp takes parts first + warp + 8k; a batch of 8 of them is loaded
-    // at once (all loads in flight), then folded into the warp's state.
+    const int unit = (b * p.n_kv_heads + kvh) * p.row_blocks + rb;
+    const int2 parts = __ldcg(p.ws_parts + unit);
+    const int first = parts.x, last = parts.y;
+    // no keys (zero-filled) or few parts (merged by the split kernel)
+    if (last - first < kFusedMaxParts) return;
+    // Each warp takes parts first + warp + kMergeWarps * k; a batch of kBatch
+    // of them is loaded at once (all loads in flight), then folded into the
+    // warp's state.
     float m = -INFINITY, l = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 10;
     for (int c0 = first + warp; c0 <= last; c0 += kBatch * kMergeWarps) {
         float lse[kBatch];
         float v[kBatch][PER];
@@ -1094,7 +1103,7 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->counter_offset = (partial + 255) & ~size_t(255);
     plan->counter_bytes = units * sizeof(int32_t);
     plan->meta_offset = plan->counter_offset + ((plan->counter_bytes + 255) & ~size_t(255));
-    const size_t meta = (2 + (size_t)plan->batch_per_launch * (plan->row_blocks + 1)) * 4;
+    const size_t meta = units * sizeof(int2);
     plan->workspace = plan->meta_offset + meta;
     // Can a unit span more than kFusedMaxParts CTAs?  Its chunks are at most
     // the key bound / 16 + 1 and every CTA takes at least kMinChunksPerCta.
@@ -1111,17 +1120,19 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
                   void *out, void *workspace, int32_t *err, cudaStream_t stream) {
-    // TMA maps over the caches viewed as [num_slots, n_kv_heads * head_dim].
-    CUtensorMap tk, tv;
-    const uint64_t dims[2] = {(uint64_t)n_kv_heads * plan.head_dim, (uint64_t)cache->num_slots};
-    const uint64_t strides[1] = {(uint64_t)n_kv_heads * plan.head_dim * 2};
-    const uint32_t box[2] = {64, (uint32_t)dec::kChunk};
-    const uint32_t box64[2] = {64, (uint32_t)dec::kTileRows};
-    CUtensorMap tk64, tv64;
-    if (!encode_tensor_map(&tk, cache->k, 2, dims, strides, box, true) ||
-        !encode_tensor_map(&tv, cache->v, 2, dims, strides, box, true) ||
-        !encode_tensor_map(&tk64, cache->k, 2, dims, strides, box64, true) ||
-        !encode_tensor_map(&tv64, cache->v, 2, dims, strides, box64, true)) {
+    // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][64]
+    // (a half is 64 columns, 128 bytes, of one head's row): a box of
+    // {64, rows, halves} brings both halves of `rows` slots of one head.
+    const int halves = plan.head_dim / 64;
+    const uint64_t dims[3] = {64, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
+    const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * 2, 128};
+    const uint32_t box[3] = {64, (uint32_t)dec::kChunk, (uint32_t)halves};
+    const uint32_t box64[3] = {64, (uint32_t)dec::kTileRows, (uint32_t)halves};
+    CUtensorMap tk, tv, tk64, tv64;
+    if (!encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true) ||
+        !encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true) ||
+        !encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true) ||
+        !encode_tensor_map(&tv64, cache->v, 3, dims, strides, box64, true)) {
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
@@ -1164,8 +1175,8 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
         p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                  plan.counter_offset);
-        p.ws_meta = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                                plan.meta_offset);
+        p.ws_parts = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) +
+                                              plan.meta_offset);
         int rc;
         if (plan.head_dim == 128)
             rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)

@@ -56,7 +56,7 @@ struct DecodePlan {
     int batch_per_launch;
     size_t workspace;     // bytes of scratch: fp32 partial states + per-unit counters
     size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
-    size_t meta_offset;   // chunk tables for the merge kernel
+    size_t meta_offset;   // per unit (first, last) CTA of its chunks, for the merge kernel
     bool merge_kernel;    // some unit may span more CTAs than the in-kernel merge takes
 };
 
