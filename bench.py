@@ -57,6 +57,28 @@ def load_peaks():
 # algorithmic work
 # --------------------------------------------------------------------------
 
+# DRAM bytes (read + write) of one full-size Qwen2-7B prompt prefill launch,
+# T = 14,449, from ncu (profiles/prefill_kernel_qwen14449_dram.md).  They
+# describe the kernel built from these exact sources and are dropped (null)
+# once either file changes.
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 199434752,
+                   "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
+                               "gqa_attention_kv_gb300/csrc/ptx.cuh"),
+                   "sha256": "8a356ae3717b34f6badb57bcc20130eca18a587c66e87eab52d1dccbfbbdc04a"}
+
+
+def prefill_traffic(T):
+    import hashlib
+
+    if T != PREFILL_TRAFFIC["T"]:
+        return None
+    h = hashlib.sha256()
+    for f in PREFILL_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return PREFILL_TRAFFIC["bytes"] if h.hexdigest() == PREFILL_TRAFFIC["sha256"] else None
+
+
 def prefill_flops(T, Hq, D, window=0):
     """4 * D * Hq * (unmasked query-key pairs): QK^T and PV, 2 flops per MAC."""
     if window and window > 0:
@@ -106,6 +128,15 @@ class ClockSampler:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: hold the timed region until the
+        # first sample is on disk, so every sample falls inside it
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None:
+            self.f.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -576,7 +607,7 @@ def cpu_sample(workload_name, steps=1, warmup=0, budget_s=None, max_rows=160):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen",
@@ -692,7 +723,9 @@ def main():
         roof = {"kernel": f"gqa::pre::prefill_kernel<{getattr(wl, 'D', 128)}>",
                 "bound": "tensor",
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None,
+                "frac": round(ach / peak, 4),
+                "traffic": prefill_traffic(getattr(wl, "T", None)),
+                "traffic_unit": "DRAM bytes per launch (ncu)",
                 "peak_source": f"{peak_src} bf16_tflops (burst)"}
     else:
         dominant = "decode"
