@@ -53,19 +53,19 @@ constexpr int kBN = 128;          // keys per tile
 constexpr int kThreads = 384;     // 3 warpgroups
 // Registers: launched at 168 per thread (384 x 168 = 64,512; three warps of
 // 168 fit one SM sub-partition's 16,384).  The TMA/MMA warpgroup then drops
-// to 56 and the two softmax warpgroups rise to 224: 4x32x56 + 8x32x224 =
-// 64,512, exactly the launch total, and 56 + 224 + 224 <= 512 per
+// to 72 and the two softmax warpgroups rise to 216: 4x32x72 + 8x32x216 =
+// 64,512, exactly the launch total, and 72 + 216 + 216 <= 512 per
 // sub-partition lane slot.
-constexpr uint32_t kRegsControl = 56;
-constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int HD>
 struct Cfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kKStages = HD == 128 ? 3 : 4;
-    static constexpr int kVStages = HD == 128 ? 2 : 4;
+    static constexpr int kKStages = HD == 128 ? 2 : 4;
+    static constexpr int kVStages = HD == 128 ? 3 : 4;
     static constexpr int kQBytes = kBM * HD * 2;  // one Q tile
     static constexpr int kKBytes = kBN * HD * 2;
     static constexpr int kVBytes = kBN * HD * 2;
@@ -121,6 +121,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key_lo = p.window > 0 ? max(0, q0 - p.window + 1) : 0;
     const int kt0 = key_lo / kBN;
     const int n_kt = (key_hi + kBN - 1) / kBN - kt0;
+    // The G heads of a KV group read the same K/V tiles; each starts its walk
+    // over them at a different tile (the order of the tiles does not change
+    // the result of the online softmax), so the CTAs resident at one time do
+    // not all ask L2 for the same lines at once.
+    const int rot = n_kt > 0 ? (int)(((int64_t)(h % p.group) * n_kt) / p.group) : 0;
+    auto tile_of = [&](int j) { const int t = j + rot; return kt0 + (t >= n_kt ? t - n_kt : t); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kKStages; ++s) {
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&k_full[st], C::kKBytes);
                     for (int hf = 0; hf < C::kHalves; ++hf)
                         tma_load_3d(sK + st * C::kKBytes + hf * (kBN * 128), &tm_k,
-                                    g * HD + hf * 64, (kt0 + kj) * kBN, b, &k_full[st]);
+                                    g * HD + hf * 64, tile_of(kj) * kBN, b, &k_full[st]);
                     ++kj;
                 } else {
                     const int st = vj % C::kVStages;
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&v_full[st], C::kVBytes);
                     for (int hf = 0; hf < C::kHalves; ++hf)
                         tma_load_3d(sV + st * C::kVBytes + hf * (kBN * 128), &tm_v,
-                                    g * HD + hf * 64, (kt0 + vj) * kBN, b, &v_full[st]);
+                                    g * HD + hf * 64, tile_of(vj) * kBN, b, &v_full[st]);
                     ++vj;
                 }
             }
@@ -196,22 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, 0, 1);
-            const uint32_t q_addr = smem_u32(sQ);
-            auto issue_qk = [&](int a, int j) {
-                const uint32_t k_addr = smem_u32(sK + (j % C::kKStages) * C::kKBytes);
-                const uint32_t qa = q_addr + a * C::kQBytes;
+            // Descriptors are built once; a k-step adds its byte offset >> 4 to
+            // the start-address field (no carry: shared addresses < 256 KB).
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            // V tile: keys are rows (K), head_dim contiguous (N): MN-major.
+            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sV), kBN * 128, 1024);
+            auto issue_qk = [&](int a, int kst) {
+                const uint64_t qd = q_desc + (uint64_t)((a * C::kQBytes) >> 4);
+                const uint64_t kd = k_desc0 + (uint64_t)((kst * C::kKBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    tc_mma_ss(tmem + a * 128, smem_desc_sw128(qa + off, 16, 1024),
-                              smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk,
-                              kk > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                    tc_mma_ss(tmem + a * 128, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[a]);
             };
             // O_a += P_a V for keys 64h .. 64h+63 of the tile (P hi, then P lo)
-            auto issue_pv_half = [&](int a, int j, int hh) {
-                const uint32_t v_addr = smem_u32(sV + (j % C::kVStages) * C::kVBytes);
+            auto issue_pv_half = [&](int a, int vst, int hh, bool first) {
+                const uint64_t vd = v_desc0 + (uint64_t)((vst * C::kVBytes) >> 4);
                 const uint32_t p_tmem = tmem + a * 128;
                 const uint32_t o_tmem = tmem + 256 + a * HD;
 #pragma unroll
@@ -219,11 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k4 = 0; k4 < kBN / 32; ++k4) {
                         const int kk = hh * (kBN / 32) + k4;
-                        // V tile: keys are rows (K), head_dim contiguous (N): MN-major.
-                        const uint64_t bdesc =
-                            smem_desc_sw128(v_addr + kk * 16 * 128, kBN * 128, 1024);
-                        tc_mma_ts(o_tmem, p_tmem + part * 64 + kk * 8, bdesc, idesc_pv,
-                                  (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                        tc_mma_ts(o_tmem, p_tmem + part * 64 + kk * 8,
+                                  vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                                  (!first || k4 > 0 || part > 0) ? 1u : 0u);
                     }
             };
             bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
@@ -233,30 +240,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_qk(1, 0);
                 tc_commit(&k_empty[0]);
             }
+            // stage indices and phases of the K and V rings, stepped without division
+            int vst = 0, vph = 0, kst = 0, kph = 0;
             for (int j = 0; j < n_kt && ok; ++j) {
-                ok = mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, p.err);
+                ok = mbar_wait(&v_full[vst], vph, p.err);
                 const bool more = j + 1 < n_kt;
+                if (more && ++kst == C::kKStages) {
+                    kst = 0;
+                    kph ^= 1;
+                }
                 for (int a = 0; a < 2 && ok; ++a) {
                     // each half of P as soon as the softmax has written it
                     for (int hh = 0; hh < 2 && ok; ++hh) {
                         ok = mbar_wait(&p_full[a * 2 + hh], j & 1, p.err);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv_half(a, j, hh);
+                        issue_pv_half(a, vst, hh, j == 0 && hh == 0);
                     }
                     if (!ok) break;
-                    if (a == 1) tc_commit(&v_empty[j % C::kVStages]);
+                    if (a == 1) tc_commit(&v_empty[vst]);
                     if (more) {
                         if (a == 0) {
-                            const int nj = j + 1;
-                            ok = mbar_wait(&k_full[nj % C::kKStages], (nj / C::kKStages) & 1,
-                                           p.err);
+                            ok = mbar_wait(&k_full[kst], kph, p.err);
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        issue_qk(a, j + 1);
-                        if (a == 1) tc_commit(&k_empty[(j + 1) % C::kKStages]);
+                        issue_qk(a, kst);
+                        if (a == 1) tc_commit(&k_empty[kst]);
                     }
+                }
+                if (++vst == C::kVStages) {
+                    vst = 0;
+                    vph ^= 1;
                 }
             }
             tc_commit(o_done);
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 96));
                 tmem_wait_ld();
             }
-            const int key0 = (kt0 + j) * kBN;
+            const int key0 = tile_of(j) * kBN;
             const bool needs_mask =
                 key0 + kBN - 1 > qa0 || (p.window > 0 && qa0 + kBM - 1 - key0 >= p.window);
             if (needs_mask) {
