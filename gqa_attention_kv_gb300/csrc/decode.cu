@@ -102,7 +102,8 @@ struct Geo {
     // 2 * kHalves pieces of 16 x 128 B, which it has finished reading); only
     // 32-row units need a dedicated area.  Row maxima and sums always have one.
     static constexpr bool kParkInStage = RB * HD * 4 <= 2 * kHalves * kChunk * 128;
-    static constexpr int kMergeBytes = (kParkInStage ? 0 : kWarps * RB * HD * 4) + 2 * kWarps * RB * 4;
+    // + per row and warp: max, sum, combined weight; per row: log-sum-exp
+    static constexpr int kMergeBytes = (kParkInStage ? 0 : kWarps * RB * HD * 4) + (3 * kWarps + 1) * RB * 4;
     static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
     // as many stages as the shared memory of kCtasPerSm CTAs allows (max 8)
     static constexpr int kBudget = (kCtasPerSm == 2 ? 115712 : 232448) - 1024 - kMergeBytes -
@@ -242,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     float *mo = reinterpret_cast<float *>(smem + G::kOffMerge);  // [kWarps][RB][HD] (if !kParkInStage)
     float *mm = mo + (G::kParkInStage ? 0 : kWarps * RB * HD);   // [kWarps][RB]
     float *ml = mm + kWarps * RB;                                // [kWarps][RB]
+    float *wgt = ml + kWarps * RB;                               // [RB][kWarps]
+    float *rlse = wgt + kWarps * RB;                             // [RB]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::kOffBars);
     uint64_t *empty = full + kStages;
     int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
@@ -497,14 +500,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         // the stage of the segment's last tile: its consumers keep it until
         // the warps' states have been merged through it
         const int st_last = (tile + n_tiles - 1) % kStages;
-        auto park = [&](int w, int row) -> float * {
+        // wl: the layout flag of stage st_last (read once per segment end)
+        auto park = [&](bool wl, int w, int row) -> float * {
             if constexpr (!G::kParkInStage) {
                 return mo + ((size_t)w * RB + row) * HD;
             } else {
                 constexpr int kRowsPerPiece = kChunk * 128 / (HD * 4);
                 const int piece = row / kRowsPerPiece;
                 const int tensor = piece / G::kHalves, h = piece - tensor * G::kHalves;
-                const bool wl = info_whole[st_last] != 0;
                 uint8_t *base = stages + st_last * G::kStageBytes + tensor * G::kTileBytes +
                                 chunk_base<HD>(wl, w) + h * half_stride(wl);
                 return reinterpret_cast<float *>(base + (row - piece * kRowsPerPiece) * HD * 4);
@@ -513,26 +516,29 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         if constexpr (MT == 0) {
             // ---- up to 8 rows: S^T = K Q^T (keys x rows), O^T = V^T P^T (d x rows)
             // Q^T as the B operand: thread holds row gq, d pairs 2tq (+8) of each k-step
+            // Loads are unconditional (a padding row reads the unit's first
+            // row, whose scores are then masked and never stored), so nothing
+            // waits on them before the first tile's MMAs.
             uint32_t qb[HD / 16][2];
             {
-                const int i = row0 + gq;
-                const bool valid = i < row1;
-                const int r = valid ? i / p.group : 0;
-                const int g = valid ? i - r * p.group : 0;
+                const int i = row0 + gq < row1 ? row0 + gq : row0;
+                const int r = i / p.group, g = i - r * p.group;
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
                     p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    qb[kk][0] = valid ? __ldg(qrow + kk * 8 + tq) : 0u;
-                    qb[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+                    qb[kk][0] = __ldg(qrow + kk * 8 + tq);
+                    qb[kk][1] = __ldg(qrow + kk * 8 + 4 + tq);
                 }
             }
             // this thread's S^T columns are rows 2tq and 2tq+1
             int cpos[2];
+            bool cvalid[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int i = row0 + 2 * tq + e;
-                cpos[e] = i < row1 ? p.positions[(int64_t)b * p.q_rows + i / p.group] : -1;
+                cvalid[e] = i < row1;
+                cpos[e] = __ldg(p.positions + (int64_t)b * p.q_rows + (cvalid[e] ? i : row0) / p.group);
             }
             float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
             float o[HD / 16][4];  // m-tile md: (d = 16md + gq (+8), rows 2tq, 2tq+1)
@@ -572,8 +578,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         for (int hk = 0; hk < 2; ++hk) {
                             const int n = gq + hk * 8;
                             const int t = t0 + n;
-                            const bool valid = ((mask16 >> n) & 1u) && t < seq_len && t <= pos &&
-                                               t >= ring_lo && (window <= 0 || pos - t < window);
+                            const bool valid = cvalid[e] && ((mask16 >> n) & 1u) && t < seq_len &&
+                                               t <= pos && t >= ring_lo &&
+                                               (window <= 0 || pos - t < window);
                             const float v = valid ? sacc[e + 2 * hk] * p.scale_log2 : -INFINITY;
                             sacc[e + 2 * hk] = v;
                             mx = fmaxf(mx, v);
@@ -629,13 +636,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 l_run[e] = l;
             }
             __syncwarp();  // the warp's reads of the last tile are done
+            const bool wl = info_whole[st_last] != 0;
 #pragma unroll
             for (int md = 0; md < HD / 16; ++md)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = 2 * tq + (e & 1);
                     const int d = md * 16 + gq + (e >> 1) * 8;
-                    park(warp, row)[d] = o[md][e];
+                    park(wl, warp, row)[d] = o[md][e];
                 }
             if (gq == 0) {
 #pragma unroll
@@ -645,23 +653,25 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 }
             }
         } else {
+            // unconditional loads, as in the MT = 0 path
             uint32_t qa[MT][HD / 16][4];
             int rpos[MT][2];
+            bool rvalid[MT][2];
     #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
     #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int i = row0 + mt * 16 + gq + hr * 8;
-                    const bool valid = i < row1;
-                    const int r = valid ? i / p.group : 0;
-                    const int g = valid ? i - r * p.group : 0;
-                    rpos[mt][hr] = valid ? p.positions[(int64_t)b * p.q_rows + r] : -1;
+                    const int i0 = row0 + mt * 16 + gq + hr * 8;
+                    rvalid[mt][hr] = i0 < row1;
+                    const int i = rvalid[mt][hr] ? i0 : row0;
+                    const int r = i / p.group, g = i - r * p.group;
+                    rpos[mt][hr] = __ldg(p.positions + (int64_t)b * p.q_rows + r);
                     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
                         p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
     #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        qa[mt][kk][hr] = valid ? __ldg(qrow + kk * 8 + tq) : 0u;
-                        qa[mt][kk][2 + hr] = valid ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+                        qa[mt][kk][hr] = __ldg(qrow + kk * 8 + tq);
+                        qa[mt][kk][2 + hr] = __ldg(qrow + kk * 8 + 4 + tq);
                     }
                 }
             }
@@ -722,8 +732,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                                 for (int e = 0; e < 2; ++e) {
                                     const int n = j * 8 + tq * 2 + e;
                                     const int t = t0 + n;
-                                    const bool valid = ((mask16 >> n) & 1u) && t < seq_len &&
-                                                       t <= pos && t >= ring_lo &&
+                                    const bool valid = rvalid[mt][hr] && ((mask16 >> n) & 1u) &&
+                                                       t < seq_len && t <= pos && t >= ring_lo &&
                                                        (window <= 0 || pos - t < window);
                                     const float v =
                                         valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
@@ -789,12 +799,13 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     l_run[mt][hr] = l;
                 }
             __syncwarp();  // the warp's reads of the last tile are done
+            const bool wl = info_whole[st_last] != 0;
     #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
     #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int row = mt * 16 + gq + hr * 8;
-                    float *dst = park(warp, row);
+                    float *dst = park(wl, warp, row);
     #pragma unroll
                     for (int n = 0; n < HD / 8; ++n)
                         *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
@@ -806,46 +817,71 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-        for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
-            const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
-            const int i = row0 + row;
-            if (i >= row1) continue;
+        // per row: each warp's weight exp2(m_w - M) / sum and the row's log-sum-exp
+        if (ctid < RB) {
+            const int row = ctid;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * RB + row]);
-            float Lsum = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
+            float f[kWarps], Lsum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float mw = mm[w * RB + row];
-                    if (mw == -INFINITY) continue;
-                    const float f = fast_exp2(mw - M);
-                    Lsum += ml[w * RB + row] * f;
-                    const float4 v =
-                        *reinterpret_cast<const float4 *>(park(w, row) + d);
-                    acc.x += f * v.x;
-                    acc.y += f * v.y;
-                    acc.z += f * v.z;
-                    acc.w += f * v.w;
-                }
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = mm[w * RB + row];
+                f[w] = (M == -INFINITY || mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+                Lsum += ml[w * RB + row] * f[w];
             }
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            if (sg.whole) {
-                const int r = i / p.group, g = i - (i / p.group) * p.group;
-                __nv_bfloat16 *dst =
-                    p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD +
-                    d;
-                uint2 packed;
-                packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                *reinterpret_cast<uint2 *>(dst) = packed;
-            } else {
-                // partial slot (unit, this CTA): unit + blockIdx.x is unique
-                const int64_t slot = ((int64_t)sg.unit + blockIdx.x) * RB + row;
-                *reinterpret_cast<float4 *>(p.ws_o + slot * HD + d) =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                if (d == 0) p.ws_lse[slot] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) wgt[row * kWarps + w] = f[w] * inv;
+            rlse[row] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+        {
+            // every output piece of the unit: all parked loads in flight at once
+            constexpr int kItems = RB * (HD / 4) / (kWarps * 32);
+            static_assert(kItems * kWarps * 32 == RB * (HD / 4), "whole items per thread");
+            const bool wl = info_whole[st_last] != 0;
+            float4 acc[kItems];
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int idx = ctid + k * (kWarps * 32);
+                const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+                const float4 wt = *reinterpret_cast<const float4 *>(wgt + row * kWarps);
+                float4 v[kWarps];
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w)
+                    v[w] = *reinterpret_cast<const float4 *>(park(wl, w, row) + d);
+                const float ww[4] = {wt.x, wt.y, wt.z, wt.w};
+                acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    acc[k].x += ww[w] * v[w].x;
+                    acc[k].y += ww[w] * v[w].y;
+                    acc[k].z += ww[w] * v[w].z;
+                    acc[k].w += ww[w] * v[w].w;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int idx = ctid + k * (kWarps * 32);
+                const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+                const int i = row0 + row;
+                if (i >= row1) continue;
+                if (sg.whole) {
+                    const int r = i / p.group, g = i - (i / p.group) * p.group;
+                    __nv_bfloat16 *dst =
+                        p.out + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD +
+                        d;
+                    uint2 packed;
+                    packed.x = pack_bf16x2(acc[k].x, acc[k].y);
+                    packed.y = pack_bf16x2(acc[k].z, acc[k].w);
+                    *reinterpret_cast<uint2 *>(dst) = packed;
+                } else {
+                    // partial slot (unit, this CTA): unit + blockIdx.x is unique
+                    const int64_t slot = ((int64_t)sg.unit + blockIdx.x) * RB + row;
+                    *reinterpret_cast<float4 *>(p.ws_o + slot * HD + d) = acc[k];
+                    if (d == 0) p.ws_lse[slot] = rlse[row];
+                }
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // parked rows read
