@@ -53,7 +53,7 @@ constexpr int kChunk = 16;                   // key positions per chunk
 constexpr int kWarps = 4;                    // consumer warps = chunks per tile
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
-constexpr int kMaxTableEntries = 512;        // (request, row block) pairs per launch
+constexpr int kMaxTableEntries = 256;        // (request, row block) pairs per launch
 constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per CTA
 constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
 constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
@@ -105,17 +105,25 @@ struct Geo {
     // + per row and warp: max, sum, combined weight; per row: log-sum-exp
     static constexpr int kMergeBytes = (kParkInStage ? 0 : kWarps * RB * HD * 4) + (3 * kWarps + 1) * RB * 4;
     static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
+    // q rows and row positions of a segment, staged by the producer, two
+    // segments deep; rows padded by 16 bytes so the 8 rows of a fragment load
+    // fall in different banks
+    static constexpr int kQStride = HD * 2 + 16;
+    static constexpr int kQBytes = 2 * RB * kQStride + 2 * RB * 4;
     // as many stages as the shared memory of kCtasPerSm CTAs allows (max 8)
     static constexpr int kBudget = (kCtasPerSm == 2 ? 115712 : 232448) - 1024 - kMergeBytes -
-                                   kTableBytes - 1024;
+                                   kTableBytes - kQBytes - 1024;
     static constexpr int kStages = kBudget / kStageBytes > 8 ? 8 : kBudget / kStageBytes;
     static constexpr int kOffMerge = kStages * kStageBytes;
     static constexpr int kOffBars = kOffMerge + kMergeBytes;
-    static constexpr int kOffInfo = kOffBars + 2 * kStages * 8;
+    // full[kStages], empty[kStages], q_full[2], q_empty[2]
+    static constexpr int kOffInfo = kOffBars + (2 * kStages + 4) * 8;
     // info: t0[kStages][kWarps], mask[kStages][kWarps], whole[kStages], last[4]
     static constexpr int kOffTable = kOffInfo + ((2 * kStages * kWarps + kStages + 4) * 4 + 15) / 16 * 16;
     // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
-    static constexpr size_t kSmem = 1024 + kOffTable + kTableBytes;
+    static constexpr int kOffQ = (kOffTable + kTableBytes + 15) / 16 * 16;
+    static constexpr size_t kSmem = 1024 + kOffQ + kQBytes;
+    static_assert(kStages >= 3 || MT == 2, "three stages for up to 16 rows");
     static_assert(kStages >= 2, "at least a double-buffered ring");
 };
 
@@ -247,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     float *rlse = wgt + kWarps * RB;                             // [RB]
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::kOffBars);
     uint64_t *empty = full + kStages;
+    uint64_t *q_full = empty + kStages;  // [2]: a segment's q rows and positions landed
+    uint64_t *q_empty = q_full + 2;      // [2]: the consumers have read them
+    uint8_t *qbuf = smem + G::kOffQ;     // [2][RB][kQStride]
+    int *posbuf = reinterpret_cast<int *>(qbuf + 2 * RB * G::kQStride);  // [2][RB]
     int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
     uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
     int *info_whole = reinterpret_cast<int *>(info_mask + kStages * kWarps);  // [kStages]
@@ -262,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 32);       // one arrival per producer lane (+ TMA bytes)
             mbar_init(&empty[s], kWarps);  // one arrival per consumer warp
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 32);
+            mbar_init(&q_empty[s], kWarps);
         }
         fence_barrier_init();
     }
@@ -341,8 +357,32 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         SegmentWalker walk{g0, g1};
         Segment sg;
         int tile = 0;  // tiles issued by this CTA (stage / phase counter)
+        int seg = 0;   // segments started (q staging buffer / phase counter)
         bool ok = true;
         while (ok && walk.next(p, tb, sg)) {
+            {
+                // stage the segment's q rows and row positions for the consumers
+                const int qi = seg & 1;
+                if (seg >= 2 && !mbar_wait(&q_empty[qi], ((seg >> 1) - 1) & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const int qrow0 = sg.rb * RB, nrows = min(p.rows, qrow0 + RB) - qrow0;
+                constexpr int kPieces = HD / 8;  // 16-byte pieces of a q row
+                uint8_t *qdst = qbuf + qi * RB * G::kQStride;
+                for (int pc = lane; pc < nrows * kPieces; pc += 32) {
+                    const int rr = pc / kPieces, c16 = pc - rr * kPieces;
+                    const int i = qrow0 + rr, r = i / p.group, g = i - r * p.group;
+                    cp_async_16(qdst + rr * G::kQStride + c16 * 16,
+                                p.q + (((int64_t)sg.b * p.q_rows + r) * p.n_q_heads +
+                                       sg.kvh * p.group + g) * HD + c16 * 8);
+                }
+                for (int rr = lane; rr < nrows; rr += 32)
+                    cp_async_4(posbuf + qi * RB + rr,
+                               p.positions + (int64_t)sg.b * p.q_rows + (qrow0 + rr) / p.group);
+                cp_async_arrive_noinc(&q_full[qi]);
+                ++seg;
+            }
             const int bg = p.b_base + sg.b;  // request index in the whole cache
             const int32_t *bt = paged ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
             // raw table entry at page index pi (range-checked when used)
@@ -481,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     SegmentWalker walk{g0, g1};
     Segment sg;
     int tile = 0;
+    int seg = 0;
     bool ok = true;
     // Partial segments merged by this CTA's end-of-share pass (a share cuts
     // at most its first and its last unit), so that no fence or atomic
@@ -516,19 +557,21 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         if constexpr (MT == 0) {
             // ---- up to 8 rows: S^T = K Q^T (keys x rows), O^T = V^T P^T (d x rows)
             // Q^T as the B operand: thread holds row gq, d pairs 2tq (+8) of each k-step
-            // Loads are unconditional (a padding row reads the unit's first
-            // row, whose scores are then masked and never stored), so nothing
-            // waits on them before the first tile's MMAs.
+            // q rows and positions staged by the producer (a padding row uses
+            // the unit's first row; its scores are masked and never stored)
+            const int qi = seg & 1;
+            ok = mbar_wait(&q_full[qi], (seg >> 1) & 1, p.err);
+            __syncwarp();
+            if (!ok) break;
+            const uint8_t *qs = qbuf + qi * RB * G::kQStride;
             uint32_t qb[HD / 16][2];
             {
-                const int i = row0 + gq < row1 ? row0 + gq : row0;
-                const int r = i / p.group, g = i - r * p.group;
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
+                    qs + (row0 + gq < row1 ? gq : 0) * G::kQStride);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    qb[kk][0] = __ldg(qrow + kk * 8 + tq);
-                    qb[kk][1] = __ldg(qrow + kk * 8 + 4 + tq);
+                    qb[kk][0] = qrow[kk * 8 + tq];
+                    qb[kk][1] = qrow[kk * 8 + 4 + tq];
                 }
             }
             // this thread's S^T columns are rows 2tq and 2tq+1
@@ -536,10 +579,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             bool cvalid[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int i = row0 + 2 * tq + e;
-                cvalid[e] = i < row1;
-                cpos[e] = __ldg(p.positions + (int64_t)b * p.q_rows + (cvalid[e] ? i : row0) / p.group);
+                cvalid[e] = row0 + 2 * tq + e < row1;
+                cpos[e] = posbuf[qi * RB + (cvalid[e] ? 2 * tq + e : 0)];
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qi]);
+            ++seg;
             float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
             float o[HD / 16][4];  // m-tile md: (d = 16md + gq (+8), rows 2tq, 2tq+1)
 #pragma unroll
@@ -653,7 +698,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 }
             }
         } else {
-            // unconditional loads, as in the MT = 0 path
+            // q rows and positions staged by the producer, as in the MT = 0 path
+            const int qi = seg & 1;
+            ok = mbar_wait(&q_full[qi], (seg >> 1) & 1, p.err);
+            __syncwarp();
+            if (!ok) break;
+            const uint8_t *qs = qbuf + qi * RB * G::kQStride;
             uint32_t qa[MT][HD / 16][4];
             int rpos[MT][2];
             bool rvalid[MT][2];
@@ -661,20 +711,21 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             for (int mt = 0; mt < MT; ++mt) {
     #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int i0 = row0 + mt * 16 + gq + hr * 8;
-                    rvalid[mt][hr] = i0 < row1;
-                    const int i = rvalid[mt][hr] ? i0 : row0;
-                    const int r = i / p.group, g = i - r * p.group;
-                    rpos[mt][hr] = __ldg(p.positions + (int64_t)b * p.q_rows + r);
-                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                        p.q + (((int64_t)b * p.q_rows + r) * p.n_q_heads + kvh * p.group + g) * HD);
+                    const int rr = mt * 16 + gq + hr * 8;
+                    rvalid[mt][hr] = row0 + rr < row1;
+                    const int rc = rvalid[mt][hr] ? rr : 0;
+                    rpos[mt][hr] = posbuf[qi * RB + rc];
+                    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + rc * G::kQStride);
     #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        qa[mt][kk][hr] = __ldg(qrow + kk * 8 + tq);
-                        qa[mt][kk][2 + hr] = __ldg(qrow + kk * 8 + 4 + tq);
+                        qa[mt][kk][hr] = qrow[kk * 8 + tq];
+                        qa[mt][kk][2 + hr] = qrow[kk * 8 + 4 + tq];
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qi]);
+            ++seg;
             float m_run[MT][2], l_run[MT][2];
             float o[MT][HD / 8][4];
     #pragma unroll

@@ -161,6 +161,11 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
                  : "memory");
 }
 
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed; the
 // arrival counts as one of the barrier's expected arrivals.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {

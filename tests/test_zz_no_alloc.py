@@ -70,18 +70,19 @@ def test_noalloc_matches_attn_decode_twice():
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
     dev = "cuda"
-    # 1024 requests x 8 KV heads over 32k keys needs more partial state than
-    # the fixed array holds: refused before any launch.
-    k = torch.zeros(16, 8, 128, dtype=torch.bfloat16, device=dev)
+    # 1024 requests x 16 KV heads x 32 query rows per head (8 rows x group 4)
+    # over 32k keys needs more partial state than the fixed array holds:
+    # refused before any launch.
+    k = torch.zeros(16, 16, 128, dtype=torch.bfloat16, device=dev)
     cache = gq.KVCache(synth.LINEAR, k, k, slots_per_seq=16)
     big = gq.KVCache(synth.PAGED, k, k,
                      block_table=torch.zeros(1024, 2048, dtype=torch.int32, device=dev),
                      block_size=16)
-    need = gq.attn_decode_workspace_size(big, 1024, 4, 32, 32768, 0)
+    need = gq.attn_decode_workspace_size(big, 1024, 8, 64, 32768, 0)
     assert need > (32 << 20)
-    q = torch.zeros(1024, 4, 32, 128, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(1024, 8, 64, 128, dtype=torch.bfloat16, device=dev)
     seq = torch.full((1024,), 16, dtype=torch.int32, device=dev)
-    pos = torch.zeros(4096, dtype=torch.int32, device=dev)
+    pos = torch.zeros(8192, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     rc = _noalloc_via_cabi(q, big, seq, pos, 32768, 0, 0.1, out, err)
