@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
         const int c = lane & (kWarps - 1);
+        const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
         SegmentWalker walk{g0, g1};
         Segment sg;
         int tile = 0;  // tiles issued by this CTA (stage / phase counter)
@@ -476,9 +477,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     uint8_t *dst = tensor ? vst : kst;
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD / 8; ++c16)
-                        cp_async_16(dst + chunk_base<HD>(false, gc) +
+                        cp_async_16_hint(dst + chunk_base<HD>(false, gc) +
                                         piece_offset(half_stride(false), r, c16),
-                                    src + c16 * 8);
+                                    src + c16 * 8, kv_policy);
                     issued_cp = true;
                 }
                 if (lane == 0) info_whole[st] = whole_tile ? 1 : 0;
@@ -494,13 +495,15 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 // [half index = kv head * halves + half][slot][64 columns]
                 if (whole_tile) {
                     if (lane < 2)
-                        tma_load_3d(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, (int)slot00,
-                                    sg.kvh * G::kHalves, &full[st]);
+                        tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
+                                         (int)slot00, sg.kvh * G::kHalves, &full[st], kv_policy);
                 } else if (lane < kWarps && slot0 >= -1) {
                     const int y = slot0 < 0 ? -kChunk : (int)slot0;
                     const uint32_t off = chunk_base<HD>(false, lane);
-                    tma_load_3d(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st]);
-                    tma_load_3d(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st]);
+                    tma_load_3d_hint(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st],
+                                     kv_policy);
+                    tma_load_3d_hint(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st],
+                                     kv_policy);
                 }
                 __syncwarp();
                 if (issued_cp)
