@@ -55,6 +55,11 @@ constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kProducerWarp = kWarps;
 constexpr int kMaxTableEntries = 256;        // (request, row block) pairs per launch
 constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per CTA
+// A CTA that moves from one unit to the next pays for a second segment
+// (merge of its warps, partial store, new q): in the share arithmetic every
+// unit is followed by this many chunks of nothing, so such a CTA gets that
+// much less real work.
+constexpr int kUnitGapChunks = 6;
 constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
 constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
 
@@ -190,48 +195,58 @@ struct Segment {
     int b, kvh, rb;
     int c_begin, c_end;  // chunk range inside the unit's key range
     int unit;
-    int unit_start, n_u; // the unit's chunks in the global order: [unit_start, +n_u)
+    int first, last;     // the CTAs that hold the unit's pieces
     bool whole;          // the piece is the whole unit
     bool head;           // the piece starts the unit
 };
 
-// The segments of global chunk range [g, g_end), in order.
+// The segments of global range [g, g_end), in order.  The range is in the
+// order of all units' chunks laid end to end, each unit followed by
+// kUnitGapChunks chunks that hold nothing (skipped).
 struct SegmentWalker {
     int g, g_end;
+    int L;  // chunks (with gaps) per CTA
     __device__ bool next(const Params &p, const Tables &t, Segment &s) {
-        if (g >= g_end) return false;
         const int B = p.batch, RBc = p.row_blocks;
-        // request: the largest b with Pb[b] <= g (requests with no chunks are skipped)
-        int lo = 0, hi = B;  // invariant: Pb[lo] <= g < Pb[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (t.Pb[mid] <= g)
-                lo = mid;
-            else
-                hi = mid;
+        while (g < g_end) {
+            // request: the largest b with Pb[b] <= g (requests with no chunks are skipped)
+            int lo = 0, hi = B;  // invariant: Pb[lo] <= g < Pb[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (t.Pb[mid] <= g)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const int b = lo;
+            const int per_head = (t.Pb[b + 1] - t.Pb[b]) / p.n_kv_heads;
+            int off = g - t.Pb[b];
+            const int kvh = off / per_head;
+            off -= kvh * per_head;
+            int rb = 0;
+            auto span = [&](int e) { return t.cnt[e] > 0 ? t.cnt[e] + kUnitGapChunks : 0; };
+            while (off >= span(b * RBc + rb)) off -= span(b * RBc + rb++);
+            const int n_u = t.cnt[b * RBc + rb];
+            const int unit_start = g - off;
+            if (off >= n_u) {  // in the unit's gap
+                g = min(g_end, unit_start + n_u + kUnitGapChunks);
+                continue;
+            }
+            const int seg_end = min(g_end, unit_start + n_u);
+            s.b = b;
+            s.kvh = kvh;
+            s.rb = rb;
+            s.c_begin = t.clo[b * RBc + rb] + off;
+            s.c_end = s.c_begin + (seg_end - g);
+            s.unit = (b * p.n_kv_heads + kvh) * RBc + rb;
+            s.first = unit_start / L;
+            s.last = (unit_start + n_u - 1) / L;
+            s.whole = (off == 0 && seg_end == unit_start + n_u);
+            s.head = off == 0;
+            g = seg_end;
+            return true;
         }
-        const int b = lo;
-        const int per_head = (t.Pb[b + 1] - t.Pb[b]) / p.n_kv_heads;
-        int off = g - t.Pb[b];
-        const int kvh = off / per_head;
-        off -= kvh * per_head;
-        int rb = 0;
-        while (off >= t.cnt[b * RBc + rb]) off -= t.cnt[b * RBc + rb++];
-        const int n_u = t.cnt[b * RBc + rb];
-        const int unit_start = g - off;
-        const int seg_end = min(g_end, unit_start + n_u);
-        s.b = b;
-        s.kvh = kvh;
-        s.rb = rb;
-        s.c_begin = t.clo[b * RBc + rb] + off;
-        s.c_end = s.c_begin + (seg_end - g);
-        s.unit = (b * p.n_kv_heads + kvh) * RBc + rb;
-        s.unit_start = unit_start;
-        s.n_u = n_u;
-        s.whole = (off == 0 && seg_end == unit_start + n_u);
-        s.head = off == 0;
-        g = seg_end;
-        return true;
+        return false;
     }
 };
 
@@ -309,7 +324,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             const int b = base + lane;
             int v = 0;
             if (b < B)
-                for (int rb = 0; rb < RBc; ++rb) v += tb.cnt[b * RBc + rb];
+                for (int rb = 0; rb < RBc; ++rb) {
+                    const int n = tb.cnt[b * RBc + rb];
+                    v += n > 0 ? n + kUnitGapChunks : 0;
+                }
             v *= p.n_kv_heads;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -355,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
         const int c = lane & (kWarps - 1);
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
-        SegmentWalker walk{g0, g1};
+        SegmentWalker walk{g0, g1, L};
         Segment sg;
         int tile = 0;  // tiles issued by this CTA (stage / phase counter)
         int seg = 0;   // segments started (q staging buffer / phase counter)
@@ -521,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     // ---------------------------------------------------------------- consumers
     const int gq = lane >> 2, tq = lane & 3;
     const int ctid = threadIdx.x;  // 0 .. 127
-    SegmentWalker walk{g0, g1};
+    SegmentWalker walk{g0, g1, L};
     Segment sg;
     int tile = 0;
     int seg = 0;
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     while (ok && walk.next(p, tb, sg)) {
         const int b = sg.b, kvh = sg.kvh;
         if (sg.head && ctid == 0)  // for the merge kernel: the CTAs holding the unit
-            p.ws_parts[sg.unit] = make_int2(sg.unit_start / L, (sg.unit_start + sg.n_u - 1) / L);
+            p.ws_parts[sg.unit] = make_int2(sg.first, sg.last);
         const int row0 = sg.rb * RB;
         const int row1 = min(p.rows, row0 + RB);
         const int seq_len = tb.seqlen[b];
@@ -940,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // parked rows read
         if (lane == 0) mbar_arrive(&empty[st_last]);
-        if (!sg.whole && (sg.unit_start + sg.n_u - 1) / L - sg.unit_start / L < kFusedMaxParts) {
+        if (!sg.whole && sg.last - sg.first < kFusedMaxParts) {
             if (n_pend == 0)
                 pend0 = sg;
             else
@@ -957,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     if (ctid == 0) {
         for (int k = 0; k < n_pend; ++k) {
             const Segment &u = k == 0 ? pend0 : pend1;
-            const int first = u.unit_start / L, last = (u.unit_start + u.n_u - 1) / L;
+            const int first = u.first, last = u.last;
             const int prev = atomicAdd(p.ws_count + u.unit, 1);
             s_last[k] = (prev == last - first) ? 1 : 0;
         }
@@ -968,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         if (!s_last[k]) continue;  // uniform across the consumer warps
         __threadfence();
         const Segment &u = k == 0 ? pend0 : pend1;
-        const int first = u.unit_start / L, last = (u.unit_start + u.n_u - 1) / L;
+        const int first = u.first, last = u.last;
         const int parts = last - first + 1;  // <= kFusedMaxParts
         const int row0 = u.rb * RB, row1 = min(p.rows, row0 + RB);
         // 1) every part's log-sum-exp of every row into shared memory, 2) per
