@@ -59,7 +59,7 @@ constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per
 // (merge of its warps, partial store, new q): in the share arithmetic every
 // unit is followed by this many chunks of nothing, so such a CTA gets that
 // much less real work.
-constexpr int kUnitGapChunks = 6;
+constexpr int kUnitGapChunks = 12;
 constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
 constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
 
