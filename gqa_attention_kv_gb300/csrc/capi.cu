@@ -176,6 +176,37 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_decode_append(const void *q, const void *k_new, const void *v_new,
+                       const int64_t *slot_mapping, const attn_kv_cache *cache,
+                       const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
+                       int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
+                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                       int32_t *err_word, attn_stream_t stream) {
+    int rc = check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim,
+                                max_seq_len, window);
+    if (rc != ATTN_OK) return rc;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
+    if (batch == 0) return ATTN_OK;
+    if (!q || !k_new || !v_new || !slot_mapping || !seq_lens || !positions || !out ||
+        !cache->k || !cache->v)
+        return ATTN_ERR_NULL;
+    if (cache->kind == ATTN_CACHE_PAGED && !cache->block_table) return ATTN_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(cache->k) || !aligned16(cache->v) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return ATTN_ERR_ALIGN;
+    gqa::DecodePlan plan;
+    gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
+                     &plan);
+    if (plan.workspace > 0) {
+        if (!workspace) return ATTN_ERR_NULL;
+        if (workspace_bytes < plan.workspace) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    }
+    return gqa::launch_decode(plan, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
+                              window, n_q_heads, n_kv_heads, scale, out, workspace, err_word,
+                              reinterpret_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping);
+}
+
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,
                  int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,
                  int32_t *err_word, attn_stream_t stream) {

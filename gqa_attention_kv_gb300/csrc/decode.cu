@@ -87,6 +87,11 @@ struct Params {
     float *ws_o;
     float *ws_lse;
     int32_t *ws_count;  // per unit: partial states written so far (zero between calls)
+    // fused append (nullptr: none): the step's rows, bf16 [batch * q_rows][n_kv_heads][HD],
+    // row b * q_rows + r being the key at position seq_len_b - q_rows + r, and their slots
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    const int64_t *slot_mapping;
     int2 *ws_parts;     // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     int32_t *err;
 };
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
         const int c = lane & (kWarps - 1);
+        const bool fused = p.k_new != nullptr;
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
         SegmentWalker walk{g0, g1, L};
         Segment sg;
@@ -420,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 return (s >= 0 && s < p.num_slots) ? s : -1;
             };
             const int seq_len = tb.seqlen[sg.b];
+            const int new_lo = seq_len - p.q_rows;  // first of the step's new keys
             const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
             // page ids of two consecutive 32-page windows, one per lane; the
             // second is fetched a window ahead of its use
@@ -457,7 +464,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         slot0 = (v < 0 || v >= num_pages)
                                     ? -1
                                     : (int64_t)v * p.block_size + t0 % p.block_size;
-                } else if (chunk < sg.c_end) {
+                }
+                // a chunk holding any of the step's new keys (fused append) is
+                // gathered, the new rows taken from k_new / v_new
+                const bool has_new = fused && chunk < sg.c_end && t0 + kChunk > new_lo &&
+                                     t0 < seq_len;
+                if (has_new) {
+                    slot0 = -2;
+                } else if (!paged_tma && chunk < sg.c_end) {
                     if (p.kind == ATTN_CACHE_LINEAR) {
                         slot0 = (int64_t)bg * p.slots_per_seq + t0;
                     } else if (paged) {
@@ -485,13 +499,21 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const int gc = __ffs(bits) - 1;
                     const int gt0 = (chunk0 + gc) * kChunk;
                     const int r = lane & (kChunk - 1), tensor = lane >> 4;
-                    const int64_t s = slot_of(gt0 + r);
-                    const unsigned valid = __ballot_sync(0xffffffffu, s >= 0) & 0xFFFFu;
-                    if (lane < kChunk && s < 0 && gt0 + r < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
+                    const int t = gt0 + r;
+                    const bool is_new = fused && t >= new_lo && t < seq_len;
+                    const int64_t s = is_new ? 0 : slot_of(t);
+                    const unsigned valid = __ballot_sync(0xffffffffu, is_new || s >= 0) & 0xFFFFu;
+                    if (lane < kChunk && !is_new && s < 0 && t < seq_len)
+                        report_error(p.err, ATTN_ERR_BOUNDS);
                     if (lane == gc) gmask = valid;
-                    // a masked row reads slot 0 (any valid slot will do)
-                    const __nv_bfloat16 *src = (tensor ? p.v_cache : p.k_cache) +
-                                               (s < 0 ? 0 : s) * row_elems + (int64_t)sg.kvh * HD;
+                    // a new key comes from the step's rows; a masked row reads
+                    // slot 0 (any valid slot will do)
+                    const __nv_bfloat16 *src =
+                        is_new ? (tensor ? p.v_new : p.k_new) +
+                                     ((int64_t)(sg.b * p.q_rows + (t - new_lo)) * p.n_kv_heads +
+                                      sg.kvh) * HD
+                               : (tensor ? p.v_cache : p.k_cache) + (s < 0 ? 0 : s) * row_elems +
+                                     (int64_t)sg.kvh * HD;
                     uint8_t *dst = tensor ? vst : kst;
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD / 8; ++c16)
@@ -539,6 +561,29 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     // ---------------------------------------------------------------- consumers
     const int gq = lane >> 2, tq = lane & 3;
     const int ctid = threadIdx.x;  // 0 .. 127
+    if (p.k_new != nullptr) {
+        // fused append: the step's rows into their cache slots, for later
+        // steps (this launch reads them from k_new / v_new); 16-byte pieces
+        const int pieces = p.n_kv_heads * HD / 8;  // of one row of one tensor
+        const int64_t total = (int64_t)p.batch * p.q_rows * pieces * 2;
+        for (int64_t idx = (int64_t)blockIdx.x * (kWarps * 32) + ctid; idx < total;
+             idx += (int64_t)p.grid * (kWarps * 32)) {
+            const int64_t row = idx / (2 * pieces);
+            const int rem = (int)(idx - row * 2 * pieces);
+            const int tensor = rem / pieces, pc = rem - tensor * pieces;
+            const int64_t slot = p.slot_mapping[row];
+            if (slot < 0 || slot >= p.num_slots) {
+                if (rem == 0) report_error(p.err, ATTN_ERR_BOUNDS);
+                continue;
+            }
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(tensor ? p.v_new : p.k_new) + row * pieces + pc;
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                             const_cast<__nv_bfloat16 *>(tensor ? p.v_cache : p.k_cache)) +
+                         slot * pieces + pc;
+            *dst = __ldg(src);
+        }
+    }
     SegmentWalker walk{g0, g1, L};
     Segment sg;
     int tile = 0;
@@ -1227,7 +1272,8 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
 int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *cache,
                   const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
-                  void *out, void *workspace, int32_t *err, cudaStream_t stream) {
+                  void *out, void *workspace, int32_t *err, cudaStream_t stream,
+                  const void *k_new, const void *v_new, const int64_t *slot_mapping) {
     // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][64]
     // (a half is 64 columns, 128 bytes, of one head's row): a box of
     // {64, rows, halves} brings both halves of `rows` slots of one head.
@@ -1264,6 +1310,10 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.max_blocks = cache->max_blocks_per_seq;
         p.seq_lens = seq_lens + b0;
         p.positions = positions + (int64_t)b0 * q_rows;
+        const int64_t new_off = (int64_t)b0 * q_rows * n_kv_heads * plan.head_dim;
+        p.k_new = k_new ? static_cast<const __nv_bfloat16 *>(k_new) + new_off : nullptr;
+        p.v_new = v_new ? static_cast<const __nv_bfloat16 *>(v_new) + new_off : nullptr;
+        p.slot_mapping = slot_mapping ? slot_mapping + (int64_t)b0 * q_rows : nullptr;
         p.batch = nb;
         p.b_base = b0;
         p.q_rows = q_rows;

@@ -63,10 +63,14 @@ struct DecodePlan {
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
                 int head_dim, int max_seq_len, int window, DecodePlan *plan);
 
+// k_new / v_new / slot_mapping non-null: the step's rows are appended by the
+// same launch (attn_decode_append).
 int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *cache,
                   const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
-                  void *out, void *workspace, int32_t *err, cudaStream_t stream);
+                  void *out, void *workspace, int32_t *err, cudaStream_t stream,
+                  const void *k_new = nullptr, const void *v_new = nullptr,
+                  const int64_t *slot_mapping = nullptr);
 
 int launch_prefill(const void *q, const void *k, const void *v, int batch, int seq_len,
                    int window, int n_q_heads, int n_kv_heads, int head_dim, float scale,

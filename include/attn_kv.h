@@ -180,6 +180,35 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
                 attn_stream_t stream);
 
 /*
+ * attn_decode_append -- the step's KV append and its decode in one launch.
+ *
+ * Source: vibevoice.c, "The decode step is one submission" (the new K/V row
+ * lands at a device-side slot inside the captured step, before attention);
+ * talker_multiframe, NarrowStep fields (a step writes its K rows, then
+ * attends).  Same result as
+ *     attn_kv_append(k_new, v_new, slot_mapping, batch * q_rows, cache, ...);
+ *     attn_decode(q, cache, seq_lens, positions, ...);
+ * when the step's rows follow the position contract: new row b*q_rows + r is
+ * the key at position seq_lens[b] - q_rows + r, and slot_mapping of that row
+ * is its slot in the cache.  The decode takes those keys from k_new / v_new
+ * directly, so it never waits for the cache writes; the cache rows are
+ * written by the same launch for later steps.
+ *
+ *   k_new, v_new   bf16 [batch * q_rows, n_kv_heads, head_dim], device,
+ *                  16-byte aligned
+ *   slot_mapping   int64 [batch * q_rows], device.  A slot outside
+ *                  [0, num_slots) is skipped and reported as ATTN_ERR_BOUNDS
+ *                  in *err_word.
+ *   Every other argument, the workspace and the statuses are attn_decode's.
+ */
+int attn_decode_append(const void *q, const void *k_new, const void *v_new,
+                       const int64_t *slot_mapping, const attn_kv_cache *cache,
+                       const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
+                       int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
+                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                       int32_t *err_word, attn_stream_t stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart to it.
  *

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("attn_kv_append", "attn_decode", "attn_decode_workspace_size", "attn_prefill",
-                 "attn_status_string", "attn_version"):
+                 "attn_decode_append", "attn_status_string", "attn_version"):
         assert want in names, names
 
 
@@ -145,3 +145,20 @@ def test_product_path_does_not_reach_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_oracle" not in text, f
+
+
+def test_decode_append_validation(lib):
+    """Host checks of attn_decode_append, made before any launch."""
+    c = cache(slots=4096 * 4, sps=4096)
+    cs = c.struct()
+    f = lib.attn_decode_append
+    need = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 4096, 0)
+    args = lambda q=16, kn=32, vn=48, sm=64, ws=1 << 20, ws_bytes=need, scale=0.1, hq=32: (
+        q, kn, vn, sm, ctypes.byref(cs), 80, 96, 2, 1, 4096, 0, hq, 8, 128, scale, 112, ws,
+        ws_bytes, None, None)
+    assert f(*args(kn=None)) == gq.ATTN_ERR_NULL
+    assert f(*args(sm=None)) == gq.ATTN_ERR_NULL
+    assert f(*args(vn=40)) == gq.ATTN_ERR_ALIGN
+    assert f(*args(ws_bytes=need - 1)) == gq.ATTN_ERR_WORKSPACE
+    assert f(*args(hq=30)) == gq.ATTN_ERR_SHAPE
+    assert f(*args(scale=0.0)) == gq.ATTN_ERR_SHAPE

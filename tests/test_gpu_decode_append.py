@@ -1,0 +1,76 @@
+"""attn_decode_append: the step's append fused into the decode launch.
+
+It must give what attn_kv_append followed by attn_decode gives (vibevoice.c,
+"The decode step is one submission": the new row lands at its device-side
+slot, then attention reads it): the same output bits, the same cache bits
+after the call, and the oracle's answer within the tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_kv_gb300 as gq
+import oracle
+from gqa_attention_kv_gb300 import synth
+from helpers import compare, oracle_decode, to_device
+
+pytestmark = pytest.mark.gpu
+
+LINEAR, PAGED, RING = synth.LINEAR, synth.PAGED, synth.RING
+
+CASES = [
+    # kind, B, R, Hq, Hkv, D, seq_lens, extra
+    (LINEAR, 3, 1, 32, 8, 128, [513, 1, 4097], {}),
+    (LINEAR, 2, 4, 28, 4, 128, [2000, 37], {}),
+    (PAGED, 4, 4, 32, 8, 128, [64, 100, 1030, 17], {"block_size": 16}),
+    (PAGED, 3, 2, 16, 4, 64, [37, 300, 129], {"block_size": 5, "num_blocks": 200}),
+    (RING, 4, 1, 32, 8, 128, [9000, 300, 16390, 8193], {"window": 8192, "ring": 16384}),
+    (RING, 3, 4, 16, 4, 128, [1500 + 3, 4, 1501], {"window": 750, "ring": 1500}),
+]
+
+
+def _run(case, fused):
+    dev = "cuda"
+    cache = to_device(case, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+    sm, seq, pos = case.slot_mapping.to(dev), case.seq_lens.to(dev), case.positions.to(dev)
+    if fused:
+        out = gq.attn_decode_append(q, kn, vn, sm, cache, seq, pos, case.max_seq_len(),
+                                    case.window, case.scale, err=err)
+    else:
+        gq.attn_kv_append(kn, vn, sm, cache, err=err)
+        out = gq.attn_decode(q, cache, seq, pos, case.max_seq_len(), case.window, case.scale,
+                             err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out, cache
+
+
+@pytest.mark.parametrize("kind,B,R,Hq,Hkv,D,seq,extra", CASES)
+def test_fused_equals_append_then_decode(kind, B, R, Hq, Hkv, D, seq, extra):
+    case = synth.decode_case(9200 + B * R + D + 10 * int(kind), kind, B, R, Hq, Hkv, D, seq, **extra)
+    out_f, cache_f = _run(case, fused=True)
+    out_u, cache_u = _run(case, fused=False)
+    assert torch.equal(out_f, out_u), "fused decode differs from append + decode"
+    assert torch.equal(cache_f.k, cache_u.k) and torch.equal(cache_f.v, cache_u.v)
+    ref, kc, vc = oracle_decode(case)
+    compare(out_f, ref, f"fused {kind} R={R}")
+    assert np.array_equal(oracle.bf16_bits(cache_f.k), kc)
+    assert np.array_equal(oracle.bf16_bits(cache_f.v), vc)
+
+
+def test_fused_reports_out_of_range_slot():
+    case = synth.decode_case(9300, LINEAR, 2, 1, 8, 2, 128, [40, 40])
+    sm = case.slot_mapping.clone()
+    sm[1] = 10_000_000
+    case.slot_mapping = sm
+    dev = "cuda"
+    cache = to_device(case, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gq.attn_decode_append(case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev),
+                                sm.to(dev), cache, case.seq_lens.to(dev), case.positions.to(dev),
+                                40, 0, case.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gq.ATTN_ERR_BOUNDS
+    assert torch.isfinite(out.float()).all()
