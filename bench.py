@@ -8,7 +8,7 @@ Qwen2-7B-shaped decoder (28 q / 4 kv heads, head_dim 128, bf16):
   2. KV append of those 14,449 prompt rows            (attn_kv_append)
   3. five decode steps of 2 slots x 1 row, at contexts 14,449 / 17,623 /
      20,797 / 23,971 and the mixed pair (14,449, 23,971), each appending its
-     2 new rows first                                  (attn_kv_append + attn_decode)
+     2 new rows in the same launch                     (attn_decode_append)
 
 Printed metric (one JSON line): decode-attention KV GB/s over the step's
 decode launches (``value``), prefill TFLOP/s over its prefill launch
@@ -77,6 +77,19 @@ def prefill_traffic(T):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return PREFILL_TRAFFIC["bytes"] if h.hexdigest() == PREFILL_TRAFFIC["sha256"] else None
+
+
+def merge_kernel_launched(max_seq_len, window, q_rows, ring):
+    """1 if a decode call also launches the merge kernel: the library's rule
+    (a unit may span more than 8 CTAs of at least 8 chunks of 16 keys)."""
+    keys = max_seq_len
+    if window > 0:
+        keys = min(keys, window + q_rows - 1)
+    if ring:
+        keys = min(keys, ring)
+    max_chunks = (keys + 15) // 16 + 1
+    max_parts = (max_chunks + 7) // 8 + 1
+    return 1 if max_parts > 8 else 0
 
 
 def prefill_flops(T, Hq, D, window=0):
@@ -237,8 +250,8 @@ class QwenWorkload(Workload):
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
-        plan_splits = self.ws.numel() > 0
-        self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * (2 + (1 if plan_splits else 0))
+        self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * (
+            1 + merge_kernel_launched(self.max_seq, 0, 1, None))
         self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",
                          "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D,
                          "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
@@ -268,9 +281,9 @@ class QwenWorkload(Workload):
                 for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
                     d[key].copy_(hd[key], non_blocking=True)
             c = self.caches[(s * 6 + 1 + i) % self.ncopy]
-            gq.attn_kv_append(d["k_new"], d["v_new"], d["slots"], c, err=self.err)
-            gq.attn_decode(d["q"], c, d["seq"], d["pos"], self.max_seq, 0, self.scale,
-                           out=d["out"], workspace=self.ws, err=self.err)
+            gq.attn_decode_append(d["q"], d["k_new"], d["v_new"], d["slots"], c, d["seq"],
+                                  d["pos"], self.max_seq, 0, self.scale, out=d["out"],
+                                  workspace=self.ws, err=self.err)
             if e2e:
                 self.h["dec"][i]["out"].copy_(d["out"], non_blocking=True)
 
@@ -377,7 +390,9 @@ class DecodeOnlyWorkload(Workload):
         self.out = torch.empty_like(base.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
-        self.launches_per_step = 2 + (1 if self.ws.numel() > 0 else 0)
+        self.launches_per_step = 1 + merge_kernel_launched(
+            self.max_seq, base.window, base.q_rows,
+            base.slots_per_seq if base.kind == synth.RING else None)
         # valid keys per (request, row) summed over rows' union per request
         seq = base.seq_lens.cpu().tolist()
         keys = 0
@@ -411,9 +426,9 @@ class DecodeOnlyWorkload(Workload):
         c = self.case
         for layer in range(self.layers):
             cache = self.caches[(s * self.layers + layer) % self.ncopy]
-            self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
-            self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq, c.window,
-                                c.scale, out=self.out, workspace=self.ws, err=self.err)
+            self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
+                                       c.seq_lens, c.positions, self.max_seq, c.window,
+                                       c.scale, out=self.out, workspace=self.ws, err=self.err)
 
     def capture(self, stream, e2e=False):
         torch = self.torch
