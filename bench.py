@@ -370,6 +370,7 @@ class DecodeOnlyWorkload(Workload):
 
         self.gq, self.torch = gq, torch
         make = {"voxtral": synth.voxtral_decode_step, "ring": synth.ring_window_decode,
+                "stream-encoder": synth.streaming_encoder_step,
                 "paged": synth.paged_multirow_decode}[which]
         base = make(device=dev)
         self.case = base
@@ -407,11 +408,13 @@ class DecodeOnlyWorkload(Workload):
         self.keys = keys
         # one step = one decode per decoder layer, each layer its own cache
         # (Voxtral decoder: 26 layers); bigger workloads: one layer per step
-        self.layers = 26 if which == "voxtral" else 1
+        self.layers = {"voxtral": 26, "stream-encoder": 32}.get(which, 1)
         self.launches_per_step *= self.layers
         self.name = {"voxtral": "voxtral decode step B=1 R=1 32/8 D=128 linear 512 keys, "
                                 "26 layers",
                      "ring": "ring window decode B=16 32/8 D=128 ring 16384 window 8192",
+                     "stream-encoder": "streaming encoder step, 4 frames over a 1500-slot ring, "
+                                       "window 750, 32/32 D=64, 32 layers",
                      "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16"}[which]
         self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
                          "layers_per_step": self.layers,
@@ -501,7 +504,7 @@ class PrefillOnlyWorkload(Workload):
 def make_workload(name, dev):
     if name == "qwen":
         return QwenWorkload(dev)
-    if name in ("voxtral", "ring", "paged"):
+    if name in ("voxtral", "ring", "paged", "stream-encoder"):
         return DecodeOnlyWorkload(dev, name)
     if name in ("encoder", "encoder-long", "qwen-prefill", "prefill-8k"):
         return PrefillOnlyWorkload(dev, name)
@@ -627,6 +630,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen",
                     choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged",
+                             "stream-encoder",
                              "qwen-prefill", "prefill-8k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -244,6 +244,15 @@ def ring_window_decode(device="cpu", batch=16):
                        ring=16384, device=device)
 
 
+def streaming_encoder_step(device="cpu", batch=1):
+    """Streaming speech encoder, one step of one layer: 4 new frames attend
+    over a 1,500-slot ring with a 750-frame window, 32 = 32 heads, D=64, scale
+    1/8, the stream long past the ring's wrap (Voxtral notes, "Encoder KV
+    cache")."""
+    return decode_case(20266, RING, batch, 4, 32, 32, 64, [6004] * batch, window=750,
+                       ring=1500, scale=0.125, device=device)
+
+
 def paged_multirow_decode(device="cpu", batch=64):
     """Paged K=4 uniform decode: 64 requests x 4 rows, bs 16, 200k-slot pool
     (12,500 pages dealt from a seeded permutation), seq_lens in [64, 4,096]."""

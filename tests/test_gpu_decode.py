@@ -203,3 +203,13 @@ def test_append_bit_exact():
         torch.cuda.synchronize()
         assert np.array_equal(oracle.bf16_bits(cache.k), kc)
         assert np.array_equal(oracle.bf16_bits(cache.v), vc)
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_streaming_encoder_step(batch):
+    """4 new frames over a 1,500-slot ring with a 750-frame window, 32 = 32
+    heads, D=64 (Voxtral notes, "Encoder KV cache"), long past the wrap."""
+    case = synth.streaming_encoder_step(batch=batch)
+    ref, _, _ = oracle_decode(case)
+    out, _ = gpu_decode(case)
+    compare(out, ref, f"streaming encoder B={batch}")
