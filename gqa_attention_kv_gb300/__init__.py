@@ -65,8 +65,8 @@ def lib():
             L.attn_decode.argtypes = [p, cp, p, p, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, p, p, sz, p, p]
             L.attn_decode.restype = i32
-            L.attn_decode_append.argtypes = [p, p, p, p, cp, p, p, i32, i32, i32, i32, i32, i32,
-                                             i32, ctypes.c_float, p, p, sz, p, p]
+            L.attn_decode_append.argtypes = [p, p, p, p, p, cp, p, p, i32, i32, i32, i32, i32,
+                                             i32, i32, ctypes.c_float, p, p, sz, p, p]
             L.attn_decode_append.restype = i32
             L.attn_prefill.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, ctypes.c_float, p,
                                        p, p]
@@ -180,11 +180,13 @@ def attn_decode(q, cache: KVCache, seq_lens, positions, max_seq_len, window, sca
 
 def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, positions,
                        max_seq_len, window, scale, out=None, workspace=None, err=None,
-                       stream=None):
+                       stream=None, rope_inv_freq=None):
     """The step's KV append and its decode in one launch: same result as
     attn_kv_append(k_new, v_new, slot_mapping, cache) then attn_decode(...)
     when new row b*R + r is the key at position seq_lens[b] - R + r.
-    k_new / v_new bf16 [B*R, Hkv, D]; slot_mapping int64 [B*R]."""
+    k_new / v_new bf16 [B*R, Hkv, D]; slot_mapping int64 [B*R].  With
+    rope_inv_freq (float32 [D/2] on the device), q and k_new are first rotated
+    at their positions (interleaved pairs)."""
     import torch
 
     B, R, Hq, D = q.shape
@@ -195,7 +197,8 @@ def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, 
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     c = cache.struct()
     rc = lib().attn_decode_append(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), ctypes.byref(c), _ptr(seq_lens),
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(rope_inv_freq),
+        ctypes.byref(c), _ptr(seq_lens),
         _ptr(positions), B, R, int(max_seq_len), int(window), Hq, cache.n_kv_heads, D,
         float(scale), _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(err),

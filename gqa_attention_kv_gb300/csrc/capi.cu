@@ -177,7 +177,8 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
 }
 
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,
-                       const int64_t *slot_mapping, const attn_kv_cache *cache,
+                       const int64_t *slot_mapping, const float *rope_inv_freq,
+                       const attn_kv_cache *cache,
                        const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                        int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void *out, void *workspace, size_t workspace_bytes,
@@ -204,7 +205,8 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
     }
     return gqa::launch_decode(plan, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
                               window, n_q_heads, n_kv_heads, scale, out, workspace, err_word,
-                              reinterpret_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping);
+                              reinterpret_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping,
+                              rope_inv_freq);
 }
 
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,

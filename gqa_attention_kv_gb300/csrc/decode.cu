@@ -92,6 +92,7 @@ struct Params {
     const __nv_bfloat16 *k_new;
     const __nv_bfloat16 *v_new;
     const int64_t *slot_mapping;
+    const float *rope_inv_freq;  // [HD / 2] (nullptr: no rotary embedding)
     int2 *ws_parts;     // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     int32_t *err;
 };
@@ -119,7 +120,7 @@ struct Geo {
     // segments deep; rows padded by 16 bytes so the 8 rows of a fragment load
     // fall in different banks
     static constexpr int kQStride = HD * 2 + 16;
-    static constexpr int kQBytes = 2 * RB * kQStride + 2 * RB * 4;
+    static constexpr int kQBytes = 2 * RB * kQStride + 2 * RB * 4 + HD / 2 * 4;  // + rope table
     // as many stages as the shared memory of kCtasPerSm CTAs allows (max 8)
     static constexpr int kBudget = (kCtasPerSm == 2 ? 115712 : 232448) - 1024 - kMergeBytes -
                                    kTableBytes - kQBytes - 1024;
@@ -138,6 +139,15 @@ struct Geo {
 };
 
 constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
+
+// Rotary embedding of one interleaved pair held as bf16x2 (low half = x[2i]):
+// rotated by the float32 angle pos * inv_freq in float32, rounded to bf16.
+__device__ __forceinline__ uint32_t rope_pair(uint32_t w, int pos, float inv_freq) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float sn, cs;
+    sincosf((float)pos * inv_freq, &sn, &cs);
+    return pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+}
 
 // A stage holds the K and V of one 64-key tile, each in one of two
 // 128-byte-swizzled layouts (an 8-row group always spans 1024 aligned bytes):
@@ -255,7 +265,9 @@ struct SegmentWalker {
     }
 };
 
-template <int HD, int MT>
+// ROPE: the fused append's rotary embedding (its code is compiled only into
+// the kernels that need it).
+template <int HD, int MT, bool ROPE>
 __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -279,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     uint64_t *q_empty = q_full + 2;      // [2]: the consumers have read them
     uint8_t *qbuf = smem + G::kOffQ;     // [2][RB][kQStride]
     int *posbuf = reinterpret_cast<int *>(qbuf + 2 * RB * G::kQStride);  // [2][RB]
+    float *rope_if = reinterpret_cast<float *>(posbuf + 2 * RB);        // [HD / 2]
     int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
     uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
     int *info_whole = reinterpret_cast<int *>(info_mask + kStages * kWarps);  // [kStages]
@@ -561,6 +574,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     // ---------------------------------------------------------------- consumers
     const int gq = lane >> 2, tq = lane & 3;
     const int ctid = threadIdx.x;  // 0 .. 127
+    constexpr bool rope = ROPE;
+    if (rope) {
+        for (int i = ctid; i < HD / 2; i += kWarps * 32) rope_if[i] = p.rope_inv_freq[i];
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    }
     if (p.k_new != nullptr) {
         // fused append: the step's rows into their cache slots, for later
         // steps (this launch reads them from k_new / v_new); 16-byte pieces
@@ -581,7 +599,18 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             uint4 *dst = reinterpret_cast<uint4 *>(
                              const_cast<__nv_bfloat16 *>(tensor ? p.v_cache : p.k_cache)) +
                          slot * pieces + pc;
-            *dst = __ldg(src);
+            uint4 w = __ldg(src);
+            if (rope && tensor == 0) {
+                // key row b*q_rows + r sits at position seq_len_b - q_rows + r
+                const int b = (int)(row / p.q_rows), r = (int)(row - (int64_t)b * p.q_rows);
+                const int pos = tb.seqlen[b] - p.q_rows + r;
+                const int i0 = (pc % (HD / 8)) * 4;  // first pair of the piece in its head
+                w.x = rope_pair(w.x, pos, rope_if[i0]);
+                w.y = rope_pair(w.y, pos, rope_if[i0 + 1]);
+                w.z = rope_pair(w.z, pos, rope_if[i0 + 2]);
+                w.w = rope_pair(w.w, pos, rope_if[i0 + 3]);
+            }
+            *dst = w;
         }
     }
     SegmentWalker walk{g0, g1, L};
@@ -632,12 +661,20 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             const uint8_t *qs = qbuf + qi * RB * G::kQStride;
             uint32_t qb[HD / 16][2];
             {
-                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                    qs + (row0 + gq < row1 ? gq : 0) * G::kQStride);
+                const int qr = row0 + gq < row1 ? gq : 0;
+                const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + qr * G::kQStride);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     qb[kk][0] = qrow[kk * 8 + tq];
                     qb[kk][1] = qrow[kk * 8 + 4 + tq];
+                }
+                if (rope) {  // word w of a row is pair w
+                    const int qpos = posbuf[qi * RB + qr];
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        qb[kk][0] = rope_pair(qb[kk][0], qpos, rope_if[kk * 8 + tq]);
+                        qb[kk][1] = rope_pair(qb[kk][1], qpos, rope_if[kk * 8 + 4 + tq]);
+                    }
                 }
             }
             // this thread's S^T columns are rows 2tq and 2tq+1
@@ -668,6 +705,18 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const uint32_t kbase =
                         smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
+                    if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
+                        // new keys of the step, gathered unrotated from k_new:
+                        // rotate them in place (word w of a row is pair w)
+                        const int t_end = min(t0 + kChunk, seq_len);
+                        for (int t = max(t0, seq_len - p.q_rows); t < t_end; ++t)
+                            for (int w = lane; w < HD / 2; w += 32) {
+                                const uint32_t a =
+                                    kbase + piece_offset(hs, t - t0, w >> 2) + (w & 3) * 4;
+                                st_shared_u32(a, rope_pair(ld_shared_u32(a), t, rope_if[w]));
+                            }
+                        __syncwarp();
+                    }
                     const int m = lane >> 3;
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
                     {
@@ -787,6 +836,15 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         qa[mt][kk][hr] = qrow[kk * 8 + tq];
                         qa[mt][kk][2 + hr] = qrow[kk * 8 + 4 + tq];
                     }
+                    if (rope) {  // word w of a row is pair w
+    #pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            qa[mt][kk][hr] =
+                                rope_pair(qa[mt][kk][hr], rpos[mt][hr], rope_if[kk * 8 + tq]);
+                            qa[mt][kk][2 + hr] = rope_pair(qa[mt][kk][2 + hr], rpos[mt][hr],
+                                                           rope_if[kk * 8 + 4 + tq]);
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -815,6 +873,18 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const uint32_t kbase =
                         smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
+                    if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
+                        // new keys of the step, gathered unrotated from k_new:
+                        // rotate them in place (word w of a row is pair w)
+                        const int t_end = min(t0 + kChunk, seq_len);
+                        for (int t = max(t0, seq_len - p.q_rows); t < t_end; ++t)
+                            for (int w = lane; w < HD / 2; w += 32) {
+                                const uint32_t a =
+                                    kbase + piece_offset(hs, t - t0, w >> 2) + (w & 3) * 4;
+                                st_shared_u32(a, rope_pair(ld_shared_u32(a), t, rope_if[w]));
+                            }
+                        __syncwarp();
+                    }
                     float s[MT][2][4];
     #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
@@ -1201,14 +1271,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     }
 }
 
-template <int HD, int MT>
+template <int HD, int MT, bool ROPE>
 int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  const CUtensorMap &tk64, const CUtensorMap &tv64, bool merge,
                  cudaStream_t stream) {
     using G = Geo<HD, MT>;
     static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
                   "shared memory budget");
-    auto kern = decode_split_kernel<HD, MT>;
+    auto kern = decode_split_kernel<HD, MT, ROPE>;
     const size_t smem = G::kSmem;
     static int configured_device = -1;
     int dev = 0;
@@ -1273,7 +1343,8 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
-                  const void *k_new, const void *v_new, const int64_t *slot_mapping) {
+                  const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                  const float *rope_inv_freq) {
     // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][64]
     // (a half is 64 columns, 128 bytes, of one head's row): a box of
     // {64, rows, halves} brings both halves of `rows` slots of one head.
@@ -1314,6 +1385,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.k_new = k_new ? static_cast<const __nv_bfloat16 *>(k_new) + new_off : nullptr;
         p.v_new = v_new ? static_cast<const __nv_bfloat16 *>(v_new) + new_off : nullptr;
         p.slot_mapping = slot_mapping ? slot_mapping + (int64_t)b0 * q_rows : nullptr;
+        p.rope_inv_freq = rope_inv_freq;
         p.batch = nb;
         p.b_base = b0;
         p.q_rows = q_rows;
@@ -1336,14 +1408,19 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_parts = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) +
                                               plan.meta_offset);
         int rc;
+        const bool r = rope_inv_freq != nullptr;
+#define GQA_SPLIT(D, M)                                                                     \
+    (r ? dec::launch_split<D, M, true>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)    \
+       : dec::launch_split<D, M, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream))
         if (plan.head_dim == 128)
-            rc = plan.m_tiles == 0   ? dec::launch_split<128, 0>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<128, 1>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
-                                     : dec::launch_split<128, 2>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream);
+            rc = plan.m_tiles == 0 ? GQA_SPLIT(128, 0)
+                 : plan.m_tiles == 1 ? GQA_SPLIT(128, 1)
+                                     : GQA_SPLIT(128, 2);
         else
-            rc = plan.m_tiles == 0   ? dec::launch_split<64, 0>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
-                 : plan.m_tiles == 1 ? dec::launch_split<64, 1>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
-                                     : dec::launch_split<64, 2>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream);
+            rc = plan.m_tiles == 0 ? GQA_SPLIT(64, 0)
+                 : plan.m_tiles == 1 ? GQA_SPLIT(64, 1)
+                                     : GQA_SPLIT(64, 2);
+#undef GQA_SPLIT
         if (rc != ATTN_OK) return rc;
     }
     return ATTN_OK;

@@ -199,10 +199,19 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *   slot_mapping   int64 [batch * q_rows], device.  A slot outside
  *                  [0, num_slots) is skipped and reported as ATTN_ERR_BOUNDS
  *                  in *err_word.
+ *   rope_inv_freq  float32 [head_dim / 2], device, or NULL for none: rotary
+ *                  embedding of q and k_new before use (Voxtral notes,
+ *                  "RoPE" and "Shared Patterns"): the interleaved pairs
+ *                  (x[2i], x[2i+1]) of every head of a row at position p are
+ *                  rotated by the float32 angle p * rope_inv_freq[i], in
+ *                  float32, and rounded to bf16; the cache receives the
+ *                  rotated keys.  q row (b, r) uses positions[b*q_rows + r],
+ *                  new key row b*q_rows + r the position seq_lens[b] - q_rows + r.
  *   Every other argument, the workspace and the statuses are attn_decode's.
  */
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,
-                       const int64_t *slot_mapping, const attn_kv_cache *cache,
+                       const int64_t *slot_mapping, const float *rope_inv_freq,
+                       const attn_kv_cache *cache,
                        const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                        int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void *out, void *workspace, size_t workspace_bytes,

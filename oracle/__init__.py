@@ -62,6 +62,8 @@ def _load():
                                                   p, i64]
             lib.oracle_decode_weights.restype = i64
             lib.oracle_prefill.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, f64, p, i32, p]
+            lib.oracle_rope_bf16.argtypes = [p, i64, i32, i32, p, p, p]
+            lib.oracle_rope_bf16.restype = None
             lib.oracle_prefill.restype = i32
             _lib = lib
     return _lib
@@ -114,6 +116,21 @@ def kv_append(k_cache, v_cache, k_new, v_new, slot_mapping) -> int:
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     return int(_load().oracle_kv_append(_ptr(k_cache), _ptr(v_cache), num_slots, row, _ptr(kn),
                                         _ptr(vn), _ptr(sm), sm.shape[0]))
+
+
+def rope(x, positions, inv_freq) -> np.ndarray:
+    """Rotary embedding of interleaved pairs: x bf16 [n, heads, D] (tensor or
+    uint16 bits), positions int [n], inv_freq float32 [D/2].  Returns uint16
+    bf16 bits of the rotated rows (oracle_rope_bf16)."""
+    xb = _u16(x)
+    n, heads, D = xb.shape
+    pos = _i32(positions).reshape(-1)
+    inv = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float32).reshape(-1))
+    if pos.shape[0] != n or inv.shape[0] != D // 2:
+        raise ValueError("positions must have one entry per row and inv_freq D/2 entries")
+    out = np.empty_like(xb)
+    _load().oracle_rope_bf16(_ptr(xb), n, heads, D, _ptr(pos), _ptr(inv), _ptr(out))
+    return out
 
 
 def _cache_args(cache: dict):

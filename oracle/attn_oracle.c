@@ -35,6 +35,8 @@
  *    keys written including this step's rows).
  *  - Append: rows are applied in order, cache[slot_mapping[i]] = new[i],
  *    as raw 16-bit copies; with a repeated slot the last row wins.
+ *  - RoPE (for the fused append): interleaved pairs rotated by a float32
+ *    angle pos * inv_freq[i], see oracle_rope_bf16.
  *  - Prefill: query i of a sequence attends keys 0..i (and i - t < window
  *    when window > 0) of the same sequence (Voxtral notes, "Offline
  *    Encoder": causal SDPA).
@@ -106,6 +108,39 @@ int64_t oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache, int64_t num_slots
         }
     }
     return skipped;
+}
+
+/* Round a binary32 value to bf16, nearest even (NaN kept quiet). */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t w;
+    memcpy(&w, &f, sizeof w);
+    if ((w & 0x7F800000u) == 0x7F800000u && (w & 0x007FFFFFu) != 0)
+        return (uint16_t)((w >> 16) | 0x0040u);
+    const uint32_t lsb = (w >> 16) & 1u;
+    return (uint16_t)((w + 0x7FFFu + lsb) >> 16);
+}
+
+/* Rotary position embedding of interleaved pairs, as the pages state it
+ * (Voxtral Realtime notes, "RoPE": frequencies computed on the fly from the
+ * stored inv_freq; "Shared Patterns": the pairs are (x[2i], x[2i+1]) of each
+ * head, rotated after a float32 upcast and cast back):
+ *     theta_i = pos * inv_freq[i]                 (a float32 product)
+ *     (x0, x1) -> (x0 cos theta_i - x1 sin theta_i, x0 sin theta_i + x1 cos theta_i)
+ * The angle is the float32 product the pages form; its cosine and sine and
+ * the rotation are taken in double and rounded once (through binary32) to
+ * bf16.  x, out: bf16 bits [n, n_heads, head_dim]; pos[n]; inv_freq[head_dim / 2]. */
+void oracle_rope_bf16(const uint16_t *x, int64_t n, int n_heads, int head_dim,
+                      const int32_t *pos, const float *inv_freq, uint16_t *out) {
+    for (int64_t r = 0; r < n; ++r)
+        for (int h = 0; h < n_heads; ++h)
+            for (int i = 0; i < head_dim / 2; ++i) {
+                const int64_t e = (r * n_heads + h) * head_dim + 2 * i;
+                const float theta = (float)pos[r] * inv_freq[i];
+                const double c = cos((double)theta), sn = sin((double)theta);
+                const double x0 = oracle_bf16_to_f64(x[e]), x1 = oracle_bf16_to_f64(x[e + 1]);
+                out[e] = f32_to_bf16_rne((float)(x0 * c - x1 * sn));
+                out[e + 1] = f32_to_bf16_rne((float)(x0 * sn + x1 * c));
+            }
 }
 
 /* The cache as the oracle sees it. */

@@ -74,3 +74,55 @@ def test_fused_reports_out_of_range_slot():
     torch.cuda.synchronize()
     assert int(err.item()) == gq.ATTN_ERR_BOUNDS
     assert torch.isfinite(out.float()).all()
+
+
+def _ulp_diff(a_bits, b_bits):
+    """|a - b| in bf16 steps, for bit patterns of finite values."""
+    def key(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+ROPE_CASES = [
+    (LINEAR, 2, 1, 28, 4, 128, [14449, 900], {}),
+    (PAGED, 3, 4, 32, 8, 128, [64, 1030, 17], {"block_size": 16}),
+    (RING, 2, 4, 32, 32, 64, [6004, 777], {"window": 750, "ring": 1500}),
+]
+
+
+@pytest.mark.parametrize("kind,B,R,Hq,Hkv,D,seq,extra", ROPE_CASES)
+def test_fused_rope(kind, B, R, Hq, Hkv, D, seq, extra):
+    """q and the new keys rotated at their positions (interleaved pairs,
+    float32 angle p * inv_freq[i]) before the append and the attention."""
+    case = synth.decode_case(9400 + B * R + D + 10 * int(kind), kind, B, R, Hq, Hkv, D, seq,
+                             **extra)
+    inv = (1_000_000.0 ** (-np.arange(D // 2) / (D // 2))).astype(np.float32)
+    dev = "cuda"
+    cache = to_device(case, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gq.attn_decode_append(case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev),
+                                case.slot_mapping.to(dev), cache, case.seq_lens.to(dev),
+                                case.positions.to(dev), case.max_seq_len(), case.window,
+                                case.scale, err=err, rope_inv_freq=torch.from_numpy(inv).to(dev))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # oracle: rotate, append, attend
+    qpos = case.positions.numpy()
+    kpos = np.concatenate([np.arange(s - R, s) for s in case.seq_lens.tolist()])
+    qb = oracle.bf16_bits(case.q).reshape(B * R, Hq, D)
+    q_rot = oracle.rope(qb, qpos, inv).reshape(B, R, Hq, D)
+    k_rot = oracle.rope(oracle.bf16_bits(case.k_new), kpos, inv)
+    kc, vc = oracle.bf16_bits(case.k_cache).copy(), oracle.bf16_bits(case.v_cache).copy()
+    oracle.kv_append(kc, vc, k_rot, oracle.bf16_bits(case.v_new), case.slot_mapping.numpy())
+    cd = {"kind": case.kind, "k": kc, "v": vc, "slots_per_seq": case.slots_per_seq,
+          "block_table": None if case.block_table is None else case.block_table.numpy(),
+          "block_size": case.block_size}
+    rc, ref = oracle.decode(q_rot, cd, case.seq_lens.numpy(), qpos, case.window, case.scale,
+                            case.n_kv_heads)
+    assert rc == 0
+    compare(out, ref, f"fused rope {kind} R={R}")
+    # the cache holds the rotated keys (float rounding: at most one bf16 step apart)
+    assert np.array_equal(oracle.bf16_bits(cache.v), vc)
+    d = _ulp_diff(oracle.bf16_bits(cache.k), kc)
+    assert d.max() <= 1, f"rotated keys differ by {d.max()} bf16 steps"

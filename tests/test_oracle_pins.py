@@ -471,3 +471,67 @@ def test_slot_bookkeeping_matches_oracle_positions():
         b, j = divmod(s, 10)
         pos = int(case.positions[i])
         assert oracle.ring_abs_pos(j, int(case.seq_lens[b]), 10) == pos
+
+
+# ---------------------------------------------------------------- RoPE (fused append)
+
+def _bf16_of(values):
+    """float values -> bf16 bits by round-to-nearest-even of their float32."""
+    f = np.asarray(values, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_rope_position_zero_is_identity():
+    g = np.random.default_rng(31)
+    x = _bf16_of(g.standard_normal((5, 3, 16)))
+    inv = (10000.0 ** (-np.arange(8) / 8)).astype(np.float32)
+    assert np.array_equal(oracle.rope(x, np.zeros(5), inv), x)
+
+
+def test_rope_quarter_turn_swaps_the_pair():
+    """An angle of pi/2 maps (x0, x1) to (-x1, x0) (float32 pi/2 is off by
+    4e-8, far below a bf16 step)."""
+    g = np.random.default_rng(32)
+    x = _bf16_of(g.standard_normal((4, 2, 8)))
+    inv = np.full(4, np.float32(np.pi / 2), dtype=np.float32)
+    out = oracle.rope(x, np.ones(4), inv).view(np.int16).astype(np.int32)
+    xi = x.view(np.int16).astype(np.int32)
+    neg = lambda b: (b ^ -0x8000)  # flip the bf16 sign bit
+    assert np.array_equal(out[..., 0::2], neg(xi[..., 1::2]))
+    assert np.array_equal(out[..., 1::2], xi[..., 0::2])
+
+
+def test_rope_hand_value():
+    """(1, 0) at position 1 with inv_freq 1 is (cos 1, sin 1), rounded to bf16."""
+    x = _bf16_of([[[1.0, 0.0]]])
+    out = oracle.rope(x, [1], np.ones(1, dtype=np.float32))
+    assert np.array_equal(out.reshape(-1), _bf16_of([np.cos(1.0), np.sin(1.0)]))
+
+
+def test_rope_preserves_pair_norms():
+    g = np.random.default_rng(33)
+    x = _bf16_of(g.standard_normal((6, 4, 32)))
+    inv = (10000.0 ** (-np.arange(16) / 16)).astype(np.float32)
+    pos = g.integers(0, 40000, size=6)
+    y = oracle.bf16_to_f64(oracle.rope(x, pos, inv))
+    x64 = oracle.bf16_to_f64(x)
+    nx = np.hypot(x64[..., 0::2], x64[..., 1::2])
+    ny = np.hypot(y[..., 0::2], y[..., 1::2])
+    assert np.all(np.abs(ny - nx) <= 2.0 ** -7 * nx + 1e-30)
+
+
+def test_rope_scores_depend_on_relative_position():
+    """With power-of-two frequencies the float32 angles are exact, and
+    <rope(q, m), rope(k, n)> depends on m - n only (up to the bf16 rounding of
+    the rotated rows)."""
+    g = np.random.default_rng(34)
+    q = _bf16_of(g.standard_normal((1, 1, 64)))
+    k = _bf16_of(g.standard_normal((1, 1, 64)))
+    inv = (2.0 ** -np.arange(32)).astype(np.float32)
+    dots = []
+    for shift in (0, 7, 1000):
+        qr = oracle.bf16_to_f64(oracle.rope(q, [50 + shift], inv))
+        kr = oracle.bf16_to_f64(oracle.rope(k, [20 + shift], inv))
+        dots.append(float((qr * kr).sum()))
+    scale = float(np.linalg.norm(oracle.bf16_to_f64(q)) * np.linalg.norm(oracle.bf16_to_f64(k)))
+    assert max(dots) - min(dots) <= 2.0 ** -6 * scale
