@@ -281,9 +281,11 @@ class QwenWorkload(Workload):
                 for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
                     d[key].copy_(hd[key], non_blocking=True)
             c = self.caches[(s * 6 + 1 + i) % self.ncopy]
+            # seq_lens / positions are written before the step, never by the
+            # kernel just before a decode: it may plan while that one finishes
             gq.attn_decode_append(d["q"], d["k_new"], d["v_new"], d["slots"], c, d["seq"],
                                   d["pos"], self.max_seq, 0, self.scale, out=d["out"],
-                                  workspace=self.ws, err=self.err)
+                                  workspace=self.ws, err=self.err, tables_early=True)
             if e2e:
                 self.h["dec"][i]["out"].copy_(d["out"], non_blocking=True)
 
@@ -431,7 +433,8 @@ class DecodeOnlyWorkload(Workload):
             cache = self.caches[(s * self.layers + layer) % self.ncopy]
             self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
                                        c.seq_lens, c.positions, self.max_seq, c.window,
-                                       c.scale, out=self.out, workspace=self.ws, err=self.err)
+                                       c.scale, out=self.out, workspace=self.ws, err=self.err,
+                                       tables_early=True)
 
     def capture(self, stream, e2e=False):
         torch = self.torch

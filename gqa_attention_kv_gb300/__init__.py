@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_
                 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_ALIGN"}
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
+ATTN_DECODE_TABLES_EARLY = 1  # attn_decode_append flag (include/attn_kv.h)
 
 _lock = threading.Lock()
 _lib = None
@@ -66,7 +67,8 @@ def lib():
                                       ctypes.c_float, p, p, sz, p, p]
             L.attn_decode.restype = i32
             L.attn_decode_append.argtypes = [p, p, p, p, p, cp, p, p, i32, i32, i32, i32, i32,
-                                             i32, i32, ctypes.c_float, p, p, sz, p, p]
+                                             i32, i32, ctypes.c_float, p, p, sz, p,
+                                             ctypes.c_uint, p]
             L.attn_decode_append.restype = i32
             L.attn_prefill.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, ctypes.c_float, p,
                                        p, p]
@@ -180,13 +182,15 @@ def attn_decode(q, cache: KVCache, seq_lens, positions, max_seq_len, window, sca
 
 def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, positions,
                        max_seq_len, window, scale, out=None, workspace=None, err=None,
-                       stream=None, rope_inv_freq=None):
+                       stream=None, rope_inv_freq=None, tables_early=False):
     """The step's KV append and its decode in one launch: same result as
     attn_kv_append(k_new, v_new, slot_mapping, cache) then attn_decode(...)
     when new row b*R + r is the key at position seq_lens[b] - R + r.
     k_new / v_new bf16 [B*R, Hkv, D]; slot_mapping int64 [B*R].  With
     rope_inv_freq (float32 [D/2] on the device), q and k_new are first rotated
-    at their positions (interleaved pairs)."""
+    at their positions (interleaved pairs).  tables_early: seq_lens,
+    positions and the block table were not written by the kernel launched
+    just before on this stream (ATTN_DECODE_TABLES_EARLY)."""
     import torch
 
     B, R, Hq, D = q.shape
@@ -202,7 +206,7 @@ def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, 
         _ptr(positions), B, R, int(max_seq_len), int(window), Hq, cache.n_kv_heads, D,
         float(scale), _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(err),
-        _stream(stream))
+        ATTN_DECODE_TABLES_EARLY if tables_early else 0, _stream(stream))
     _check(rc, "attn_decode_append")
     return out
 

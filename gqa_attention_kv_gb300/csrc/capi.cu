@@ -182,11 +182,12 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
                        const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                        int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void *out, void *workspace, size_t workspace_bytes,
-                       int32_t *err_word, attn_stream_t stream) {
+                       int32_t *err_word, unsigned flags, attn_stream_t stream) {
     int rc = check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim,
                                 max_seq_len, window);
     if (rc != ATTN_OK) return rc;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
+    if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return ATTN_ERR_UNSUPPORTED;
     if (batch == 0) return ATTN_OK;
     if (!q || !k_new || !v_new || !slot_mapping || !seq_lens || !positions || !out ||
         !cache->k || !cache->v)
@@ -206,7 +207,7 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
     return gqa::launch_decode(plan, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
                               window, n_q_heads, n_kv_heads, scale, out, workspace, err_word,
                               reinterpret_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping,
-                              rope_inv_freq);
+                              rope_inv_freq, (flags & ATTN_DECODE_TABLES_EARLY) != 0);
 }
 
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,

@@ -93,6 +93,9 @@ struct Params {
     const __nv_bfloat16 *v_new;
     const int64_t *slot_mapping;
     const float *rope_inv_freq;  // [HD / 2] (nullptr: no rotary embedding)
+    // seq_lens, positions and block_table may be read before the previous
+    // kernel completes (ATTN_DECODE_TABLES_EARLY)
+    bool tables_early;
     int2 *ws_parts;     // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     int32_t *err;
 };
@@ -321,8 +324,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         prefetch_tensormap(&tm_k64);
         prefetch_tensormap(&tm_v64);
     }
-    pdl_wait();  // the cache, positions and seq_lens may come from the previous kernel
-    pdl_launch_dependents();
+    // Everything may come from the previous kernel (the cache, q, the new rows,
+    // and unless the caller says otherwise seq_lens and positions), and it may
+    // still read this call's out and workspace: wait for it before those.
+    if (!p.tables_early) pdl_wait();
 
     // ---- tables: chunk counts of every (request, row block), then Pb
     const int B = p.batch, RBc = p.row_blocks;
@@ -357,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         }
     }
     __syncthreads();
+    if (p.tables_early) pdl_wait();
+    pdl_launch_dependents();
     const int N = tb.Pb[B];
     // equal shares, but at least kMinChunksPerCta so small problems do not
     // spread a few keys over every SM
@@ -1344,7 +1351,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
-                  const float *rope_inv_freq) {
+                  const float *rope_inv_freq, bool tables_early) {
     // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][64]
     // (a half is 64 columns, 128 bytes, of one head's row): a box of
     // {64, rows, halves} brings both halves of `rows` slots of one head.
@@ -1386,6 +1393,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.v_new = v_new ? static_cast<const __nv_bfloat16 *>(v_new) + new_off : nullptr;
         p.slot_mapping = slot_mapping ? slot_mapping + (int64_t)b0 * q_rows : nullptr;
         p.rope_inv_freq = rope_inv_freq;
+        p.tables_early = tables_early;
         p.batch = nb;
         p.b_base = b0;
         p.q_rows = q_rows;

@@ -207,15 +207,22 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *                  float32, and rounded to bf16; the cache receives the
  *                  rotated keys.  q row (b, r) uses positions[b*q_rows + r],
  *                  new key row b*q_rows + r the position seq_lens[b] - q_rows + r.
+ *   flags          0, or ATTN_DECODE_TABLES_EARLY: seq_lens, positions and the
+ *                  block table were not written by the kernel issued just
+ *                  before this call on the stream, so the launch may read
+ *                  them (and plan its work) while that kernel finishes,
+ *                  under programmatic dependent launch.  Everything else is
+ *                  still read after it completes.
  *   Every other argument, the workspace and the statuses are attn_decode's.
  */
+#define ATTN_DECODE_TABLES_EARLY 1u
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,
                        const int64_t *slot_mapping, const float *rope_inv_freq,
                        const attn_kv_cache *cache,
                        const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                        int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void *out, void *workspace, size_t workspace_bytes,
-                       int32_t *err_word, attn_stream_t stream);
+                       int32_t *err_word, unsigned flags, attn_stream_t stream);
 
 /*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device

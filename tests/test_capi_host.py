@@ -153,12 +153,13 @@ def test_decode_append_validation(lib):
     cs = c.struct()
     f = lib.attn_decode_append
     need = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 4096, 0)
-    args = lambda q=16, kn=32, vn=48, sm=64, ws=1 << 20, ws_bytes=need, scale=0.1, hq=32: (
-        q, kn, vn, sm, None, ctypes.byref(cs), 80, 96, 2, 1, 4096, 0, hq, 8, 128, scale, 112, ws,
-        ws_bytes, None, None)
+    args = lambda q=16, kn=32, vn=48, sm=64, ws=1 << 20, ws_bytes=need, scale=0.1, hq=32, \
+        flags=0: (q, kn, vn, sm, None, ctypes.byref(cs), 80, 96, 2, 1, 4096, 0, hq, 8, 128, scale,
+                  112, ws, ws_bytes, None, flags, None)
     assert f(*args(kn=None)) == gq.ATTN_ERR_NULL
     assert f(*args(sm=None)) == gq.ATTN_ERR_NULL
     assert f(*args(vn=40)) == gq.ATTN_ERR_ALIGN
     assert f(*args(ws_bytes=need - 1)) == gq.ATTN_ERR_WORKSPACE
     assert f(*args(hq=30)) == gq.ATTN_ERR_SHAPE
     assert f(*args(scale=0.0)) == gq.ATTN_ERR_SHAPE
+    assert f(*args(flags=2)) == gq.ATTN_ERR_UNSUPPORTED

@@ -126,3 +126,25 @@ def test_fused_rope(kind, B, R, Hq, Hkv, D, seq, extra):
     assert np.array_equal(oracle.bf16_bits(cache.v), vc)
     d = _ulp_diff(oracle.bf16_bits(cache.k), kc)
     assert d.max() <= 1, f"rotated keys differ by {d.max()} bf16 steps"
+
+
+def test_tables_early_same_result():
+    """ATTN_DECODE_TABLES_EARLY changes when seq_lens and positions are read,
+    not what is computed: back-to-back calls (each launched while the previous
+    one finishes) give the same bits with and without it."""
+    dev = "cuda"
+    case = synth.decode_case(9500, PAGED, 4, 2, 32, 8, 128, [3000, 64, 1029, 2048],
+                             block_size=16)
+    outs = {}
+    for early in (False, True):
+        cache = to_device(case, dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = (case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev),
+                case.slot_mapping.to(dev), cache, case.seq_lens.to(dev), case.positions.to(dev),
+                case.max_seq_len(), 0, case.scale)
+        res = [gq.attn_decode_append(*args, err=err, tables_early=early) for _ in range(4)]
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs[early] = res
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
