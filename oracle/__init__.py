@@ -65,6 +65,16 @@ def _load():
             lib.oracle_rope_bf16.argtypes = [p, i64, i32, i32, p, p, p]
             lib.oracle_rope_bf16.restype = None
             lib.oracle_prefill.restype = i32
+            lib.oracle_fp8_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_fp8_e4m3_to_f64.restype = f64
+            lib.oracle_f32_to_fp8_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_fp8_e4m3.restype = ctypes.c_uint8
+            lib.oracle_fp8_e4m3_to_bf16.argtypes = [ctypes.c_uint8]
+            lib.oracle_fp8_e4m3_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_kv_append_fp8.argtypes = [p, p, i64, i64, p, p, p, p, i64]
+            lib.oracle_kv_append_fp8.restype = i64
+            lib.oracle_kv_reference.argtypes = [p, i64, i64, p]
+            lib.oracle_kv_reference.restype = None
             _lib = lib
     return _lib
 
@@ -131,6 +141,60 @@ def rope(x, positions, inv_freq) -> np.ndarray:
     out = np.empty_like(xb)
     _load().oracle_rope_bf16(_ptr(xb), n, heads, D, _ptr(pos), _ptr(inv), _ptr(out))
     return out
+
+
+def fp8_to_f64(codes) -> np.ndarray:
+    """Values of E4M3 codes (uint8 array) as fp64 (oracle_fp8_e4m3_to_f64)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    lib = _load()
+    table = np.array([lib.oracle_fp8_e4m3_to_f64(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def f32_to_fp8(x) -> np.ndarray:
+    """E4M3 codes of float32 values (oracle_f32_to_fp8_e4m3), elementwise."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    lib = _load()
+    flat = np.array([lib.oracle_f32_to_fp8_e4m3(float(v)) for v in a.reshape(-1)],
+                    dtype=np.uint8)
+    return flat.reshape(a.shape)
+
+
+def fp8_to_bf16_bits(codes) -> np.ndarray:
+    """E4M3 codes -> bf16 bit patterns of the same values (exact)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    lib = _load()
+    table = np.array([lib.oracle_fp8_e4m3_to_bf16(i) for i in range(256)], dtype=np.uint16)
+    return table[c]
+
+
+def kv_append_fp8(k_cache, v_cache, k_new, v_new, slot_mapping, k_ref=None) -> int:
+    """In place on uint8 caches [S, Hkv, D]: k_cache[slot] = E4M3(k - k_ref),
+    v_cache[slot] = E4M3(v) in row order (oracle_kv_append_fp8).  k_ref:
+    float32 [Hkv, D] or None.  Returns skipped rows."""
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint8 or not c.flags.c_contiguous:
+            raise TypeError("FP8 caches must be C-contiguous uint8 arrays")
+    num_slots = k_cache.shape[0]
+    row = int(np.prod(k_cache.shape[1:]))
+    kn, vn = _u16(k_new), _u16(v_new)
+    ref = None if k_ref is None else np.ascontiguousarray(k_ref, dtype=np.float32).reshape(-1)
+    if ref is not None and ref.shape[0] != row:
+        raise ValueError("k_ref must hold n_kv_heads * head_dim values")
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return int(_load().oracle_kv_append_fp8(_ptr(k_cache), _ptr(v_cache), num_slots, row,
+                                            _ptr(kn), _ptr(vn), _ptr(ref), _ptr(sm),
+                                            sm.shape[0]))
+
+
+def kv_reference(k) -> np.ndarray:
+    """Mean over rows of bf16 keys [n, Hkv, D] (uint16 bits), fp64 [Hkv, D]."""
+    kb = _u16(k)
+    n = kb.shape[0]
+    row = int(np.prod(kb.shape[1:]))
+    out = np.empty(row, dtype=np.float64)
+    _load().oracle_kv_reference(_ptr(kb), n, row, _ptr(out))
+    return out.reshape(kb.shape[1:])
 
 
 def _cache_args(cache: dict):

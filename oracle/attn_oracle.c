@@ -37,6 +37,9 @@
  *    as raw 16-bit copies; with a repeated slot the last row wins.
  *  - RoPE (for the fused append): interleaved pairs rotated by a float32
  *    angle pos * inv_freq[i], see oracle_rope_bf16.
+ *  - FP8 cache (vibevoice.c, "KV cache"): K and V held as 8-bit floats with
+ *    no scale factor, K stored relative to a per-layer reference vector
+ *    built from the first prefill chunk; see the FP8 section below.
  *  - Prefill: query i of a sequence attends keys 0..i (and i - t < window
  *    when window > 0) of the same sequence (Voxtral notes, "Offline
  *    Encoder": causal SDPA).
@@ -141,6 +144,105 @@ void oracle_rope_bf16(const uint16_t *x, int64_t n, int n_heads, int head_dim,
                 out[e] = f32_to_bf16_rne((float)(x0 * c - x1 * sn));
                 out[e + 1] = f32_to_bf16_rne((float)(x0 * sn + x1 * c));
             }
+}
+
+/* ---- FP8 KV cache (vibevoice.c, "KV cache") ----------------------------
+ * The page fixes: the cache holds 8-bit floats converted by bit manipulation
+ * alone (no scale factor), and K is stored relative to a per-layer reference
+ * vector built from the first prefill chunk, which changes no attention
+ * output because softmax ignores a shift shared by every key's score.
+ * Readings taken where it is silent:
+ *   - the format is E4M3 of the OCP 8-bit floating point specification:
+ *     sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+ *     holds subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no
+ *     infinities; the largest finite magnitude is 1.75 * 2^8 = 448;
+ *   - encoding rounds to nearest with ties to an even mantissa and saturates
+ *     every larger magnitude (infinity included) to 448; NaN encodes as 0x7F;
+ *   - the reference is one float32 vector per KV head (the layer's key
+ *     projection output split by head): the mean of the chunk's keys;
+ *   - the difference k - ref is formed in binary32 and that value is
+ *     encoded. */
+
+/* Value of an E4M3 code, from the format's definition. */
+double oracle_fp8_e4m3_to_f64(uint8_t code) {
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Nearest integer to x >= 0, ties to even (x is exact in double). */
+static double round_half_even(double x) {
+    const double f = floor(x), r = x - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* E4M3 code of a binary32 value: round to nearest even, saturate to 448. */
+uint8_t oracle_f32_to_fp8_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; a count of 8 is the smallest
+         * normal, whose code is 8 as well */
+        return sign | (uint8_t)round_half_even(ldexp(a, 9));
+    }
+    int E;
+    frexp(a, &E); /* a in [2^(E-1), 2^E) */
+    int e = E - 1;
+    double m = round_half_even((ldexp(a, -e) - 1.0) * 8.0); /* 0 .. 8 */
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    const int field = e + 7;
+    if (field > 15 || (field == 15 && m == 7.0)) return sign | 0x7E;
+    return sign | (uint8_t)((field << 3) | (int)m);
+}
+
+/* E4M3 code -> bf16 bits.  Every E4M3 value is a bf16 value, so this is exact. */
+uint16_t oracle_fp8_e4m3_to_bf16(uint8_t code) {
+    return f32_to_bf16_rne((float)oracle_fp8_e4m3_to_f64(code));
+}
+
+/* FP8 append: for rows i = 0..n-1 in order, with s = slot_mapping[i] in
+ * [0, num_slots) (other rows are skipped and counted):
+ *     k_cache[s][e] = E4M3(float32(k_new[i][e]) - k_ref[e])   (k_ref NULL: no shift)
+ *     v_cache[s][e] = E4M3(float32(v_new[i][e]))
+ * e runs over the row's n_kv_heads * head_dim elements; k_ref is float32
+ * [n_kv_heads][head_dim].  Caches are byte arrays [num_slots][row_elems]. */
+int64_t oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, int64_t num_slots,
+                             int64_t row_elems, const uint16_t *k_new, const uint16_t *v_new,
+                             const float *k_ref, const int64_t *slot_mapping, int64_t n) {
+    int64_t skipped = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0 || s >= num_slots) {
+            ++skipped;
+            continue;
+        }
+        for (int64_t e = 0; e < row_elems; ++e) {
+            const float kf = (float)oracle_bf16_to_f64(k_new[i * row_elems + e]);
+            volatile float d = k_ref ? kf - k_ref[e] : kf; /* a binary32 difference */
+            k_cache[s * row_elems + e] = oracle_f32_to_fp8_e4m3(d);
+            v_cache[s * row_elems + e] =
+                oracle_f32_to_fp8_e4m3((float)oracle_bf16_to_f64(v_new[i * row_elems + e]));
+        }
+    }
+    return skipped;
+}
+
+/* Reference vector: ref[e] = (1/n) * sum_i k[i][e] over the n rows of a
+ * chunk, in fp64.  k: bf16 bits [n][row_elems]. */
+void oracle_kv_reference(const uint16_t *k, int64_t n, int64_t row_elems, double *ref) {
+    for (int64_t e = 0; e < row_elems; ++e) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < n; ++i) acc += oracle_bf16_to_f64(k[i * row_elems + e]);
+        ref[e] = n > 0 ? acc / (double)n : 0.0;
+    }
 }
 
 /* The cache as the oracle sees it. */
