@@ -101,12 +101,13 @@ def prefill_flops(T, Hq, D, window=0):
     return 4.0 * D * Hq * pairs
 
 
-def decode_bytes(keys_per_request_head, Hkv, D, B, R, Hq, append_rows):
+def decode_bytes(keys_per_request_head, Hkv, D, B, R, Hq, append_rows, kv_elem=2):
     """K+V bytes of the valid keys (each KV head read once) + q + out + the
-    appended rows (read + write)."""
-    kv = 2 * 2 * D * Hkv * keys_per_request_head
+    appended rows (bf16 read + cache write); kv_elem = bytes per cache element
+    (2: bf16, 1: FP8)."""
+    kv = 2 * kv_elem * D * Hkv * keys_per_request_head
     qo = 2 * 2 * B * R * Hq * D
-    app = 2 * 2 * 2 * append_rows * Hkv * D
+    app = 2 * (2 + kv_elem) * append_rows * Hkv * D
     return kv + qo + app
 
 
@@ -371,21 +372,44 @@ class DecodeOnlyWorkload(Workload):
         from gqa_attention_kv_gb300 import synth
 
         self.gq, self.torch = gq, torch
+        self.fp8 = which.endswith("-fp8")
+        which = which[:-4] if self.fp8 else which
         make = {"voxtral": synth.voxtral_decode_step, "ring": synth.ring_window_decode,
                 "stream-encoder": synth.streaming_encoder_step,
                 "paged": synth.paged_multirow_decode}[which]
         base = make(device=dev)
         self.case = base
-        per_copy = 2 * base.k_cache.numel() * 2
+        self.kv_elem = 1 if self.fp8 else 2
+        per_copy = 2 * base.k_cache.numel() * self.kv_elem
         self.ncopy = max(2, min(256, math.ceil(4 * _l2_bytes() / per_copy) + 1))
         g = synth.generator(777, dev)
-        self.caches = [gq.KVCache(base.kind, base.k_cache if i == 0 else
-                                  synth.normal_bf16(g, base.k_cache.shape, dev),
-                                  base.v_cache if i == 0 else
-                                  synth.normal_bf16(g, base.v_cache.shape, dev),
-                                  slots_per_seq=base.slots_per_seq,
-                                  block_table=base.block_table, block_size=base.block_size)
-                       for i in range(self.ncopy)]
+        if self.fp8:
+            # E4M3 caches (keys relative to the reference of the first 512
+            # rows), written by the library's own FP8 append
+            S, Hkv, D = base.k_cache.shape
+            all_slots = torch.arange(S, dtype=torch.int64, device=dev)
+            self.k_ref = gq.attn_kv_reference(base.k_cache[:512])
+            self.caches = []
+            for i in range(self.ncopy):
+                kb = base.k_cache if i == 0 else synth.normal_bf16(g, base.k_cache.shape, dev)
+                vb = base.v_cache if i == 0 else synth.normal_bf16(g, base.v_cache.shape, dev)
+                c = gq.KVCache(base.kind, torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev),
+                               torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev),
+                               slots_per_seq=base.slots_per_seq, block_table=base.block_table,
+                               block_size=base.block_size, dtype=gq.ATTN_KV_FP8_E4M3,
+                               k_ref=self.k_ref)
+                gq.attn_kv_append(kb, vb, all_slots, c)
+                self.caches.append(c)
+                del kb, vb
+            torch.cuda.synchronize()
+        else:
+            self.caches = [gq.KVCache(base.kind, base.k_cache if i == 0 else
+                                      synth.normal_bf16(g, base.k_cache.shape, dev),
+                                      base.v_cache if i == 0 else
+                                      synth.normal_bf16(g, base.v_cache.shape, dev),
+                                      slots_per_seq=base.slots_per_seq,
+                                      block_table=base.block_table, block_size=base.block_size)
+                           for i in range(self.ncopy)]
         self.max_seq = base.max_seq_len()
         self.ws = torch.zeros(gq.attn_decode_workspace_size(
             self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window),
@@ -393,7 +417,8 @@ class DecodeOnlyWorkload(Workload):
         self.out = torch.empty_like(base.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
-        self.launches_per_step = 1 + merge_kernel_launched(
+        # fused append + decode (bf16), or append then decode (FP8)
+        self.launches_per_step = (2 if self.fp8 else 1) + merge_kernel_launched(
             self.max_seq, base.window, base.q_rows,
             base.slots_per_seq if base.kind == synth.RING else None)
         # valid keys per (request, row) summed over rows' union per request
@@ -418,23 +443,32 @@ class DecodeOnlyWorkload(Workload):
                      "stream-encoder": "streaming encoder step, 4 frames over a 1500-slot ring, "
                                        "window 750, 32/32 D=64, 32 layers",
                      "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16"}[which]
+        if self.fp8:
+            self.name += ", FP8 (E4M3) cache"
         self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
-                         "layers_per_step": self.layers,
-                         "l2_defeat": "caches rotate over copies > 4x L2"}
+                         "layers_per_step": self.layers, "kv_cache": "fp8_e4m3" if self.fp8
+                         else "bf16", "l2_defeat": "caches rotate over copies > 4x L2"}
 
     def decode_bytes_per_step(self):
         c = self.case
         return self.layers * decode_bytes(self.keys, c.n_kv_heads, c.head_dim, c.batch,
-                                          c.q_rows, c.n_q_heads, c.batch * c.q_rows)
+                                          c.q_rows, c.n_q_heads, c.batch * c.q_rows,
+                                          self.kv_elem)
 
     def _decode_part(self, s):
         c = self.case
         for layer in range(self.layers):
             cache = self.caches[(s * self.layers + layer) % self.ncopy]
-            self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
-                                       c.seq_lens, c.positions, self.max_seq, c.window,
-                                       c.scale, out=self.out, workspace=self.ws, err=self.err,
-                                       tables_early=True)
+            if self.fp8:
+                self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
+                self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq,
+                                    c.window, c.scale, out=self.out, workspace=self.ws,
+                                    err=self.err)
+            else:
+                self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
+                                           c.seq_lens, c.positions, self.max_seq, c.window,
+                                           c.scale, out=self.out, workspace=self.ws,
+                                           err=self.err, tables_early=True)
 
     def capture(self, stream, e2e=False):
         torch = self.torch
@@ -507,7 +541,8 @@ class PrefillOnlyWorkload(Workload):
 def make_workload(name, dev):
     if name == "qwen":
         return QwenWorkload(dev)
-    if name in ("voxtral", "ring", "paged", "stream-encoder"):
+    if name in ("voxtral", "ring", "paged", "stream-encoder", "ring-fp8", "paged-fp8",
+                "voxtral-fp8"):
         return DecodeOnlyWorkload(dev, name)
     if name in ("encoder", "encoder-long", "qwen-prefill", "prefill-8k"):
         return PrefillOnlyWorkload(dev, name)
@@ -633,7 +668,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen",
                     choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged",
-                             "stream-encoder",
+                             "stream-encoder", "ring-fp8", "paged-fp8", "voxtral-fp8",
                              "qwen-prefill", "prefill-8k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -762,7 +797,9 @@ def main():
             "unit": "GB/s" if dec_gbs is not None else "TFLOP/s",
             "n_gpus": world, "steps": K, "warmup": warmup,
             "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 cache, f16 mma" if getattr(wl, "fp8", False) else "bf16",
+            "data": "synthetic",
             "config": dict(wl.describe) | {"parallelism": f"replicas x{world}" if world > 1
                                             else "single GPU"},
             "step_ms": {"prefill": round(pre_ms / K, 4), "prompt_append": round(app_ms / K, 4),

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
 ATTN_DECODE_TABLES_EARLY = 1  # attn_decode_append flag (include/attn_kv.h)
+ATTN_KV_BF16, ATTN_KV_FP8_E4M3 = 0, 1  # cache element types (attn_kv_dtype)
 
 _lock = threading.Lock()
 _lib = None
@@ -44,7 +45,8 @@ class _Cache(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("num_slots", ctypes.c_int64), ("slots_per_seq", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32),
-                ("max_blocks_per_seq", ctypes.c_int32)]
+                ("max_blocks_per_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("k_ref", ctypes.c_void_p)]
 
 
 def lib():
@@ -70,6 +72,11 @@ def lib():
                                              i32, i32, ctypes.c_float, p, p, sz, p,
                                              ctypes.c_uint, p]
             L.attn_decode_append.restype = i32
+            L.attn_decode_noalloc.argtypes = [p, cp, p, p, i32, i32, i32, i32, i32, i32, i32,
+                                              ctypes.c_float, p, p, p]
+            L.attn_decode_noalloc.restype = i32
+            L.attn_kv_reference.argtypes = [p, i64, i32, i32, p, p]
+            L.attn_kv_reference.restype = i32
             L.attn_prefill.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, ctypes.c_float, p,
                                        p, p]
             L.attn_prefill.restype = i32
@@ -109,18 +116,23 @@ def _check(rc, where):
 
 
 class KVCache:
-    """One layer's cache: k, v bf16 [num_slots, n_kv_heads, head_dim] on the device.
+    """One layer's cache: k, v [num_slots, n_kv_heads, head_dim] on the device,
+    bf16, or uint8 E4M3 codes for an FP8 cache (dtype ATTN_KV_FP8_E4M3, whose
+    keys are stored relative to k_ref, float32 [n_kv_heads, head_dim] or None).
 
     kind LINEAR: slots_per_seq = per-request capacity.
     kind PAGED : block_table int32 [batch, max_blocks_per_seq] (device), block_size.
     kind RING  : slots_per_seq = ring size.
     """
 
-    def __init__(self, kind, k, v, slots_per_seq=0, block_table=None, block_size=0):
+    def __init__(self, kind, k, v, slots_per_seq=0, block_table=None, block_size=0,
+                 dtype=ATTN_KV_BF16, k_ref=None):
         self.kind, self.k, self.v = int(kind), k, v
         self.slots_per_seq = int(slots_per_seq)
         self.block_table = block_table
         self.block_size = int(block_size)
+        self.dtype = int(dtype)
+        self.k_ref = k_ref
 
     @property
     def n_kv_heads(self):
@@ -134,7 +146,8 @@ class KVCache:
         bt = self.block_table
         return _Cache(self.kind, self.k.data_ptr(), self.v.data_ptr(), self.k.shape[0],
                       self.slots_per_seq, None if bt is None else bt.data_ptr(),
-                      self.block_size, 0 if bt is None else bt.shape[-1])
+                      self.block_size, 0 if bt is None else bt.shape[-1], self.dtype,
+                      None if self.k_ref is None else self.k_ref.data_ptr())
 
 
 def attn_kv_append(k_new, v_new, slot_mapping, cache: KVCache, err=None, stream=None):
@@ -144,6 +157,19 @@ def attn_kv_append(k_new, v_new, slot_mapping, cache: KVCache, err=None, stream=
                               slot_mapping.shape[0], ctypes.byref(c), cache.n_kv_heads,
                               cache.head_dim, _ptr(err), _stream(stream))
     _check(rc, "attn_kv_append")
+
+
+def attn_kv_reference(k, ref=None, stream=None):
+    """Per-head mean of bf16 keys k [n, Hkv, D] as float32 [Hkv, D] (the FP8
+    cache's reference vector).  Writes into ref if given."""
+    import torch
+
+    n, Hkv, D = k.shape
+    if ref is None:
+        ref = torch.empty(Hkv, D, dtype=torch.float32, device=k.device)
+    rc = lib().attn_kv_reference(_ptr(k), n, Hkv, D, _ptr(ref), _stream(stream))
+    _check(rc, "attn_kv_reference")
+    return ref
 
 
 def attn_decode_workspace_size(cache: KVCache, batch, q_rows, n_q_heads, max_seq_len,
@@ -232,13 +258,7 @@ def attn_decode_noalloc(q, cache: KVCache, seq_lens, positions, max_seq_len, win
     GPU share that array and race; order them on one stream."""
     import torch
 
-    L = lib()
-    f = L.attn_decode_noalloc
-    if f.restype is not ctypes.c_int:
-        p, i32 = ctypes.c_void_p, ctypes.c_int
-        f.argtypes = [p, ctypes.POINTER(_Cache), p, p, i32, i32, i32, i32, i32, i32, i32,
-                      ctypes.c_float, p, p, p]
-        f.restype = i32
+    f = lib().attn_decode_noalloc
     B, R, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)

@@ -7,6 +7,7 @@
 // for the frame).  It is a pure copy: each thread moves 16-byte pieces, and
 // consecutive threads move consecutive pieces of one row, so both the read of
 // the new rows and the write into the slot are coalesced.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -41,6 +42,110 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
         uint4 *dst = tensor == 0 ? k_cache : v_cache;
         dst[slot * pieces_per_row + piece] = __ldg(src + row * pieces_per_row + piece);
     }
+}
+
+// FP8 cache (vibevoice.c, "KV cache"): each thread writes one 16-byte piece
+// of a cache row, 16 E4M3 codes, from 32 bytes of bf16 input; a K element is
+// shifted by the reference vector first, the difference formed in fp32.
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+    const float4 *__restrict__ k_ref, const int64_t *__restrict__ slot_mapping, int64_t n,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
+    int pieces_per_row, int32_t *err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t per_row = 2ll * pieces_per_row;
+    const int64_t total = n * per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += stride) {
+        const int64_t row = idx / per_row;
+        const int rem = (int)(idx - row * per_row);
+        const int tensor = rem / pieces_per_row;  // 0: K, 1: V
+        const int piece = rem - tensor * pieces_per_row;
+        const int64_t slot = __ldg(slot_mapping + row);
+        if (slot < 0 || slot >= num_slots) {
+            if (rem == 0) report_error(err, ATTN_ERR_BOUNDS);
+            continue;
+        }
+        // 16 bf16 inputs: two 16-byte loads
+        const uint4 *src = (tensor == 0 ? k_new : v_new) + (row * pieces_per_row + piece) * 2;
+        const uint4 a = __ldg(src), b = __ldg(src + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        if (tensor == 0 && k_ref != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 r = __ldg(k_ref + piece * 4 + i);
+                x[4 * i] = __fsub_rn(x[4 * i], r.x);
+                x[4 * i + 1] = __fsub_rn(x[4 * i + 1], r.y);
+                x[4 * i + 2] = __fsub_rn(x[4 * i + 2], r.z);
+                x[4 * i + 3] = __fsub_rn(x[4 * i + 3], r.w);
+            }
+        }
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1]) |
+                   (f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]) << 16);
+        uint4 *dst = tensor == 0 ? k_cache : v_cache;
+        dst[slot * pieces_per_row + piece] = make_uint4(c[0], c[1], c[2], c[3]);
+    }
+}
+
+// Reference vector: ref[e] = mean over n rows of k[i][e].  Block: 32 columns
+// x 8 row lanes; each thread sums every 8th row in fp64, the 8 partial sums
+// are added in a fixed order, so the result does not depend on timing.
+__global__ void __launch_bounds__(256) kv_reference_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                           int64_t n, int row_elems,
+                                                           float *__restrict__ ref) {
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ double part[8][32];
+    const int col = blockIdx.x * 32 + (threadIdx.x & 31), lane_row = threadIdx.x >> 5;
+    double acc = 0.0;
+    if (col < row_elems)
+        for (int64_t i = lane_row; i < n; i += 8)
+            acc += (double)__bfloat162float(k[i * row_elems + col]);
+    part[lane_row][threadIdx.x & 31] = acc;
+    __syncthreads();
+    if (lane_row == 0 && col < row_elems) {
+        double s = 0.0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) s += part[r][threadIdx.x];
+        ref[col] = (float)(s / (double)n);
+    }
+}
+
+int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,
+                        cudaStream_t stream) {
+    const unsigned blocks = (unsigned)((row_elems + 31) / 32);
+    const cudaError_t e = launch_pdl(kv_reference_kernel, dim3(blocks), dim3(256), 0, stream,
+                                     static_cast<const __nv_bfloat16 *>(k), n, row_elems, ref);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_ref,
+                         const int64_t *slot_mapping, int64_t n, void *k_cache, void *v_cache,
+                         int64_t num_slots, int row_elems, int32_t *err, cudaStream_t stream) {
+    if (n <= 0) return ATTN_OK;
+    const int pieces = row_elems / 16;  // 16 codes per piece
+    const int64_t total = n * 2ll * pieces;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    const cudaError_t e = launch_pdl(
+        kv_append_fp8_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+        reinterpret_cast<const float4 *>(k_ref), slot_mapping, n, static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), num_slots, pieces, err);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,

@@ -50,7 +50,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
+                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128,
+                       bool bytes) {
     auto fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t gd[5];
@@ -62,7 +63,8 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint6
         es[i] = 1;
         if (i + 1 < rank) gs[i] = strides_bytes[i];
     }
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+    CUresult r = fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    (cuuint32_t)rank,
                     const_cast<void *>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -91,6 +93,9 @@ int check_decode_shape(const attn_kv_cache *cache, int batch, int q_rows, int n_
         return ATTN_ERR_SHAPE;
     }
     if (cache->num_slots < 1 || cache->num_slots >= (int64_t(1) << 31)) return ATTN_ERR_SHAPE;
+    if (cache->dtype != ATTN_KV_BF16 && cache->dtype != ATTN_KV_FP8_E4M3)
+        return ATTN_ERR_UNSUPPORTED;
+    if (cache->dtype == ATTN_KV_FP8_E4M3 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     switch (cache->kind) {
     case ATTN_CACHE_LINEAR:
         if (cache->slots_per_seq < 1 ||
@@ -131,9 +136,27 @@ int attn_kv_append(const void *k_new, const void *v_new, const int64_t *slot_map
     if (cache->num_slots < 1) return ATTN_ERR_SHAPE;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cache->k) || !aligned16(cache->v))
         return ATTN_ERR_ALIGN;
+    if (cache->dtype == ATTN_KV_FP8_E4M3) {
+        if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+        if (cache->k_ref && !aligned16(cache->k_ref)) return ATTN_ERR_ALIGN;
+        return gqa::launch_kv_append_fp8(k_new, v_new, cache->k_ref, slot_mapping, n, cache->k,
+                                         cache->v, cache->num_slots, n_kv_heads * head_dim,
+                                         err_word, reinterpret_cast<cudaStream_t>(stream));
+    }
+    if (cache->dtype != ATTN_KV_BF16) return ATTN_ERR_UNSUPPORTED;
     return gqa::launch_kv_append(k_new, v_new, slot_mapping, n, cache->k, cache->v,
                                  cache->num_slots, n_kv_heads * head_dim * 2, err_word,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_kv_reference(const void *k, int64_t n, int n_kv_heads, int head_dim, float *ref,
+                      attn_stream_t stream) {
+    if (n < 1 || n_kv_heads < 1 || head_dim < 1) return ATTN_ERR_SHAPE;
+    if ((int64_t)n_kv_heads * head_dim >= (int64_t(1) << 31)) return ATTN_ERR_SHAPE;
+    if (!k || !ref) return ATTN_ERR_NULL;
+    if (!aligned16(k) || !aligned16(ref)) return ATTN_ERR_ALIGN;
+    return gqa::launch_kv_reference(k, n, n_kv_heads * head_dim, ref,
+                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_rows,
@@ -188,6 +211,7 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
     if (rc != ATTN_OK) return rc;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
     if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return ATTN_ERR_UNSUPPORTED;
+    if (cache->dtype != ATTN_KV_BF16) return ATTN_ERR_UNSUPPORTED;
     if (batch == 0) return ATTN_OK;
     if (!q || !k_new || !v_new || !slot_mapping || !seq_lens || !positions || !out ||
         !cache->k || !cache->v)
@@ -234,7 +258,9 @@ const char *attn_status_string(int status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_NULL: return "a required pointer is NULL";
     case ATTN_ERR_SHAPE: return "inconsistent or out-of-range sizes";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 64 or 128)";
+    case ATTN_ERR_UNSUPPORTED:
+        return "unsupported request (head_dim other than 64 / 128, an FP8 cache where it is not "
+               "implemented, an unknown dtype or flag)";
     case ATTN_ERR_WORKSPACE: return "workspace too small";
     case ATTN_ERR_BOUNDS: return "slot, page or position outside its buffer";
     case ATTN_ERR_TIMEOUT: return "a bounded device wait gave up";

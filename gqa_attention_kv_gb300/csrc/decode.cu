@@ -103,11 +103,14 @@ struct Params {
 // MT = 0: up to 8 query rows per unit; keys are the M dimension of the
 //         mma (S^T = K Q^T, O^T = V^T P^T), rows the N dimension of 8.
 // MT = 1, 2: 16 or 32 rows per unit; rows are the M dimension.
-template <int HD, int MT>
+// FP8: the cache holds 1-byte E4M3 elements (head_dim 128: one 128-byte block
+// per head row) instead of bf16.
+template <int HD, int MT, bool FP8 = false>
 struct Geo {
     static constexpr int RB = MT == 0 ? 8 : 16 * MT;        // rows per unit
     static constexpr int kCtasPerSm = MT == 2 ? 1 : 2;
-    static constexpr int kHalves = HD / 64;                 // 128-byte column blocks
+    static constexpr int kElem = FP8 ? 1 : 2;               // bytes per cache element
+    static constexpr int kHalves = HD * kElem / 128;        // 128-byte column blocks
     static constexpr int kChunkBytes = kHalves * kChunk * 128;
     static constexpr int kTileBytes = kWarps * kChunkBytes;  // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
@@ -139,6 +142,7 @@ struct Geo {
     static constexpr size_t kSmem = 1024 + kOffQ + kQBytes;
     static_assert(kStages >= 3 || MT == 2, "three stages for up to 16 rows");
     static_assert(kStages >= 2, "at least a double-buffered ring");
+    static_assert(!FP8 || HD == 128, "FP8 caches have 128-element heads");
 };
 
 constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
@@ -157,17 +161,29 @@ __device__ __forceinline__ uint32_t rope_pair(uint32_t w, int pos, float inv_fre
 //   whole tile (one TMA box of 64 rows): [half][64 rows][128 B]
 //   chunked    (16-row boxes / rows)   : [chunk][half][16 rows][128 B]
 // Chunk c's rows start at chunk_base() and its halves are half_stride() apart.
-template <int HD>
+template <int HALVES>
 __device__ __forceinline__ uint32_t chunk_base(bool whole, int c) {
-    return whole ? (uint32_t)c * (kChunk * 128) : (uint32_t)c * ((HD / 64) * kChunk * 128);
+    return whole ? (uint32_t)c * (kChunk * 128) : (uint32_t)c * (HALVES * kChunk * 128);
 }
 __device__ __forceinline__ uint32_t half_stride(bool whole) {
     return whole ? (uint32_t)(kTileRows * 128) : (uint32_t)(kChunk * 128);
 }
-// Offset of 16-byte piece c16 (0 .. HD/8-1) of row `key` (0 .. 15) of a chunk.
+// Offset of 16-byte piece c16 (0 .. row bytes / 16 - 1) of row `key` (0 .. 15)
+// of a chunk.
 __device__ __forceinline__ uint32_t piece_offset(uint32_t hstride, int key, int c16) {
     const int half = c16 >> 3, cc = c16 & 7;
     return half * hstride + key * 128 + ((cc ^ (key & 7)) << 4);
+}
+
+// Where a warp parks 16-byte unit u (0 .. HD/4-1) of output row `row` for the
+// end-of-segment merge.  The FP8 paths hold whole 16-byte runs of a row per
+// thread and permute the units inside each row so that their stores do not
+// collide in shared-memory banks; the merge reads through the same map.
+template <int MT, bool FP8>
+__device__ __forceinline__ int park_unit(int row, int u) {
+    if constexpr (!FP8) return u;
+    else if constexpr (MT == 0) return u ^ ((row >> 1) & 3);
+    else return u ^ ((2 * (u >> 3) + (row & 1)) & 7);
 }
 
 // Key chunk range of unit (request b, row block rb): chunk c covers positions
@@ -269,14 +285,16 @@ struct SegmentWalker {
 };
 
 // ROPE: the fused append's rotary embedding (its code is compiled only into
-// the kernels that need it).
-template <int HD, int MT, bool ROPE>
-__global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
+// the kernels that need it).  FP8: an E4M3 cache (vibevoice.c, "KV cache"),
+// read as stored: scores from f16 q and f16 keys (the E4M3 -> f16 conversion
+// is exact), P V from f16 weights and values, fp32 accumulation.
+template <int HD, int MT, bool ROPE, bool FP8>
+__global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_k64,
                         const __grid_constant__ CUtensorMap tm_v64, const Params p) {
-    using G = Geo<HD, MT>;
+    using G = Geo<HD, MT, FP8>;
     constexpr int RB = G::RB;
     constexpr int kStages = G::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -397,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
         const int c = lane & (kWarps - 1);
-        const bool fused = p.k_new != nullptr;
+        const bool fused = !FP8 && p.k_new != nullptr;
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
         SegmentWalker walk{g0, g1, L};
         Segment sg;
@@ -528,18 +546,19 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     if (lane == gc) gmask = valid;
                     // a new key comes from the step's rows; a masked row reads
                     // slot 0 (any valid slot will do)
-                    const __nv_bfloat16 *src =
-                        is_new ? (tensor ? p.v_new : p.k_new) +
+                    const uint8_t *src =
+                        is_new ? reinterpret_cast<const uint8_t *>(
+                                     (tensor ? p.v_new : p.k_new) +
                                      ((int64_t)(sg.b * p.q_rows + (t - new_lo)) * p.n_kv_heads +
-                                      sg.kvh) * HD
-                               : (tensor ? p.v_cache : p.k_cache) + (s < 0 ? 0 : s) * row_elems +
-                                     (int64_t)sg.kvh * HD;
+                                      sg.kvh) * HD)
+                               : reinterpret_cast<const uint8_t *>(tensor ? p.v_cache : p.k_cache) +
+                                     ((s < 0 ? 0 : s) * row_elems + (int64_t)sg.kvh * HD) * G::kElem;
                     uint8_t *dst = tensor ? vst : kst;
 #pragma unroll 4
-                    for (int c16 = 0; c16 < HD / 8; ++c16)
-                        cp_async_16_hint(dst + chunk_base<HD>(false, gc) +
+                    for (int c16 = 0; c16 < HD * G::kElem / 16; ++c16)
+                        cp_async_16_hint(dst + chunk_base<G::kHalves>(false, gc) +
                                         piece_offset(half_stride(false), r, c16),
-                                    src + c16 * 8, kv_policy);
+                                    src + c16 * 16, kv_policy);
                     issued_cp = true;
                 }
                 if (lane == 0) info_whole[st] = whole_tile ? 1 : 0;
@@ -559,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                                          (int)slot00, sg.kvh * G::kHalves, &full[st], kv_policy);
                 } else if (lane < kWarps && slot0 >= -1) {
                     const int y = slot0 < 0 ? -kChunk : (int)slot0;
-                    const uint32_t off = chunk_base<HD>(false, lane);
+                    const uint32_t off = chunk_base<G::kHalves>(false, lane);
                     tma_load_3d_hint(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st],
                                      kv_policy);
                     tma_load_3d_hint(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st],
@@ -586,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
         for (int i = ctid; i < HD / 2; i += kWarps * 32) rope_if[i] = p.rope_inv_freq[i];
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
     }
-    if (p.k_new != nullptr) {
+    if (!FP8 && p.k_new != nullptr) {
         // fused append: the step's rows into their cache slots, for later
         // steps (this launch reads them from k_new / v_new); 16-byte pieces
         const int pieces = p.n_kv_heads * HD / 8;  // of one row of one tensor
@@ -652,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 const int piece = row / kRowsPerPiece;
                 const int tensor = piece / G::kHalves, h = piece - tensor * G::kHalves;
                 uint8_t *base = stages + st_last * G::kStageBytes + tensor * G::kTileBytes +
-                                chunk_base<HD>(wl, w) + h * half_stride(wl);
+                                chunk_base<G::kHalves>(wl, w) + h * half_stride(wl);
                 return reinterpret_cast<float *>(base + (row - piece * kRowsPerPiece) * HD * 4);
             }
         };
@@ -672,8 +691,17 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + qr * G::kQStride);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    qb[kk][0] = qrow[kk * 8 + tq];
-                    qb[kk][1] = qrow[kk * 8 + 4 + tq];
+                    if constexpr (FP8) {
+                        // k-step kk pairs with bytes 4 (kk % 4) .. + 3 of piece
+                        // tq + 4 (kk / 4) of a key row (see the score loop):
+                        // the same dims of q, as f16
+                        const int w = 8 * (tq + 4 * (kk >> 2)) + 2 * (kk & 3);
+                        qb[kk][0] = bf16x2_to_f16x2(qrow[w]);
+                        qb[kk][1] = bf16x2_to_f16x2(qrow[w + 1]);
+                    } else {
+                        qb[kk][0] = qrow[kk * 8 + tq];
+                        qb[kk][1] = qrow[kk * 8 + 4 + tq];
+                    }
                 }
                 if (rope) {  // word w of a row is pair w
                     const int qpos = posbuf[qi * RB + qr];
@@ -710,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const bool whole = info_whole[st] != 0;
                     const uint32_t hs = half_stride(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
                         // new keys of the step, gathered unrotated from k_new:
@@ -726,7 +754,30 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     }
                     const int m = lane >> 3;
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
-                    {
+                    if constexpr (FP8) {
+                        // A = K, keys gq and gq + 8: k-step kk takes word kk % 4 of
+                        // 16-byte piece tq + 4 (kk / 4) of each key row, its two
+                        // low codes as k = 2tq, 2tq + 1 and its two high codes as
+                        // k = 2tq + 8, 2tq + 9
+                        uint32_t kw[2][8];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 lo = ld_shared_v4(kbase + piece_offset(hs, gq + 8 * h, tq));
+                            const uint4 hi =
+                                ld_shared_v4(kbase + piece_offset(hs, gq + 8 * h, tq + 4));
+                            kw[h][0] = lo.x, kw[h][1] = lo.y, kw[h][2] = lo.z, kw[h][3] = lo.w;
+                            kw[h][4] = hi.x, kw[h][5] = hi.y, kw[h][6] = hi.z, kw[h][7] = hi.w;
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2(kw[0][kk]);
+                            a[1] = e4m3x2_to_f16x2(kw[1][kk]);
+                            a[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
+                            a[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+                            mma_f16_16816(sacc, a, qb[kk][0], qb[kk][1]);
+                        }
+                    } else {
                         const int key = (m & 1) * 8 + (lane & 7);
 #pragma unroll
                         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -772,6 +823,34 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                         o[n][2] *= alpha[0];
                         o[n][3] *= alpha[1];
                     }
+                    if constexpr (FP8) {
+                        // P^T in f16 (one rounding: 11 significant bits)
+                        const uint32_t bh0 = movmatrix_trans(pack_f16x2(sacc[0], sacc[1]));
+                        const uint32_t bh1 = movmatrix_trans(pack_f16x2(sacc[2], sacc[3]));
+                        // A = V^T: this thread supplies keys 2tq, 2tq+1 (k = 2tq,
+                        // 2tq+1) and 2tq+8, 2tq+9, all from 16-byte piece gq; rows
+                        // gq and gq + 8 of m-tile md are dims 16 gq + 2 md and + 1
+                        uint32_t vw[4][4];
+#pragma unroll
+                        for (int kr = 0; kr < 4; ++kr) {
+                            const uint4 v = ld_shared_v4(
+                                vbase + piece_offset(hs, 2 * tq + (kr & 1) + 8 * (kr >> 1), gq));
+                            vw[kr][0] = v.x, vw[kr][1] = v.y, vw[kr][2] = v.z, vw[kr][3] = v.w;
+                        }
+#pragma unroll
+                        for (int md = 0; md < HD / 16; ++md) {
+                            // bytes 2md, 2md+1 of the piece, interleaved key by key
+                            const uint32_t sel = (md & 1) ? 0x7362u : 0x5140u;
+                            const uint32_t x = __byte_perm(vw[0][md >> 1], vw[1][md >> 1], sel);
+                            const uint32_t y = __byte_perm(vw[2][md >> 1], vw[3][md >> 1], sel);
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2(x);
+                            a[1] = e4m3x2_to_f16x2(x >> 16);
+                            a[2] = e4m3x2_to_f16x2(y);
+                            a[3] = e4m3x2_to_f16x2(y >> 16);
+                            mma_f16_16816(o[md], a, bh0, bh1);
+                        }
+                    } else {
                     // P^T fragments: transpose the (key x row) blocks of keys 0-7 and 8-15
                     uint32_t h0, l0, h1, l1;
                     split_bf16x2(sacc[0], sacc[1], h0, l0);
@@ -789,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                             mma_bf16_16816(o[md], a, bl0, bl1);
                         }
                     }
+                    }
                 }
                 __syncwarp();
                 if (lane == 0 && it + 1 < n_tiles) mbar_arrive(&empty[st]);
@@ -804,14 +884,28 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
             }
             __syncwarp();  // the warp's reads of the last tile are done
             const bool wl = info_whole[st_last] != 0;
+            if constexpr (FP8) {
+                // rows 2tq + e hold dims 16 gq .. 16 gq + 15 here: 16-byte stores
 #pragma unroll
-            for (int md = 0; md < HD / 16; ++md)
+                for (int e = 0; e < 2; ++e) {
+                    const int row = 2 * tq + e;
+                    float *dst = park(wl, warp, row);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = 2 * tq + (e & 1);
-                    const int d = md * 16 + gq + (e >> 1) * 8;
-                    park(wl, warp, row)[d] = o[md][e];
+                    for (int qd = 0; qd < 4; ++qd)
+                        *reinterpret_cast<float4 *>(dst + 4 * park_unit<MT, FP8>(row, 4 * gq + qd)) =
+                            make_float4(o[2 * qd][e], o[2 * qd][e + 2], o[2 * qd + 1][e],
+                                        o[2 * qd + 1][e + 2]);
                 }
+            } else {
+#pragma unroll
+                for (int md = 0; md < HD / 16; ++md)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = 2 * tq + (e & 1);
+                        const int d = md * 16 + gq + (e >> 1) * 8;
+                        park(wl, warp, row)[d] = o[md][e];
+                    }
+            }
             if (gq == 0) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -840,8 +934,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qs + rc * G::kQStride);
     #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        qa[mt][kk][hr] = qrow[kk * 8 + tq];
-                        qa[mt][kk][2 + hr] = qrow[kk * 8 + 4 + tq];
+                        if constexpr (FP8) {  // the score loop's dim order, as f16
+                            const int w = 8 * (tq + 4 * (kk >> 2)) + 2 * (kk & 3);
+                            qa[mt][kk][hr] = bf16x2_to_f16x2(qrow[w]);
+                            qa[mt][kk][2 + hr] = bf16x2_to_f16x2(qrow[w + 1]);
+                        } else {
+                            qa[mt][kk][hr] = qrow[kk * 8 + tq];
+                            qa[mt][kk][2 + hr] = qrow[kk * 8 + 4 + tq];
+                        }
                     }
                     if (rope) {  // word w of a row is pair w
     #pragma unroll
@@ -878,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                     const bool whole = info_whole[st] != 0;
                     const uint32_t hs = half_stride(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes) + chunk_base<HD>(whole, warp);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, warp);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
                         // new keys of the step, gathered unrotated from k_new:
@@ -898,7 +998,31 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
     #pragma unroll
                         for (int j = 0; j < 2; ++j)
                             s[mt][j][0] = s[mt][j][1] = s[mt][j][2] = s[mt][j][3] = 0.f;
-                    {
+                    if constexpr (FP8) {
+                        // B = K^T, keys gq (n-tile 0) and gq + 8 (n-tile 1), read
+                        // as in the MT = 0 score loop
+                        uint32_t kw[2][8];
+    #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 lo = ld_shared_v4(kbase + piece_offset(hs, gq + 8 * h, tq));
+                            const uint4 hi =
+                                ld_shared_v4(kbase + piece_offset(hs, gq + 8 * h, tq + 4));
+                            kw[h][0] = lo.x, kw[h][1] = lo.y, kw[h][2] = lo.z, kw[h][3] = lo.w;
+                            kw[h][4] = hi.x, kw[h][5] = hi.y, kw[h][6] = hi.z, kw[h][7] = hi.w;
+                        }
+    #pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            const uint32_t b00 = e4m3x2_to_f16x2(kw[0][kk]);
+                            const uint32_t b01 = e4m3x2_to_f16x2(kw[0][kk] >> 16);
+                            const uint32_t b10 = e4m3x2_to_f16x2(kw[1][kk]);
+                            const uint32_t b11 = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+    #pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_f16_16816(s[mt][0], qa[mt][kk], b00, b01);
+                                mma_f16_16816(s[mt][1], qa[mt][kk], b10, b11);
+                            }
+                        }
+                    } else {
                         const int m = lane >> 3;
                         const int key = (m >> 1) * 8 + (lane & 7);
     #pragma unroll
@@ -956,12 +1080,43 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                                 o[mt][n][hr * 2 + 1] *= alpha;
                             }
                         }
-                        split_bf16x2(s[mt][0][0], s[mt][0][1], pa[mt][0], pl[mt][0]);
-                        split_bf16x2(s[mt][0][2], s[mt][0][3], pa[mt][1], pl[mt][1]);
-                        split_bf16x2(s[mt][1][0], s[mt][1][1], pa[mt][2], pl[mt][2]);
-                        split_bf16x2(s[mt][1][2], s[mt][1][3], pa[mt][3], pl[mt][3]);
+                        if constexpr (FP8) {  // P in f16, one rounding
+                            pa[mt][0] = pack_f16x2(s[mt][0][0], s[mt][0][1]);
+                            pa[mt][1] = pack_f16x2(s[mt][0][2], s[mt][0][3]);
+                            pa[mt][2] = pack_f16x2(s[mt][1][0], s[mt][1][1]);
+                            pa[mt][3] = pack_f16x2(s[mt][1][2], s[mt][1][3]);
+                        } else {
+                            split_bf16x2(s[mt][0][0], s[mt][0][1], pa[mt][0], pl[mt][0]);
+                            split_bf16x2(s[mt][0][2], s[mt][0][3], pa[mt][1], pl[mt][1]);
+                            split_bf16x2(s[mt][1][0], s[mt][1][1], pa[mt][2], pl[mt][2]);
+                            split_bf16x2(s[mt][1][2], s[mt][1][3], pa[mt][3], pl[mt][3]);
+                        }
                     }
-                    {
+                    if constexpr (FP8) {
+                        // B = V: this thread supplies keys 2tq, 2tq+1, 2tq+8, 2tq+9
+                        // of column n = gq; n-tile j's column gq is dim 16 gq + j,
+                        // byte j of 16-byte piece gq
+                        uint32_t vw[4][4];
+    #pragma unroll
+                        for (int kr = 0; kr < 4; ++kr) {
+                            const uint4 v = ld_shared_v4(
+                                vbase + piece_offset(hs, 2 * tq + (kr & 1) + 8 * (kr >> 1), gq));
+                            vw[kr][0] = v.x, vw[kr][1] = v.y, vw[kr][2] = v.z, vw[kr][3] = v.w;
+                        }
+    #pragma unroll
+                        for (int jj = 0; jj < HD / 16; ++jj) {  // n-tiles 2jj, 2jj + 1
+                            const uint32_t sel = (jj & 1) ? 0x7362u : 0x5140u;
+                            const uint32_t x = __byte_perm(vw[0][jj >> 1], vw[1][jj >> 1], sel);
+                            const uint32_t y = __byte_perm(vw[2][jj >> 1], vw[3][jj >> 1], sel);
+                            const uint32_t x0 = e4m3x2_to_f16x2(x), x1 = e4m3x2_to_f16x2(x >> 16);
+                            const uint32_t y0 = e4m3x2_to_f16x2(y), y1 = e4m3x2_to_f16x2(y >> 16);
+    #pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_f16_16816(o[mt][2 * jj], pa[mt], x0, y0);
+                                mma_f16_16816(o[mt][2 * jj + 1], pa[mt], x1, y1);
+                            }
+                        }
+                    } else {
                         const int m = lane >> 3;
                         const int key = (m & 1) * 8 + (lane & 7);
     #pragma unroll
@@ -1000,10 +1155,27 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 for (int hr = 0; hr < 2; ++hr) {
                     const int row = mt * 16 + gq + hr * 8;
                     float *dst = park(wl, warp, row);
+                    if constexpr (FP8) {
+                        // columns 2tq, 2tq + 1 of n-tile j are dims 32 tq + j and
+                        // 32 tq + 16 + j: this thread holds dims 32 tq .. 32 tq + 31
     #pragma unroll
-                    for (int n = 0; n < HD / 8; ++n)
-                        *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
-                            make_float2(o[mt][n][hr * 2], o[mt][n][hr * 2 + 1]);
+                        for (int qd = 0; qd < 4; ++qd) {
+                            *reinterpret_cast<float4 *>(
+                                dst + 4 * park_unit<MT, FP8>(row, 8 * tq + qd)) =
+                                make_float4(o[mt][4 * qd][hr * 2], o[mt][4 * qd + 1][hr * 2],
+                                            o[mt][4 * qd + 2][hr * 2], o[mt][4 * qd + 3][hr * 2]);
+                            *reinterpret_cast<float4 *>(
+                                dst + 4 * park_unit<MT, FP8>(row, 8 * tq + 4 + qd)) =
+                                make_float4(o[mt][4 * qd][hr * 2 + 1], o[mt][4 * qd + 1][hr * 2 + 1],
+                                            o[mt][4 * qd + 2][hr * 2 + 1],
+                                            o[mt][4 * qd + 3][hr * 2 + 1]);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int n = 0; n < HD / 8; ++n)
+                            *reinterpret_cast<float2 *>(dst + n * 8 + tq * 2) =
+                                make_float2(o[mt][n][hr * 2], o[mt][n][hr * 2 + 1]);
+                    }
                     if (tq == 0) {
                         mm[warp * RB + row] = m_run[mt][hr];
                         ml[warp * RB + row] = l_run[mt][hr];
@@ -1044,7 +1216,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT>::kCtasPerSm)
                 float4 v[kWarps];
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w)
-                    v[w] = *reinterpret_cast<const float4 *>(park(wl, w, row) + d);
+                    v[w] = *reinterpret_cast<const float4 *>(park(wl, w, row) +
+                                                             4 * park_unit<MT, FP8>(row, d >> 2));
                 const float ww[4] = {wt.x, wt.y, wt.z, wt.w};
                 acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -1278,14 +1451,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     }
 }
 
-template <int HD, int MT, bool ROPE>
+template <int HD, int MT, bool ROPE, bool FP8>
 int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
                  const CUtensorMap &tk64, const CUtensorMap &tv64, bool merge,
                  cudaStream_t stream) {
-    using G = Geo<HD, MT>;
+    using G = Geo<HD, MT, FP8>;
     static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
                   "shared memory budget");
-    auto kern = decode_split_kernel<HD, MT, ROPE>;
+    auto kern = decode_split_kernel<HD, MT, ROPE, FP8>;
     const size_t smem = G::kSmem;
     static int configured_device = -1;
     int dev = 0;
@@ -1352,19 +1525,22 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
                   const float *rope_inv_freq, bool tables_early) {
-    // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][64]
-    // (a half is 64 columns, 128 bytes, of one head's row): a box of
-    // {64, rows, halves} brings both halves of `rows` slots of one head.
-    const int halves = plan.head_dim / 64;
-    const uint64_t dims[3] = {64, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
-    const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * 2, 128};
-    const uint32_t box[3] = {64, (uint32_t)dec::kChunk, (uint32_t)halves};
-    const uint32_t box64[3] = {64, (uint32_t)dec::kTileRows, (uint32_t)halves};
+    // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][cols]
+    // (a half is 128 bytes of one head's row: 64 bf16 or 128 E4M3 columns): a
+    // box of {cols, rows, halves} brings the whole head row of `rows` slots.
+    const bool fp8 = cache->dtype == ATTN_KV_FP8_E4M3;
+    const int esize = fp8 ? 1 : 2;
+    const int halves = plan.head_dim * esize / 128;
+    const uint32_t cols = 128 / esize;
+    const uint64_t dims[3] = {cols, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
+    const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * esize, 128};
+    const uint32_t box[3] = {cols, (uint32_t)dec::kChunk, (uint32_t)halves};
+    const uint32_t box64[3] = {cols, (uint32_t)dec::kTileRows, (uint32_t)halves};
     CUtensorMap tk, tv, tk64, tv64;
-    if (!encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true) ||
-        !encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true) ||
-        !encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true) ||
-        !encode_tensor_map(&tv64, cache->v, 3, dims, strides, box64, true)) {
+    if (!encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true, fp8) ||
+        !encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true, fp8) ||
+        !encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true, fp8) ||
+        !encode_tensor_map(&tv64, cache->v, 3, dims, strides, box64, true, fp8)) {
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
@@ -1417,10 +1593,16 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                                               plan.meta_offset);
         int rc;
         const bool r = rope_inv_freq != nullptr;
-#define GQA_SPLIT(D, M)                                                                     \
-    (r ? dec::launch_split<D, M, true>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)    \
-       : dec::launch_split<D, M, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream))
-        if (plan.head_dim == 128)
+#define GQA_SPLIT(D, M)                                                                         \
+    (r ? dec::launch_split<D, M, true, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream) \
+       : dec::launch_split<D, M, false, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream))
+#define GQA_SPLIT_FP8(M) \
+    dec::launch_split<128, M, false, true>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+        if (fp8)  // head_dim 128, no fused append (refused before the launch)
+            rc = plan.m_tiles == 0 ? GQA_SPLIT_FP8(0)
+                 : plan.m_tiles == 1 ? GQA_SPLIT_FP8(1)
+                                     : GQA_SPLIT_FP8(2);
+        else if (plan.head_dim == 128)
             rc = plan.m_tiles == 0 ? GQA_SPLIT(128, 0)
                  : plan.m_tiles == 1 ? GQA_SPLIT(128, 1)
                                      : GQA_SPLIT(128, 2);
@@ -1429,6 +1611,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                  : plan.m_tiles == 1 ? GQA_SPLIT(64, 1)
                                      : GQA_SPLIT(64, 2);
 #undef GQA_SPLIT
+#undef GQA_SPLIT_FP8
         if (rc != ATTN_OK) return rc;
     }
     return ATTN_OK;

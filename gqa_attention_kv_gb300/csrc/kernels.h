@@ -36,13 +36,25 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return e;
 }
 
-// Encode a 2D/3D bf16 tensor map with 128-byte swizzle (returns false on failure).
+// Encode a 2D/3D tensor map of bf16 (or, with bytes, 8-bit) elements, with
+// 128-byte swizzle (returns false on failure).
 bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
+                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128,
+                       bool bytes = false);
 
 int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
                      void *k_cache, void *v_cache, int64_t num_slots, int row_bytes,
                      int32_t *err, cudaStream_t stream);
+
+// FP8 cache append: row_elems = n_kv_heads * head_dim (a multiple of 16);
+// k_ref float32 [row_elems] or nullptr.
+int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_ref,
+                         const int64_t *slot_mapping, int64_t n, void *k_cache, void *v_cache,
+                         int64_t num_slots, int row_elems, int32_t *err, cudaStream_t stream);
+
+// ref[e] = mean over n rows of the bf16 matrix k[n][row_elems], as float32.
+int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,
+                        cudaStream_t stream);
 
 // Decode plan: a persistent grid of one CTA per SM; requests are processed
 // in launches of at most batch_per_launch (the per-request tables live in

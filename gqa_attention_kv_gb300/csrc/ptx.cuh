@@ -233,6 +233,54 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Two fp32 values -> f16x2 (lo in the low half), each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// bf16x2 -> f16x2, each value rounded to the nearest f16.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ------------------------------------------------------------ 8-bit E4M3 floats
+// The low 16 bits of `two` hold two E4M3 codes; the result holds their values
+// as f16x2, the low byte's in the low half.  Exact (every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t d;
+    const unsigned short a = (unsigned short)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(a));
+    return d;
+}
+
+// E4M3 codes of lo (low byte) and hi: round to nearest even, saturating to
+// +-448; NaN stays NaN.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // Transpose an 8x8 matrix of 16-bit values held in the mma fragment layout
 // (thread t: row t/4, columns 2(t%4) and 2(t%4)+1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {

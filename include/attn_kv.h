@@ -76,10 +76,16 @@ typedef enum {
     ATTN_CACHE_RING = 2    /* -> slot b*slots_per_seq + t % slots_per_seq (ring of that size) */
 } attn_cache_kind;
 
+typedef enum {
+    ATTN_KV_BF16 = 0,    /* 16-bit bf16 elements */
+    ATTN_KV_FP8_E4M3 = 1 /* 8-bit E4M3 elements, K stored relative to k_ref */
+} attn_kv_dtype;
+
 /*
- * One layer's KV cache.  k and v are [num_slots, n_kv_heads, head_dim] bf16
- * (the pages' [B, S, H, D] layout with requests and positions flattened into
- * slots).  The struct itself is read on the host during the call only.
+ * One layer's KV cache.  k and v are [num_slots, n_kv_heads, head_dim]
+ * elements of the cache's dtype (the pages' [B, S, H, D] layout with requests
+ * and positions flattened into slots).  The struct itself is read on the host
+ * during the call only.
  *
  *   LINEAR: slots_per_seq = capacity of each request's window.
  *   PAGED : block_table is a DEVICE int32 [batch, max_blocks_per_seq] array of
@@ -88,16 +94,31 @@ typedef enum {
  *           calls (a captured graph follows it).
  *   RING  : slots_per_seq = ring size R; position t of request b lives in slot
  *           b*R + t % R.  A ring holds the last R positions written.
+ *
+ * dtype ATTN_KV_FP8_E4M3 (vibevoice.c, "KV cache": the cache stored as 8-bit
+ * floats to halve its size, K relative to a per-layer reference vector): each
+ * element is one byte in the E4M3 format of the OCP 8-bit floating point
+ * specification (bias 7, no infinities, 0x7F / 0xFF NaN, largest finite 448),
+ * with no scale factor.  attn_kv_append stores
+ *     k_cache = E4M3(float32(k) - k_ref[head][d]),  v_cache = E4M3(float32(v)),
+ * rounding to nearest even and saturating to +-448; k_ref (float32
+ * [n_kv_heads][head_dim], device; NULL: no shift) is usually the mean of the
+ * first prefill chunk's keys (attn_kv_reference).  Subtracting one vector from
+ * every key of a head adds the same amount to all of a query row's scores, so
+ * attention reads the stored keys as they are and needs no k_ref.  FP8 caches
+ * require head_dim 128.  A zero-initialised struct is a bf16 cache.
  */
 typedef struct {
     int32_t kind;               /* attn_cache_kind */
-    void *k;                    /* bf16 [num_slots, n_kv_heads, head_dim] */
-    void *v;                    /* bf16 [num_slots, n_kv_heads, head_dim] */
+    void *k;                    /* [num_slots, n_kv_heads, head_dim] of dtype */
+    void *v;                    /* [num_slots, n_kv_heads, head_dim] of dtype */
     int64_t num_slots;
     int32_t slots_per_seq;      /* LINEAR capacity, RING size; unused for PAGED */
     const int32_t *block_table; /* PAGED only, device */
     int32_t block_size;         /* PAGED only */
     int32_t max_blocks_per_seq; /* PAGED only: row length of block_table */
+    int32_t dtype;              /* attn_kv_dtype */
+    const float *k_ref;         /* FP8 only: float32 [n_kv_heads, head_dim], device, or NULL */
 } attn_kv_cache;
 
 /*
@@ -115,11 +136,26 @@ typedef struct {
  *                 its row and stores ATTN_ERR_BOUNDS in *err_word
  *   n             rows to write (0 is a no-op)
  * Copies are bit-exact.  With a slot repeated inside one call, which row lands
- * is unspecified.  Does not read cache->kind: slots are absolute.
+ * is unspecified.  Does not read cache->kind: slots are absolute.  For an FP8
+ * cache the rows are converted as attn_kv_cache states (bit-exact against
+ * that definition), and k_new / v_new stay bf16.
  */
 int attn_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
                    const attn_kv_cache *cache, int n_kv_heads, int head_dim, int32_t *err_word,
                    attn_stream_t stream);
+
+/*
+ * attn_kv_reference -- the FP8 cache's reference vector: ref[h][d] = mean over
+ * the n rows of k[i][h][d] (vibevoice.c, "KV cache": a per-layer reference
+ * built from the first prefill chunk).
+ *
+ *   k     bf16 [n, n_kv_heads, head_dim], device, 16-byte aligned; n >= 1
+ *   ref   float32 [n_kv_heads, head_dim], device, written: the sum is taken in
+ *         fp64 in a fixed order and divided by n, then rounded once to
+ *         float32, so the result does not depend on timing.
+ */
+int attn_kv_reference(const void *k, int64_t n, int n_kv_heads, int head_dim, float *ref,
+                      attn_stream_t stream);
 
 /*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
@@ -172,6 +208,10 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  *              bytes, 16-byte aligned, zero-filled before its first use (see
  *              attn_decode_workspace_size).  Calls whose kernels overlap on
  *              the GPU need separate workspaces.
+ *   An FP8 cache (head_dim 128) is read as stored: the decode converts keys
+ *   and values to f16 (exact), takes q in f16 (|q| must stay below 65504;
+ *   magnitudes under 2^-14 lose precision) and the softmax weights in f16,
+ *   and accumulates in fp32.
  */
 int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
                 const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
@@ -214,6 +254,8 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *                  under programmatic dependent launch.  Everything else is
  *                  still read after it completes.
  *   Every other argument, the workspace and the statuses are attn_decode's.
+ *   An FP8 cache returns ATTN_ERR_UNSUPPORTED: append with attn_kv_append,
+ *   then call attn_decode.
  */
 #define ATTN_DECODE_TABLES_EARLY 1u
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,

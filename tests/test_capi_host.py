@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("attn_kv_append", "attn_decode", "attn_decode_workspace_size", "attn_prefill",
-                 "attn_decode_append", "attn_status_string", "attn_version"):
+                 "attn_decode_append", "attn_kv_reference", "attn_status_string",
+                 "attn_version"):
         assert want in names, names
 
 
@@ -65,9 +66,11 @@ class FakeTensor:
         return 1
 
 
-def cache(kind=gq.LINEAR, Hkv=8, D=128, slots=1024, sps=512, bt=None, bs=0, k=4096, v=8192):
+def cache(kind=gq.LINEAR, Hkv=8, D=128, slots=1024, sps=512, bt=None, bs=0, k=4096, v=8192,
+          dtype=gq.ATTN_KV_BF16, k_ref=None):
     return gq.KVCache(kind, FakeTensor(k, (slots, Hkv, D)), FakeTensor(v, (slots, Hkv, D)),
-                      slots_per_seq=sps, block_table=bt, block_size=bs)
+                      slots_per_seq=sps, block_table=bt, block_size=bs, dtype=dtype,
+                      k_ref=k_ref)
 
 
 def decode_rc(lib, c, B=2, R=1, Hq=32, Hkv=8, D=128, L=512, W=0, q=16, out=32, ws=None,
@@ -163,3 +166,34 @@ def test_decode_append_validation(lib):
     assert f(*args(hq=30)) == gq.ATTN_ERR_SHAPE
     assert f(*args(scale=0.0)) == gq.ATTN_ERR_SHAPE
     assert f(*args(flags=2)) == gq.ATTN_ERR_UNSUPPORTED
+
+
+def test_fp8_cache_validation(lib):
+    """FP8 caches: head_dim 128 only, no fused append yet, an aligned k_ref;
+    an unknown dtype is refused."""
+    fp8 = gq.ATTN_KV_FP8_E4M3
+    assert decode_rc(lib, cache(dtype=fp8, D=64), D=64) == gq.ATTN_ERR_UNSUPPORTED
+    assert decode_rc(lib, cache(dtype=7)) == gq.ATTN_ERR_UNSUPPORTED
+    assert decode_rc(lib, cache(dtype=fp8), B=0) == gq.ATTN_OK
+    c = cache(dtype=fp8)
+    cs = c.struct()
+    assert lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 512, 0) > 0
+    f = lib.attn_kv_append
+    ref_bad = FakeTensor(4100, (8, 128))
+    cs = cache(dtype=fp8, k_ref=ref_bad).struct()
+    assert f(16, 32, 48, 4, ctypes.byref(cs), 8, 128, None, None) == gq.ATTN_ERR_ALIGN
+    cs = cache(dtype=fp8, D=64).struct()
+    assert f(16, 32, 48, 4, ctypes.byref(cs), 8, 64, None, None) == gq.ATTN_ERR_UNSUPPORTED
+    cs = cache(dtype=fp8, slots=4096 * 4, sps=4096).struct()
+    need = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 4096, 0)
+    assert lib.attn_decode_append(16, 32, 48, 64, None, ctypes.byref(cs), 80, 96, 2, 1, 4096,
+                                  0, 32, 8, 128, 0.1, 112, 1 << 20, need, None, 0,
+                                  None) == gq.ATTN_ERR_UNSUPPORTED
+
+
+def test_kv_reference_validation(lib):
+    f = lib.attn_kv_reference
+    assert f(16, 0, 8, 128, 32, None) == gq.ATTN_ERR_SHAPE
+    assert f(None, 4, 8, 128, 32, None) == gq.ATTN_ERR_NULL
+    assert f(16, 4, 8, 128, None, None) == gq.ATTN_ERR_NULL
+    assert f(18, 4, 8, 128, 32, None) == gq.ATTN_ERR_ALIGN
