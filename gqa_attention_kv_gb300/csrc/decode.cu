@@ -754,6 +754,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                     }
                     const int m = lane >> 3;
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f};  // (key gq | gq+8) x (row 2tq | 2tq+1)
+                    // odd k-steps accumulate apart: two chains of dependent mma
+                    // instead of one, added at the end
+                    float sodd[4] = {0.f, 0.f, 0.f, 0.f};
                     if constexpr (FP8) {
                         // A = K, keys gq and gq + 8: k-step kk takes word kk % 4 of
                         // 16-byte piece tq + 4 (kk / 4) of each key row, its two
@@ -775,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                             a[1] = e4m3x2_to_f16x2(kw[1][kk]);
                             a[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
                             a[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
-                            mma_f16_16816(sacc, a, qb[kk][0], qb[kk][1]);
+                            mma_f16_16816((kk & 1) ? sodd : sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     } else {
                         const int key = (m & 1) * 8 + (lane & 7);
@@ -784,9 +787,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                             uint32_t a[4];
                             ldmatrix_x4(a[0], a[1], a[2], a[3],
                                         kbase + piece_offset(hs, key, kk * 2 + (m >> 1)));
-                            mma_bf16_16816(sacc, a, qb[kk][0], qb[kk][1]);
+                            mma_bf16_16816((kk & 1) ? sodd : sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
                     float alpha[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {  // row 2tq + e: elements e (key gq), e+2 (key gq+8)
