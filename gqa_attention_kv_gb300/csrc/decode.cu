@@ -61,6 +61,7 @@ constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per
 // much less real work.
 constexpr int kUnitGapChunks = 12;
 constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
+constexpr int kPrefetchTiles = 4;            // tiles of a share fetched into L2 before the PDL wait
 constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
 
 struct Params {
@@ -380,12 +381,41 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         }
     }
     __syncthreads();
-    if (p.tables_early) pdl_wait();
-    pdl_launch_dependents();
     const int N = tb.Pb[B];
     // equal shares, but at least kMinChunksPerCta so small problems do not
     // spread a few keys over every SM
     const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
+    const int g0 = min(N, (int)blockIdx.x * L), g1 = min(N, g0 + L);
+    if (p.tables_early) {
+        // The share is known before the previous kernel has finished: start
+        // the DRAM reads of its first tiles into L2 now (whole 64-slot tiles
+        // of linear and ring caches; pages would need block-table reads
+        // first, which cost more than they hide), so the wait below overlaps
+        // their latency.  A prefetch writes nothing; a line the previous
+        // kernel rewrites is refetched.
+        if (warp == kProducerWarp && lane == 0 && p.kind != ATTN_CACHE_PAGED) {
+            SegmentWalker walk{g0, g1, L};
+            Segment sg;
+            int issued = 0;
+            while (issued < kPrefetchTiles && walk.next(p, tb, sg)) {
+                const int bg = p.b_base + sg.b;
+                for (int c = sg.c_begin; c < sg.c_end && issued < kPrefetchTiles;
+                     c += kWarps, ++issued) {
+                    const int z = sg.kvh * G::kHalves;
+                    int j = c * kChunk;  // first position of the tile
+                    if (p.kind == ATTN_CACHE_RING) {
+                        j %= p.slots_per_seq;
+                        if (j + kTileRows > p.slots_per_seq) continue;  // wraps: gathered later
+                    }
+                    const int y = (int)((int64_t)bg * p.slots_per_seq + j);
+                    tma_prefetch_3d(&tm_k64, 0, y, z);
+                    tma_prefetch_3d(&tm_v64, 0, y, z);
+                }
+            }
+        }
+        pdl_wait();
+    }
+    pdl_launch_dependents();
     if (blockIdx.x == 0) {
         // units with no valid key get zeros (no CTA visits them)
         for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
@@ -403,7 +433,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
             }
         }
     }
-    const int g0 = min(N, (int)blockIdx.x * L), g1 = min(N, g0 + L);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
