@@ -81,7 +81,7 @@ def prefill_traffic(T):
 
 def merge_kernel_launched(max_seq_len, window, q_rows, ring):
     """1 if a decode call also launches the merge kernel: the library's rule
-    (a unit may span more than 8 CTAs of at least 8 chunks of 16 keys)."""
+    (a unit may span more than 128 CTAs of at least 8 chunks of 16 keys)."""
     keys = max_seq_len
     if window > 0:
         keys = min(keys, window + q_rows - 1)
@@ -89,7 +89,7 @@ def merge_kernel_launched(max_seq_len, window, q_rows, ring):
         keys = min(keys, ring)
     max_chunks = (keys + 15) // 16 + 1
     max_parts = (max_chunks + 7) // 8 + 1
-    return 1 if max_parts > 8 else 0
+    return 1 if max_parts > 128 else 0
 
 
 def prefill_flops(T, Hq, D, window=0):
@@ -251,6 +251,8 @@ class QwenWorkload(Workload):
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
+        # prefill, prompt append, per decode the split kernel (+ the merge
+        # kernel at these long contexts)
         self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * (
             1 + merge_kernel_launched(self.max_seq, 0, 1, None))
         self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",

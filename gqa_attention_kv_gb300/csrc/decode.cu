@@ -19,9 +19,10 @@
 //     included), and each CTA streams its share through one deep TMA ring,
 //     paying the pipeline ramp once.  A CTA's share covers pieces ("segments")
 //     of one or more units; a unit wholly inside one CTA is written straight
-//     to the output; the others leave fp32 partial states in the workspace,
-//     and the CTA that stores a unit's last partial (a per-unit counter tells
-//     it) merges them in CTA order and resets the counter.  One launch.
+//     to the output; the others leave fp32 partial states in the workspace
+//     and are merged by the CTAs that store the last ones (atomic counters
+//     tell them): parts in CTA order, eight at a time, then those groups'
+//     states in order.  One launch.
 //   * A producer warp streams 64-key tiles (four 16-key chunks).  A tile
 //     whose 64 slots are consecutive (linear cache; a ring away from its wrap
 //     point) is one TMA box of 64 rows per tensor; otherwise a chunk whose 16
@@ -60,9 +61,14 @@ constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per
 // unit is followed by this many chunks of nothing, so such a CTA gets that
 // much less real work.
 constexpr int kUnitGapChunks = 12;
-constexpr int kFusedMaxParts = 8;            // units spanning more CTAs use the merge kernel
+constexpr int kGroupParts = 8;               // partial states merged by one CTA at a time
+constexpr int kMergeWarps = 4;  // merge kernel CTA: small enough to be resident beside the split kernel
+// A launch whose units may span more CTAs than this (by the host's bound)
+// leaves units of more than kGroupParts parts to the merge kernel: there one
+// CTA per query row merges all parts with every load in flight, which beats
+// two levels of counters and L2 round trips inside the split kernel.
+constexpr int kMergeKernelParts = 128;
 constexpr int kPrefetchTiles = 4;            // tiles of a share fetched into L2 before the PDL wait
-constexpr int kMergeWarps = 4;  // small enough to be resident beside the split kernel
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -87,7 +93,10 @@ struct Params {
     __nv_bfloat16 *out;
     float *ws_o;
     float *ws_lse;
-    int32_t *ws_count;  // per unit: partial states written so far (zero between calls)
+    int32_t *ws_count;   // per unit: merged groups so far (zero between calls)
+    int32_t *ws_gcount;  // per partial slot that starts a group: parts stored so far
+    int2 *ws_parts;      // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
+    bool merge_kernel;   // units of more than kGroupParts parts go to the merge kernel
     // fused append (nullptr: none): the step's rows, bf16 [batch * q_rows][n_kv_heads][HD],
     // row b * q_rows + r being the key at position seq_len_b - q_rows + r, and their slots
     const __nv_bfloat16 *k_new;
@@ -97,7 +106,6 @@ struct Params {
     // seq_lens, positions and block_table may be read before the previous
     // kernel completes (ATTN_DECODE_TABLES_EARLY)
     bool tables_early;
-    int2 *ws_parts;     // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     int32_t *err;
 };
 
@@ -284,6 +292,74 @@ struct SegmentWalker {
         return false;
     }
 };
+
+// Merge `parts` fp32 partial states of unit u's rows, stored at workspace
+// slots s0, s0 + stride, ... (in that order, the order that fixes the
+// result), either into the bf16 output (final) or, as one partial state, back
+// into slot s0.  Partial states hold O / l and the base-2 log-sum-exp.  Run by
+// the four consumer warps; sl: shared staging of parts x RB floats.
+template <int HD, int RB>
+__device__ __forceinline__ void merge_partials(const Params &p, const Segment &u, int64_t s0,
+                                               int stride, int parts, bool final, float *sl,
+                                               int ctid) {
+    const int row0 = u.rb * RB, row1 = min(p.rows, row0 + RB);
+    for (int i = ctid; i < parts * RB; i += kWarps * 32) {
+        const int c = i / RB, row = i - (i / RB) * RB;
+        sl[i] = __ldcg(p.ws_lse + (s0 + (int64_t)c * stride) * RB + row);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
+        const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+        const int i = row0 + row;
+        if (i >= row1) continue;
+        float M = -INFINITY;
+        for (int c = 0; c < parts; ++c) M = fmaxf(M, sl[c * RB + row]);
+        float Lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            // kGroupParts loads in flight at a time
+            for (int c0 = 0; c0 < parts; c0 += kGroupParts) {
+                float f[kGroupParts];
+                float4 v[kGroupParts];
+#pragma unroll
+                for (int k = 0; k < kGroupParts; ++k) {
+                    const int c = c0 + k;
+                    f[k] = 0.f;
+                    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c < parts) {
+                        f[k] = fast_exp2(sl[c * RB + row] - M);  // -inf gives 0
+                        v[k] = __ldcg(reinterpret_cast<const float4 *>(
+                            p.ws_o + ((s0 + (int64_t)c * stride) * RB + row) * HD + d));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kGroupParts; ++k) {
+                    Lsum += f[k];
+                    acc.x += f[k] * v[k].x;
+                    acc.y += f[k] * v[k].y;
+                    acc.z += f[k] * v[k].z;
+                    acc.w += f[k] * v[k].w;
+                }
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        if (final) {
+            const int r = i / p.group, g = i - (i / p.group) * p.group;
+            __nv_bfloat16 *dst =
+                p.out + (((int64_t)u.b * p.q_rows + r) * p.n_q_heads + u.kvh * p.group + g) * HD + d;
+            uint2 packed;
+            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(dst) = packed;
+        } else {
+            // this thread read (row, d) of slot s0 itself: the overwrite is safe
+            *reinterpret_cast<float4 *>(p.ws_o + (s0 * RB + row) * HD + d) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (d == 0) p.ws_lse[s0 * RB + row] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // staging free again
+}
 
 // ROPE: the fused append's rotary embedding (its code is compiled only into
 // the kernels that need it).  FP8: an E4M3 cache (vibevoice.c, "KV cache"),
@@ -1287,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // parked rows read
         if (lane == 0) mbar_arrive(&empty[st_last]);
-        if (!sg.whole && sg.last - sg.first < kFusedMaxParts) {
+        if (!sg.whole && (!p.merge_kernel || sg.last - sg.first < kGroupParts)) {
             if (n_pend == 0)
                 pend0 = sg;
             else
@@ -1296,83 +1372,56 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         }
     }
     if (n_pend == 0) return;
-    // ---- end of share: a unit spanning a few CTAs is merged by the CTA that
-    // stores its last partial state (per-unit counter): parts in CTA order,
-    // one bf16 rounding.  The ring is drained, so the stages are free.
+    // ---- end of share: merges of units split over several CTAs.  Parts
+    // first..last of a unit form groups of kGroupParts consecutive CTAs; the
+    // CTA that stores a group's last part (counter at the group's first slot)
+    // merges the group, in CTA order, into that slot; the CTA that completes
+    // a unit's last group (per-unit counter) merges the groups in order into
+    // the bf16 output.  A unit of at most kGroupParts parts is one group
+    // merged straight to the output.  The ring is drained, so the stages
+    // are free for staging.
     __threadfence();
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-    if (ctid == 0) {
-        for (int k = 0; k < n_pend; ++k) {
-            const Segment &u = k == 0 ? pend0 : pend1;
-            const int first = u.first, last = u.last;
-            const int prev = atomicAdd(p.ws_count + u.unit, 1);
-            s_last[k] = (prev == last - first) ? 1 : 0;
-        }
-    }
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
     float *sl = reinterpret_cast<float *>(stages);  // [parts][RB] log-sum-exps
     for (int k = 0; k < n_pend; ++k) {
-        if (!s_last[k]) continue;  // uniform across the consumer warps
-        __threadfence();
         const Segment &u = k == 0 ? pend0 : pend1;
-        const int first = u.first, last = u.last;
-        const int parts = last - first + 1;  // <= kFusedMaxParts
-        const int row0 = u.rb * RB, row1 = min(p.rows, row0 + RB);
-        // 1) every part's log-sum-exp of every row into shared memory, 2) per
-        // row the max and the weights, 3) the weighted outputs, all loads of
-        // a row in flight at once.
-        for (int i = ctid; i < parts * RB; i += kWarps * 32) {
-            const int c = i / RB, row = i - (i / RB) * RB;
-            sl[i] = __ldcg(p.ws_lse + ((int64_t)u.unit + first + c) * RB + row);
+        const int n = u.last - u.first + 1;
+        const int gf = u.first + (((int)blockIdx.x - u.first) / kGroupParts) * kGroupParts;
+        const int gl = min(u.last, gf + kGroupParts - 1);
+        const int64_t gslot = (int64_t)u.unit + gf;
+        // one flag per (segment, level), each written once: a thread still
+        // reading one flag never sees the next decision
+        if (ctid == 0) {
+            int32_t *cnt = n <= kGroupParts ? p.ws_count + u.unit : p.ws_gcount + gslot;
+            s_last[2 * k] = atomicAdd(cnt, 1) == gl - gf ? 1 : 0;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-        for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
-            const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
-            const int i = row0 + row;
-            if (i >= row1) continue;
-            float lse[kFusedMaxParts];
-            float4 v[kFusedMaxParts];
-#pragma unroll
-            for (int c = 0; c < kFusedMaxParts; ++c) {
-                lse[c] = -INFINITY;
-                v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c < parts) {
-                    const int64_t slot = ((int64_t)u.unit + first + c) * RB + row;
-                    lse[c] = sl[c * RB + row];
-                    v[c] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + slot * HD + d));
-                }
-            }
-            float M = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kFusedMaxParts; ++c) M = fmaxf(M, lse[c]);
-            float Lsum = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int c = 0; c < kFusedMaxParts; ++c) {
-                    const float f = fast_exp2(lse[c] - M);  // -inf gives 0
-                    Lsum += f;
-                    acc.x += f * v[c].x;
-                    acc.y += f * v[c].y;
-                    acc.z += f * v[c].z;
-                    acc.w += f * v[c].w;
-                }
-            }
-            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            const int r = i / p.group, g = i - (i / p.group) * p.group;
-            __nv_bfloat16 *dst =
-                p.out + (((int64_t)u.b * p.q_rows + r) * p.n_q_heads + u.kvh * p.group + g) * HD + d;
-            uint2 packed;
-            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2 *>(dst) = packed;
+        if (!s_last[2 * k]) continue;  // uniform across the consumer warps
+        __threadfence();
+        if (n <= kGroupParts) {
+            merge_partials<HD, RB>(p, u, gslot, 1, n, true, sl, ctid);
+            if (ctid == 0) p.ws_count[u.unit] = 0;  // ready for the next call
+            continue;
         }
-        if (ctid == 0) p.ws_count[u.unit] = 0;  // ready for the next call
-        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // staging reused
+        merge_partials<HD, RB>(p, u, gslot, 1, gl - gf + 1, false, sl, ctid);
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+        const int groups = (n + kGroupParts - 1) / kGroupParts;
+        if (ctid == 0) {
+            p.ws_gcount[gslot] = 0;
+            s_last[2 * k + 1] = atomicAdd(p.ws_count + u.unit, 1) == groups - 1 ? 1 : 0;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+        if (!s_last[2 * k + 1]) continue;
+        __threadfence();
+        merge_partials<HD, RB>(p, u, (int64_t)u.unit + u.first, kGroupParts, groups, true, sl,
+                               ctid);
+        if (ctid == 0) p.ws_count[u.unit] = 0;
     }
 }
 
-// Merge of units that span more than kFusedMaxParts CTAs: one CTA per
+// Merge kernel, for launches whose units may span very many CTAs (long
+// contexts over few units): one CTA per
 // (request, KV head, query row of the group); its warps take the parts
 // round-robin (online max / sum per warp), and the warps' states are combined
 // in a fixed order, so the result does not depend on timing.
@@ -1394,7 +1443,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int2 parts = __ldcg(p.ws_parts + unit);
     const int first = parts.x, last = parts.y;
     // no keys (zero-filled) or few parts (merged by the split kernel)
-    if (last - first < kFusedMaxParts) return;
+    if (last - first < kGroupParts) return;
     // Each warp takes parts first + warp + kMergeWarps * k; a batch of kBatch
     // of them is loaded at once (all loads in flight), then folded into the
     // warp's state.
@@ -1487,8 +1536,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
 
 template <int HD, int MT, bool ROPE, bool FP8>
 int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                 const CUtensorMap &tk64, const CUtensorMap &tv64, bool merge,
-                 cudaStream_t stream) {
+                 const CUtensorMap &tk64, const CUtensorMap &tv64, cudaStream_t stream) {
     using G = Geo<HD, MT, FP8>;
     static_assert(G::kSmem * G::kCtasPerSm + 1024 * (G::kCtasPerSm - 1) <= 232448,
                   "shared memory budget");
@@ -1509,7 +1557,7 @@ int launch_split(const Params &p, const CUtensorMap &tk, const CUtensorMap &tv,
     if (launch_pdl(kern, dim3(p.grid), dim3(kThreads), smem, stream, tk, tv, tk64, tv64, p) !=
         cudaSuccess)
         return ATTN_ERR_CUDA;
-    if (merge) {
+    if (p.merge_kernel) {
         const unsigned ctas = (unsigned)((int64_t)p.batch * p.rows * p.n_kv_heads);
         if (launch_pdl(decode_merge_kernel<HD, G::RB>, dim3(ctas), dim3(kMergeWarps * 32), 0,
                        stream, p) != cudaSuccess)
@@ -1534,22 +1582,22 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
     plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
     const size_t units = (size_t)plan->batch_per_launch * n_kv_heads * plan->row_blocks;
-    // partial slots: unit + cta < units + grid; then one counter per unit
+    // partial slots: unit + cta < units + grid; then one counter per unit and
+    // one per partial slot (a group's counter sits at its first part's slot)
     const size_t slots = units + plan->grid;
     const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
     plan->counter_offset = (partial + 255) & ~size_t(255);
-    plan->counter_bytes = units * sizeof(int32_t);
+    plan->counter_bytes = (units + slots) * sizeof(int32_t);
     plan->meta_offset = plan->counter_offset + ((plan->counter_bytes + 255) & ~size_t(255));
-    const size_t meta = units * sizeof(int2);
-    plan->workspace = plan->meta_offset + meta;
-    // Can a unit span more than kFusedMaxParts CTAs?  Its chunks are at most
-    // the key bound / 16 + 1 and every CTA takes at least kMinChunksPerCta.
+    plan->workspace = plan->meta_offset + units * sizeof(int2);
+    // How many CTAs can a unit span?  Its chunks are at most the key bound /
+    // 16 + 1 and every CTA takes at least kMinChunksPerCta.
     int64_t keys = max_seq_len;
     if (window > 0) keys = std::min<int64_t>(keys, (int64_t)window + q_rows - 1);
     if (cache->kind == ATTN_CACHE_RING) keys = std::min<int64_t>(keys, cache->slots_per_seq);
     const int64_t max_chunks = (keys + dec::kChunk - 1) / dec::kChunk + 1;
     const int64_t max_parts = (max_chunks + dec::kMinChunksPerCta - 1) / dec::kMinChunksPerCta + 1;
-    plan->merge_kernel = max_parts > dec::kFusedMaxParts;
+    plan->merge_kernel = max_parts > dec::kMergeKernelParts;
     return ATTN_OK;
 }
 
@@ -1623,15 +1671,17 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
         p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                  plan.counter_offset);
+        p.ws_gcount = p.ws_count + units;
         p.ws_parts = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) +
                                               plan.meta_offset);
+        p.merge_kernel = plan.merge_kernel;
         int rc;
         const bool r = rope_inv_freq != nullptr;
 #define GQA_SPLIT(D, M)                                                                         \
-    (r ? dec::launch_split<D, M, true, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream) \
-       : dec::launch_split<D, M, false, false>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream))
+    (r ? dec::launch_split<D, M, true, false>(p, tk, tv, tk64, tv64, stream) \
+       : dec::launch_split<D, M, false, false>(p, tk, tv, tk64, tv64, stream))
 #define GQA_SPLIT_FP8(M) \
-    dec::launch_split<128, M, false, true>(p, tk, tv, tk64, tv64, plan.merge_kernel, stream)
+    dec::launch_split<128, M, false, true>(p, tk, tv, tk64, tv64, stream)
         if (fp8)  // head_dim 128, no fused append (refused before the launch)
             rc = plan.m_tiles == 0 ? GQA_SPLIT_FP8(0)
                  : plan.m_tiles == 1 ? GQA_SPLIT_FP8(1)

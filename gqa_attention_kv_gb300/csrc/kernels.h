@@ -66,10 +66,10 @@ struct DecodePlan {
     int row_blocks;       // units along the query rows of one KV head
     int grid;             // CTAs of the split kernel
     int batch_per_launch;
-    size_t workspace;     // bytes of scratch: fp32 partial states + per-unit counters
+    size_t workspace;     // bytes of scratch: fp32 partial states + merge counters
     size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
     size_t meta_offset;   // per unit (first, last) CTA of its chunks, for the merge kernel
-    bool merge_kernel;    // some unit may span more CTAs than the in-kernel merge takes
+    bool merge_kernel;    // units spanning very many CTAs are merged by a second kernel
 };
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
