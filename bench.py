@@ -61,10 +61,10 @@ def load_peaks():
 # T = 14,449, from ncu (profiles/prefill_kernel_qwen14449_dram.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 199613184,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 199703040,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "d463a88a693a42c09b2e9e7ae5aa0d126f2944d27915e47ec3711740a00c61b8"}
+                   "sha256": "a0030926e3b8099c1e3768bc9c16390a7c1ef3e1dd6c4b14721784449382ce50"}
 
 
 def prefill_traffic(T):
