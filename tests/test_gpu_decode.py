@@ -213,3 +213,39 @@ def test_streaming_encoder_step(batch):
     ref, _, _ = oracle_decode(case)
     out, _ = gpu_decode(case)
     compare(out, ref, f"streaming encoder B={batch}")
+
+
+@pytest.mark.parametrize("B,R,Hq,Hkv", [(300, 1, 8, 2), (150, 16, 8, 2), (260, 8, 16, 4)])
+def test_batch_split_over_launches(B, R, Hq, Hkv):
+    """More (request, row block) pairs than one launch's shared tables hold:
+    the host cuts the batch into several launches (one of them ragged)."""
+    g = torch.Generator().manual_seed(B * R)
+    seq = torch.randint(R, 200, (B,), generator=g).tolist()
+    case = synth.decode_case(7100 + B + R, LINEAR, B, R, Hq, Hkv, 128, seq)
+    ref, _, _ = oracle_decode(case)
+    out, _ = gpu_decode(case)
+    compare(out, ref, f"batch {B} x {R} rows")
+
+
+@pytest.mark.parametrize("L", [8192, 8200, 16000])
+def test_one_unit_over_many_ctas(L):
+    """One (request, KV head) over 64-126 CTAs: its partial states are merged
+    inside the split kernel in groups of eight (a ragged last group), then
+    the groups; the largest of these bounds is the last one merged that way."""
+    case = synth.decode_case(7200 + L, LINEAR, 1, 1, 8, 1, 128, [L])
+    ref, _, _ = oracle_decode(case)
+    a, _ = gpu_decode(case)
+    b, _ = gpu_decode(case)
+    assert torch.equal(a, b), "run-to-run results differ"
+    compare(a, ref, f"one unit, {L} keys")
+
+
+def test_merge_kernel_threshold():
+    """Just past the bound where the library hands long units to its merge
+    kernel: same answer within tolerance, deterministic."""
+    case = synth.decode_case(7300, LINEAR, 1, 2, 16, 2, 128, [16400], slots_per_seq=16512)
+    ref, _, _ = oracle_decode(case)
+    a, _ = gpu_decode(case, max_seq_len=16512)
+    b, _ = gpu_decode(case, max_seq_len=16512)
+    assert torch.equal(a, b), "run-to-run results differ"
+    compare(a, ref, "merge kernel threshold")

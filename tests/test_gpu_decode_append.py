@@ -26,6 +26,8 @@ CASES = [
     (PAGED, 3, 2, 16, 4, 64, [37, 300, 129], {"block_size": 5, "num_blocks": 200}),
     (RING, 4, 1, 32, 8, 128, [9000, 300, 16390, 8193], {"window": 8192, "ring": 16384}),
     (RING, 3, 4, 16, 4, 128, [1500 + 3, 4, 1501], {"window": 750, "ring": 1500}),
+    # more requests than one launch takes: the batch is cut into launches
+    (LINEAR, 260, 2, 8, 2, 128, [2 + (37 * i) % 150 for i in range(260)], {}),
 ]
 
 

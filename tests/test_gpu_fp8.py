@@ -238,3 +238,15 @@ def test_fp8_noalloc_entry_point():
                                  case.positions.to(DEV), case.max_seq_len(), 0, case.scale)
     torch.cuda.synchronize()
     compare(out, want, "fp8 noalloc")
+
+
+def test_fp8_batch_split_over_launches():
+    g = torch.Generator().manual_seed(9100)
+    seq = torch.randint(1, 200, (300,), generator=g).tolist()
+    case = synth.decode_case(9101, LINEAR, 300, 1, 8, 2, 128, seq)
+    check_case(case, where="fp8 batch 300")
+
+
+def test_fp8_one_unit_over_many_ctas():
+    case = synth.decode_case(9102, LINEAR, 1, 1, 8, 1, 128, [16000])
+    check_case(case, where="fp8 one unit, 16000 keys")
