@@ -156,6 +156,16 @@ struct Geo {
 
 constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
 
+// Four E4M3 codes (one 32-bit word, lowest byte first) -> two f16x2 words:
+// lo from bytes 0, 1 and hi from bytes 2, 3 (exact).  The word is split into
+// its 16-bit halves by register naming, so no shift is needed.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
 // Rotary embedding of one interleaved pair held as bf16x2 (low half = x[2i]):
 // rotated by the float32 angle pos * inv_freq in float32, rounded to bf16.
 __device__ __forceinline__ uint32_t rope_pair(uint32_t w, int pos, float inv_freq) {
@@ -879,10 +889,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
 #pragma unroll
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2(kw[0][kk]);
-                            a[1] = e4m3x2_to_f16x2(kw[1][kk]);
-                            a[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
-                            a[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+                            e4m3x4_to_f16x2x2(kw[0][kk], a[0], a[2]);
+                            e4m3x4_to_f16x2x2(kw[1][kk], a[1], a[3]);
                             mma_f16_16816((kk & 1) ? sodd : sacc, a, qb[kk][0], qb[kk][1]);
                         }
                     } else {
@@ -954,10 +962,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                             const uint32_t x = __byte_perm(vw[0][md >> 1], vw[1][md >> 1], sel);
                             const uint32_t y = __byte_perm(vw[2][md >> 1], vw[3][md >> 1], sel);
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2(x);
-                            a[1] = e4m3x2_to_f16x2(x >> 16);
-                            a[2] = e4m3x2_to_f16x2(y);
-                            a[3] = e4m3x2_to_f16x2(y >> 16);
+                            e4m3x4_to_f16x2x2(x, a[0], a[1]);
+                            e4m3x4_to_f16x2x2(y, a[2], a[3]);
                             mma_f16_16816(o[md], a, bh0, bh1);
                         }
                     } else {
@@ -1122,10 +1128,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                         }
     #pragma unroll
                         for (int kk = 0; kk < HD / 16; ++kk) {
-                            const uint32_t b00 = e4m3x2_to_f16x2(kw[0][kk]);
-                            const uint32_t b01 = e4m3x2_to_f16x2(kw[0][kk] >> 16);
-                            const uint32_t b10 = e4m3x2_to_f16x2(kw[1][kk]);
-                            const uint32_t b11 = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+                            uint32_t b00, b01, b10, b11;
+                            e4m3x4_to_f16x2x2(kw[0][kk], b00, b01);
+                            e4m3x4_to_f16x2x2(kw[1][kk], b10, b11);
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_f16_16816(s[mt][0], qa[mt][kk], b00, b01);
@@ -1218,8 +1223,9 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                             const uint32_t sel = (jj & 1) ? 0x7362u : 0x5140u;
                             const uint32_t x = __byte_perm(vw[0][jj >> 1], vw[1][jj >> 1], sel);
                             const uint32_t y = __byte_perm(vw[2][jj >> 1], vw[3][jj >> 1], sel);
-                            const uint32_t x0 = e4m3x2_to_f16x2(x), x1 = e4m3x2_to_f16x2(x >> 16);
-                            const uint32_t y0 = e4m3x2_to_f16x2(y), y1 = e4m3x2_to_f16x2(y >> 16);
+                            uint32_t x0, x1, y0, y1;
+                            e4m3x4_to_f16x2x2(x, x0, x1);
+                            e4m3x4_to_f16x2x2(y, y0, y1);
     #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_f16_16816(o[mt][2 * jj], pa[mt], x0, y0);
