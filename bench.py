@@ -778,14 +778,21 @@ def main():
     if pre_tf is not None:
         dominant = "prefill"
         ach = pflops / (pre_ms / K / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # The prefill launches of a timed region of a second or more run back
+        # to back under the power cap: their denominator is the sustained
+        # dense bf16 rate measured the same way; a short region takes the burst.
+        long_region = total_ms >= 1000.0
+        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
         roof = {"kernel": f"gqa::pre::prefill_kernel<{getattr(wl, 'D', 128)}>",
                 "bound": "tensor",
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4),
+                "frac_of_burst": round(ach / peaks["bf16_tflops"], 4),
                 "traffic": prefill_traffic(getattr(wl, "T", None)),
                 "traffic_unit": "DRAM bytes per launch (ncu)",
-                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+                "peak_source": f"{peak_src} bf16_tflops_sustained (timed region "
+                               f"{total_ms / 1e3:.1f} s, back to back)" if long_region
+                else f"{peak_src} bf16_tflops (burst)"}
     else:
         dominant = "decode"
         ach = dbytes / (dec_ms / K / 1e3) / 1e9
@@ -816,7 +823,9 @@ def main():
     if pre_tf is not None:
         line["prefill"] = {"value": round(pre_tf, 2), "unit": "TFLOP/s",
                            "flops_per_step": pflops,
-                           "frac_of_measured_bf16": round(pre_tf / world / peaks["bf16_tflops"], 4)}
+                           "frac_of_measured_bf16": round(pre_tf / world / peaks["bf16_tflops"], 4),
+                           "frac_of_measured_bf16_sustained":
+                               round(pre_tf / world / peaks["bf16_tflops_sustained"], 4)}
     if dec_gbs is not None and pre_tf is not None:
         line["roofline_decode"] = {"bound": "hbm", "achieved": line["decode"]["value"] / world,
                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
