@@ -212,7 +212,7 @@ class QwenWorkload(Workload):
     name = "qwen2-7b prompt prefill 14449 + decode 2x1 at 14449..23971"
     CONTEXTS = [(14449, 14449), (17623, 17623), (20797, 20797), (23971, 23971), (14449, 23971)]
 
-    def __init__(self, dev):
+    def __init__(self, dev, layout=0):
         import torch
 
         import gqa_attention_kv_gb300 as gq
@@ -233,10 +233,13 @@ class QwenWorkload(Workload):
         self.ncopy = max(6, math.ceil(4 * _l2_bytes() / per_copy) + 1)
         g = synth.generator(20263 + 5000, dev)
         self.caches = []
+        # slot-major [slot][head][D], or head-major [request][head][slot][D]
+        shape = (self.B * self.cap, Hkv, D) if layout == 0 else (self.B, Hkv, self.cap, D)
         for _ in range(self.ncopy):
-            kc = synth.normal_bf16(g, (self.B * self.cap, Hkv, D), dev)
-            vc = synth.normal_bf16(g, (self.B * self.cap, Hkv, D), dev)
-            self.caches.append(gq.KVCache(synth.LINEAR, kc, vc, slots_per_seq=self.cap))
+            kc = synth.normal_bf16(g, shape, dev)
+            vc = synth.normal_bf16(g, shape, dev)
+            self.caches.append(gq.KVCache(synth.LINEAR, kc, vc, slots_per_seq=self.cap,
+                                          layout=layout))
         self.prompt_slots = torch.arange(self.T, dtype=torch.int64, device=dev)
         self.dec = []
         for i, ctx in enumerate(self.CONTEXTS):
@@ -260,6 +263,7 @@ class QwenWorkload(Workload):
                          "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
                          "decode_contexts": [list(c) for c in self.CONTEXTS],
                          "cache": "linear", "decode_cache_copies": self.ncopy,
+                         "kv_layout": "BHSD" if layout else "BSHD",
                          "l2_defeat": "decode caches rotate over copies > 4x L2; prefill "
                                       "inputs+output 236 MB > L2"}
 
@@ -367,7 +371,7 @@ class QwenWorkload(Workload):
 class DecodeOnlyWorkload(Workload):
     """A decode step (append + decode) over rotating cache copies."""
 
-    def __init__(self, dev, which):
+    def __init__(self, dev, which, layout=0):
         import torch
 
         import gqa_attention_kv_gb300 as gq
@@ -382,6 +386,13 @@ class DecodeOnlyWorkload(Workload):
         base = make(device=dev)
         self.case = base
         self.kv_elem = 1 if self.fp8 else 2
+        rows = base.block_size if base.kind == synth.PAGED else base.slots_per_seq
+
+        def placed(t):  # [S, H, D] -> the layout's shape (a pure reordering)
+            if layout == 0:
+                return t
+            S, H, D = t.shape
+            return t.reshape(S // rows, rows, H, D).permute(0, 2, 1, 3).contiguous()
         per_copy = 2 * base.k_cache.numel() * self.kv_elem
         self.ncopy = max(2, min(256, math.ceil(4 * _l2_bytes() / per_copy) + 1))
         g = synth.generator(777, dev)
@@ -395,22 +406,24 @@ class DecodeOnlyWorkload(Workload):
             for i in range(self.ncopy):
                 kb = base.k_cache if i == 0 else synth.normal_bf16(g, base.k_cache.shape, dev)
                 vb = base.v_cache if i == 0 else synth.normal_bf16(g, base.v_cache.shape, dev)
-                c = gq.KVCache(base.kind, torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev),
-                               torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev),
+                c = gq.KVCache(base.kind,
+                               placed(torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev)),
+                               placed(torch.empty(S, Hkv, D, dtype=torch.uint8, device=dev)),
                                slots_per_seq=base.slots_per_seq, block_table=base.block_table,
                                block_size=base.block_size, dtype=gq.ATTN_KV_FP8_E4M3,
-                               k_ref=self.k_ref)
+                               k_ref=self.k_ref, layout=layout)
                 gq.attn_kv_append(kb, vb, all_slots, c)
                 self.caches.append(c)
                 del kb, vb
             torch.cuda.synchronize()
         else:
-            self.caches = [gq.KVCache(base.kind, base.k_cache if i == 0 else
-                                      synth.normal_bf16(g, base.k_cache.shape, dev),
-                                      base.v_cache if i == 0 else
-                                      synth.normal_bf16(g, base.v_cache.shape, dev),
+            self.caches = [gq.KVCache(base.kind, placed(base.k_cache if i == 0 else
+                                      synth.normal_bf16(g, base.k_cache.shape, dev)),
+                                      placed(base.v_cache if i == 0 else
+                                      synth.normal_bf16(g, base.v_cache.shape, dev)),
                                       slots_per_seq=base.slots_per_seq,
-                                      block_table=base.block_table, block_size=base.block_size)
+                                      block_table=base.block_table, block_size=base.block_size,
+                                      layout=layout)
                            for i in range(self.ncopy)]
         self.max_seq = base.max_seq_len()
         self.ws = torch.zeros(gq.attn_decode_workspace_size(
@@ -449,7 +462,8 @@ class DecodeOnlyWorkload(Workload):
             self.name += ", FP8 (E4M3) cache"
         self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
                          "layers_per_step": self.layers, "kv_cache": "fp8_e4m3" if self.fp8
-                         else "bf16", "l2_defeat": "caches rotate over copies > 4x L2"}
+                         else "bf16", "kv_layout": "BHSD" if layout else "BSHD",
+                         "l2_defeat": "caches rotate over copies > 4x L2"}
 
     def decode_bytes_per_step(self):
         c = self.case
@@ -540,12 +554,12 @@ class PrefillOnlyWorkload(Workload):
         ev("end")
 
 
-def make_workload(name, dev):
+def make_workload(name, dev, layout=0):
     if name == "qwen":
-        return QwenWorkload(dev)
+        return QwenWorkload(dev, layout)
     if name in ("voxtral", "ring", "paged", "stream-encoder", "ring-fp8", "paged-fp8",
                 "voxtral-fp8"):
-        return DecodeOnlyWorkload(dev, name)
+        return DecodeOnlyWorkload(dev, name, layout)
     if name in ("encoder", "encoder-long", "qwen-prefill", "prefill-8k"):
         return PrefillOnlyWorkload(dev, name)
     raise SystemExit(f"unknown workload {name}")
@@ -668,6 +682,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layout", default="bshd", choices=["bshd", "bhsd"],
+                    help="decode cache layout: slot-major [slot, head, D] (the configured "
+                         "one) or head-major blocks [block, head, rows, D]")
     ap.add_argument("--workload", default="qwen",
                     choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged",
                              "stream-encoder", "ring-fp8", "paged-fp8", "voxtral-fp8",
@@ -715,7 +732,7 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local_rank if world > 1 else 0)
     torch.cuda.set_device(dev)
-    wl = make_workload(args.workload, dev)
+    wl = make_workload(args.workload, dev, 1 if args.layout == "bhsd" else 0)
     stream = torch.cuda.Stream(device=dev)
 
     def barrier():

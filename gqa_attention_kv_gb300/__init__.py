@@ -26,6 +26,7 @@ for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
 ATTN_DECODE_TABLES_EARLY = 1  # attn_decode_append flag (include/attn_kv.h)
 ATTN_KV_BF16, ATTN_KV_FP8_E4M3 = 0, 1  # cache element types (attn_kv_dtype)
+ATTN_LAYOUT_BSHD, ATTN_LAYOUT_BHSD = 0, 1  # cache layouts (attn_kv_layout)
 
 _lock = threading.Lock()
 _lib = None
@@ -46,7 +47,7 @@ class _Cache(ctypes.Structure):
                 ("num_slots", ctypes.c_int64), ("slots_per_seq", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("k_ref", ctypes.c_void_p)]
+                ("k_ref", ctypes.c_void_p), ("layout", ctypes.c_int32)]
 
 
 def lib():
@@ -119,6 +120,9 @@ class KVCache:
     """One layer's cache: k, v [num_slots, n_kv_heads, head_dim] on the device,
     bf16, or uint8 E4M3 codes for an FP8 cache (dtype ATTN_KV_FP8_E4M3, whose
     keys are stored relative to k_ref, float32 [n_kv_heads, head_dim] or None).
+    layout ATTN_LAYOUT_BHSD: k, v are [num_slots // rows, n_kv_heads, rows,
+    head_dim] (rows = slots_per_seq, or block_size when paged); slots are
+    numbered as in the slot-major layout.
 
     kind LINEAR: slots_per_seq = per-request capacity.
     kind PAGED : block_table int32 [batch, max_blocks_per_seq] (device), block_size.
@@ -126,13 +130,14 @@ class KVCache:
     """
 
     def __init__(self, kind, k, v, slots_per_seq=0, block_table=None, block_size=0,
-                 dtype=ATTN_KV_BF16, k_ref=None):
+                 dtype=ATTN_KV_BF16, k_ref=None, layout=ATTN_LAYOUT_BSHD):
         self.kind, self.k, self.v = int(kind), k, v
         self.slots_per_seq = int(slots_per_seq)
         self.block_table = block_table
         self.block_size = int(block_size)
         self.dtype = int(dtype)
         self.k_ref = k_ref
+        self.layout = int(layout)
 
     @property
     def n_kv_heads(self):
@@ -140,14 +145,18 @@ class KVCache:
 
     @property
     def head_dim(self):
-        return self.k.shape[2]
+        return self.k.shape[-1]
+
+    @property
+    def num_slots(self):
+        return self.k.shape[0] * (self.k.shape[2] if self.layout == ATTN_LAYOUT_BHSD else 1)
 
     def struct(self) -> _Cache:
         bt = self.block_table
-        return _Cache(self.kind, self.k.data_ptr(), self.v.data_ptr(), self.k.shape[0],
+        return _Cache(self.kind, self.k.data_ptr(), self.v.data_ptr(), self.num_slots,
                       self.slots_per_seq, None if bt is None else bt.data_ptr(),
                       self.block_size, 0 if bt is None else bt.shape[-1], self.dtype,
-                      None if self.k_ref is None else self.k_ref.data_ptr())
+                      None if self.k_ref is None else self.k_ref.data_ptr(), self.layout)
 
 
 def attn_kv_append(k_new, v_new, slot_mapping, cache: KVCache, err=None, stream=None):

@@ -18,12 +18,14 @@ namespace gqa {
 __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict__ k_new,
                                                         const uint4 *__restrict__ v_new,
                                                         const int64_t *__restrict__ slot_mapping,
-                                                        int64_t n, uint4 *__restrict__ k_cache,
-                                                        uint4 *__restrict__ v_cache,
-                                                        int64_t num_slots, int pieces_per_row,
+                                                        int64_t n, uint8_t *__restrict__ k_cache,
+                                                        uint8_t *__restrict__ v_cache,
+                                                        int64_t num_slots, KvPlace place,
                                                         int32_t *err) {
     pdl_wait();
     pdl_launch_dependents();
+    const int pieces_per_head = place.head_bytes / 16;
+    const int pieces_per_row = place.n_kv_heads * pieces_per_head;
     const int64_t per_row = 2ll * pieces_per_row;
     const int64_t total = n * per_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -38,9 +40,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
             if (rem == 0) report_error(err, ATTN_ERR_BOUNDS);
             continue;
         }
+        const int h = piece / pieces_per_head, pp = piece - h * pieces_per_head;
         const uint4 *src = tensor == 0 ? k_new : v_new;
-        uint4 *dst = tensor == 0 ? k_cache : v_cache;
-        dst[slot * pieces_per_row + piece] = __ldg(src + row * pieces_per_row + piece);
+        uint8_t *dst = (tensor == 0 ? k_cache : v_cache) + place.head_offset(slot, h) + pp * 16;
+        *reinterpret_cast<uint4 *>(dst) = __ldg(src + row * pieces_per_row + piece);
     }
 }
 
@@ -50,10 +53,12 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
     const float4 *__restrict__ k_ref, const int64_t *__restrict__ slot_mapping, int64_t n,
-    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
-    int pieces_per_row, int32_t *err) {
+    uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache, int64_t num_slots,
+    KvPlace place, int32_t *err) {
     pdl_wait();
     pdl_launch_dependents();
+    const int pieces_per_head = place.head_bytes / 16;  // 16 codes per piece
+    const int pieces_per_row = place.n_kv_heads * pieces_per_head;
     const int64_t per_row = 2ll * pieces_per_row;
     const int64_t total = n * per_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -93,8 +98,9 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(
         for (int i = 0; i < 4; ++i)
             c[i] = f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1]) |
                    (f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]) << 16);
-        uint4 *dst = tensor == 0 ? k_cache : v_cache;
-        dst[slot * pieces_per_row + piece] = make_uint4(c[0], c[1], c[2], c[3]);
+        const int h = piece / pieces_per_head, pp = piece - h * pieces_per_head;
+        uint8_t *dst = (tensor == 0 ? k_cache : v_cache) + place.head_offset(slot, h) + pp * 16;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
     }
 }
 
@@ -132,9 +138,10 @@ int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,
 
 int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_ref,
                          const int64_t *slot_mapping, int64_t n, void *k_cache, void *v_cache,
-                         int64_t num_slots, int row_elems, int32_t *err, cudaStream_t stream) {
+                         int64_t num_slots, const KvPlace &place, int32_t *err,
+                         cudaStream_t stream) {
     if (n <= 0) return ATTN_OK;
-    const int pieces = row_elems / 16;  // 16 codes per piece
+    const int pieces = place.n_kv_heads * place.head_bytes / 16;  // 16 codes per piece
     const int64_t total = n * 2ll * pieces;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
@@ -143,16 +150,16 @@ int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_re
     const cudaError_t e = launch_pdl(
         kv_append_fp8_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-        reinterpret_cast<const float4 *>(k_ref), slot_mapping, n, static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), num_slots, pieces, err);
+        reinterpret_cast<const float4 *>(k_ref), slot_mapping, n,
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), num_slots, place, err);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
-                     void *k_cache, void *v_cache, int64_t num_slots, int row_bytes,
+                     void *k_cache, void *v_cache, int64_t num_slots, const KvPlace &place,
                      int32_t *err, cudaStream_t stream) {
     if (n <= 0) return ATTN_OK;
-    const int pieces = row_bytes / 16;
+    const int pieces = place.n_kv_heads * place.head_bytes / 16;
     const int64_t total = n * 2ll * pieces;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
@@ -161,7 +168,7 @@ int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_m
     const cudaError_t e = launch_pdl(
         kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, n,
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots, pieces, err);
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), num_slots, place, err);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

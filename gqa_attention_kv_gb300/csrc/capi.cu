@@ -85,6 +85,17 @@ bool heads_ok(int n_q_heads, int n_kv_heads, int head_dim) {
            (head_dim == 64 || head_dim == 128);
 }
 
+// The layout fields: a known layout, and for the head-major one whole blocks.
+int check_layout(const attn_kv_cache *c) {
+    if (c->layout == ATTN_LAYOUT_BSHD) return ATTN_OK;
+    if (c->layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_UNSUPPORTED;
+    const int64_t rows = c->kind == ATTN_CACHE_PAGED ? c->block_size : c->slots_per_seq;
+    if (c->kind != ATTN_CACHE_LINEAR && c->kind != ATTN_CACHE_PAGED && c->kind != ATTN_CACHE_RING)
+        return ATTN_ERR_SHAPE;
+    if (rows < 1 || c->num_slots % rows != 0) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
 // Validation shared by attn_decode and attn_decode_workspace_size.
 int check_decode_shape(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
                        int n_kv_heads, int head_dim, int max_seq_len, int window) {
@@ -99,6 +110,12 @@ int check_decode_shape(const attn_kv_cache *cache, int batch, int q_rows, int n_
     if (cache->dtype != ATTN_KV_BF16 && cache->dtype != ATTN_KV_FP8_E4M3)
         return ATTN_ERR_UNSUPPORTED;
     if (cache->dtype == ATTN_KV_FP8_E4M3 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (int rc = check_layout(cache); rc != ATTN_OK) return rc;
+    if (cache->layout == ATTN_LAYOUT_BHSD &&
+        (cache->num_slots / (cache->kind == ATTN_CACHE_PAGED ? cache->block_size
+                                                              : cache->slots_per_seq)) *
+                n_kv_heads >= (int64_t(1) << 31))
+        return ATTN_ERR_SHAPE;
     switch (cache->kind) {
     case ATTN_CACHE_LINEAR:
         if (cache->slots_per_seq < 1 ||
@@ -137,19 +154,21 @@ int attn_kv_append(const void *k_new, const void *v_new, const int64_t *slot_map
     if (n == 0) return ATTN_OK;
     if (!k_new || !v_new || !slot_mapping || !cache->k || !cache->v) return ATTN_ERR_NULL;
     if (cache->num_slots < 1) return ATTN_ERR_SHAPE;
+    if (int rc = check_layout(cache); rc != ATTN_OK) return rc;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cache->k) || !aligned16(cache->v))
         return ATTN_ERR_ALIGN;
     if (cache->dtype == ATTN_KV_FP8_E4M3) {
         if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
         if (cache->k_ref && !aligned16(cache->k_ref)) return ATTN_ERR_ALIGN;
         return gqa::launch_kv_append_fp8(k_new, v_new, cache->k_ref, slot_mapping, n, cache->k,
-                                         cache->v, cache->num_slots, n_kv_heads * head_dim,
-                                         err_word, reinterpret_cast<cudaStream_t>(stream));
+                                         cache->v, cache->num_slots,
+                                         gqa::kv_place(cache, n_kv_heads, head_dim, 1), err_word,
+                                         reinterpret_cast<cudaStream_t>(stream));
     }
     if (cache->dtype != ATTN_KV_BF16) return ATTN_ERR_UNSUPPORTED;
     return gqa::launch_kv_append(k_new, v_new, slot_mapping, n, cache->k, cache->v,
-                                 cache->num_slots, n_kv_heads * head_dim * 2, err_word,
-                                 reinterpret_cast<cudaStream_t>(stream));
+                                 cache->num_slots, gqa::kv_place(cache, n_kv_heads, head_dim, 2),
+                                 err_word, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_kv_reference(const void *k, int64_t n, int n_kv_heads, int head_dim, float *ref,

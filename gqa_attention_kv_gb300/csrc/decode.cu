@@ -96,6 +96,7 @@ struct Params {
     int32_t *ws_count;   // per unit: merged groups so far (zero between calls)
     int32_t *ws_gcount;  // per partial slot that starts a group: parts stored so far
     int2 *ws_parts;      // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
+    KvPlace place;       // where a head's row of a slot lives (slot-major or head-major)
     bool merge_kernel;   // units of more than kGroupParts parts go to the merge kernel
     // fused append (nullptr: none): the step's rows, bf16 [batch * q_rows][n_kv_heads][HD],
     // row b * q_rows + r being the key at position seq_len_b - q_rows + r, and their slots
@@ -155,6 +156,25 @@ struct Geo {
 };
 
 constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
+
+// 4D tiled TMA load / L2 prefetch (head-major caches: {columns, rows, halves,
+// block x head}).
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 int z, int w, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z,
+                                                int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
 
 // Four E4M3 codes (one 32-bit word, lowest byte first) -> two f16x2 words:
 // lo from bytes 0, 1 and hi from bytes 2, 3 (exact).  The word is split into
@@ -493,6 +513,13 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                         j %= p.slots_per_seq;
                         if (j + kTileRows > p.slots_per_seq) continue;  // wraps: gathered later
                     }
+                    if (p.place.rows != 0) {  // head-major: block = request
+                        if (j + kTileRows > p.slots_per_seq) continue;
+                        const int w = bg * p.n_kv_heads + sg.kvh;
+                        tma_prefetch_4d(&tm_k64, 0, j, 0, w);
+                        tma_prefetch_4d(&tm_v64, 0, j, 0, w);
+                        continue;
+                    }
                     const int y = (int)((int64_t)bg * p.slots_per_seq + j);
                     tma_prefetch_3d(&tm_k64, 0, y, z);
                     tma_prefetch_3d(&tm_v64, 0, y, z);
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         const bool paged = p.kind == ATTN_CACHE_PAGED;
         const bool paged_tma = paged && (p.block_size % kChunk == 0);
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
-        const int64_t row_elems = (int64_t)p.n_kv_heads * HD;
+        const bool bhsd = p.place.rows != 0;  // head-major: boxes stay inside one block
         const int c = lane & (kWarps - 1);
         const bool fused = !FP8 && p.k_new != nullptr;
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
@@ -636,6 +663,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                                     : -2;
                     }
                 }
+                // head-major: a box must not cross the end of its block
+                if (bhsd && slot0 >= 0 && slot0 % p.place.rows + kChunk > p.place.rows) slot0 = -2;
                 if (lane < kWarps && slot0 == -1 && t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
                 const unsigned lanes = (1u << kWarps) - 1;
                 const unsigned boxed = __ballot_sync(0xffffffffu, slot0 >= -1) & lanes;
@@ -644,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 // a tile whose 64 slots are consecutive is one 64-row box per
                 // 64 columns; otherwise each boxed chunk is a 16-row box
                 const bool whole_tile =
-                    __all_sync(0xffffffffu, slot0 == slot00 + (int64_t)c * kChunk) && slot00 >= 0;
+                    __all_sync(0xffffffffu, slot0 == slot00 + (int64_t)c * kChunk) && slot00 >= 0 &&
+                    (!bhsd || slot00 % p.place.rows + kTileRows <= p.place.rows);
                 // gathered chunks: lane l copies row l % 16 of K (l < 16) or V
                 uint32_t gmask = 0;
                 bool issued_cp = false;
@@ -667,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                                      ((int64_t)(sg.b * p.q_rows + (t - new_lo)) * p.n_kv_heads +
                                       sg.kvh) * HD)
                                : reinterpret_cast<const uint8_t *>(tensor ? p.v_cache : p.k_cache) +
-                                     ((s < 0 ? 0 : s) * row_elems + (int64_t)sg.kvh * HD) * G::kElem;
+                                     p.place.head_offset(s < 0 ? 0 : s, sg.kvh);
                     uint8_t *dst = tensor ? vst : kst;
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD * G::kElem / 16; ++c16)
@@ -685,19 +715,37 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 const uint32_t tma_bytes = __popc(boxed) * 2 * G::kChunkBytes;
                 if (lane == 0 && tma_bytes) mbar_expect_tx(&full[st], tma_bytes);
                 __syncwarp();
-                // boxes {64 columns, rows, halves} of the caches viewed as
-                // [half index = kv head * halves + half][slot][64 columns]
+                // slot-major: boxes {columns, rows, halves} of the caches viewed
+                // as [kv head * halves + half][slot][columns]; head-major: boxes
+                // {columns, rows, halves, 1} of [block * heads + head][half][row][columns]
                 if (whole_tile) {
-                    if (lane < 2)
-                        tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
-                                         (int)slot00, sg.kvh * G::kHalves, &full[st], kv_policy);
+                    if (lane < 2) {
+                        if (bhsd)
+                            tma_load_4d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
+                                             (int)(slot00 % p.place.rows), 0,
+                                             (int)(slot00 / p.place.rows) * p.n_kv_heads + sg.kvh,
+                                             &full[st], kv_policy);
+                        else
+                            tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
+                                             (int)slot00, sg.kvh * G::kHalves, &full[st],
+                                             kv_policy);
+                    }
                 } else if (lane < kWarps && slot0 >= -1) {
-                    const int y = slot0 < 0 ? -kChunk : (int)slot0;
                     const uint32_t off = chunk_base<G::kHalves>(false, lane);
-                    tma_load_3d_hint(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st],
-                                     kv_policy);
-                    tma_load_3d_hint(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st],
-                                     kv_policy);
+                    if (bhsd) {
+                        // an out-of-range page aims above row 0: zero-filled
+                        const int y = slot0 < 0 ? -kChunk : (int)(slot0 % p.place.rows);
+                        const int w = slot0 < 0 ? sg.kvh
+                                                : (int)(slot0 / p.place.rows) * p.n_kv_heads + sg.kvh;
+                        tma_load_4d_hint(kst + off, &tm_k, 0, y, 0, w, &full[st], kv_policy);
+                        tma_load_4d_hint(vst + off, &tm_v, 0, y, 0, w, &full[st], kv_policy);
+                    } else {
+                        const int y = slot0 < 0 ? -kChunk : (int)slot0;
+                        tma_load_3d_hint(kst + off, &tm_k, 0, y, sg.kvh * G::kHalves, &full[st],
+                                         kv_policy);
+                        tma_load_3d_hint(vst + off, &tm_v, 0, y, sg.kvh * G::kHalves, &full[st],
+                                         kv_policy);
+                    }
                 }
                 __syncwarp();
                 if (issued_cp)
@@ -737,9 +785,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
             }
             const uint4 *src =
                 reinterpret_cast<const uint4 *>(tensor ? p.v_new : p.k_new) + row * pieces + pc;
+            const int h = pc / (HD / 8), pp = pc - h * (HD / 8);
             uint4 *dst = reinterpret_cast<uint4 *>(
-                             const_cast<__nv_bfloat16 *>(tensor ? p.v_cache : p.k_cache)) +
-                         slot * pieces + pc;
+                reinterpret_cast<uint8_t *>(const_cast<__nv_bfloat16 *>(tensor ? p.v_cache
+                                                                                : p.k_cache)) +
+                p.place.head_offset(slot, h) + pp * 16);
             uint4 w = __ldg(src);
             if (rope && tensor == 0) {
                 // key row b*q_rows + r sits at position seq_len_b - q_rows + r
@@ -1620,15 +1670,38 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
     const int esize = fp8 ? 1 : 2;
     const int halves = plan.head_dim * esize / 128;
     const uint32_t cols = 128 / esize;
-    const uint64_t dims[3] = {cols, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
-    const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * esize, 128};
-    const uint32_t box[3] = {cols, (uint32_t)dec::kChunk, (uint32_t)halves};
-    const uint32_t box64[3] = {cols, (uint32_t)dec::kTileRows, (uint32_t)halves};
+    const KvPlace place = kv_place(cache, n_kv_heads, plan.head_dim, esize);
     CUtensorMap tk, tv, tk64, tv64;
-    if (!encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true, fp8) ||
-        !encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true, fp8) ||
-        !encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true, fp8) ||
-        !encode_tensor_map(&tv64, cache->v, 3, dims, strides, box64, true, fp8)) {
+    bool maps_ok;
+    if (place.rows == 0) {
+        const uint64_t dims[3] = {cols, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
+        const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * esize, 128};
+        const uint32_t box[3] = {cols, (uint32_t)dec::kChunk, (uint32_t)halves};
+        const uint32_t box64[3] = {cols, (uint32_t)dec::kTileRows, (uint32_t)halves};
+        maps_ok = encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true, fp8) &&
+                  encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true, fp8) &&
+                  encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true, fp8) &&
+                  encode_tensor_map(&tv64, cache->v, 3, dims, strides, box64, true, fp8);
+    } else {
+        // [block * heads + head][row][half][columns], iterated {columns, row, half,
+        // block-head} so a box lands as [half][rows][128 B].  Boxes taller than
+        // a block are encoded at the block's height and never issued (the
+        // kernel boxes only chunks and tiles that lie inside one block).
+        const uint64_t row_bytes = (uint64_t)plan.head_dim * esize;
+        const uint64_t rows = (uint64_t)place.rows;
+        const uint64_t dims[4] = {cols, rows, (uint64_t)halves,
+                                  (uint64_t)(cache->num_slots / place.rows) * n_kv_heads};
+        const uint64_t strides[3] = {row_bytes, 128, rows * row_bytes};
+        const uint32_t r16 = (uint32_t)std::min<uint64_t>(rows, dec::kChunk);
+        const uint32_t r64 = (uint32_t)std::min<uint64_t>(rows, dec::kTileRows);
+        const uint32_t box[4] = {cols, r16, (uint32_t)halves, 1};
+        const uint32_t box64[4] = {cols, r64, (uint32_t)halves, 1};
+        maps_ok = encode_tensor_map(&tk, cache->k, 4, dims, strides, box, true, fp8) &&
+                  encode_tensor_map(&tv, cache->v, 4, dims, strides, box, true, fp8) &&
+                  encode_tensor_map(&tk64, cache->k, 4, dims, strides, box64, true, fp8) &&
+                  encode_tensor_map(&tv64, cache->v, 4, dims, strides, box64, true, fp8);
+    }
+    if (!maps_ok) {
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
@@ -1681,6 +1754,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_parts = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) +
                                               plan.meta_offset);
         p.merge_kernel = plan.merge_kernel;
+        p.place = place;
         int rc;
         const bool r = rope_inv_freq != nullptr;
 #define GQA_SPLIT(D, M)                                                                         \

@@ -42,15 +42,39 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint6
                        const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128,
                        bool bytes = false);
 
+// Where head h's row of cache slot s starts, in bytes (attn_kv_cache's layouts):
+// slot-major (rows == 0) or head-major inside blocks of `rows` slots.
+struct KvPlace {
+    int64_t rows;    // 0: ATTN_LAYOUT_BSHD; else the block size of ATTN_LAYOUT_BHSD
+    int n_kv_heads;
+    int head_bytes;  // head_dim x element size
+    __host__ __device__ __forceinline__ int64_t head_offset(int64_t s, int h) const {
+        return rows == 0 ? (s * n_kv_heads + h) * head_bytes
+                         : (((s / rows) * n_kv_heads + h) * rows + s % rows) * head_bytes;
+    }
+};
+
+// The placement a cache descriptor asks for (element size esize bytes).
+inline KvPlace kv_place(const attn_kv_cache *c, int n_kv_heads, int head_dim, int esize) {
+    KvPlace p;
+    p.rows = c->layout == ATTN_LAYOUT_BHSD
+                 ? (c->kind == ATTN_CACHE_PAGED ? c->block_size : c->slots_per_seq)
+                 : 0;
+    p.n_kv_heads = n_kv_heads;
+    p.head_bytes = head_dim * esize;
+    return p;
+}
+
 int launch_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int64_t n,
-                     void *k_cache, void *v_cache, int64_t num_slots, int row_bytes,
+                     void *k_cache, void *v_cache, int64_t num_slots, const KvPlace &place,
                      int32_t *err, cudaStream_t stream);
 
 // FP8 cache append: row_elems = n_kv_heads * head_dim (a multiple of 16);
 // k_ref float32 [row_elems] or nullptr.
 int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_ref,
                          const int64_t *slot_mapping, int64_t n, void *k_cache, void *v_cache,
-                         int64_t num_slots, int row_elems, int32_t *err, cudaStream_t stream);
+                         int64_t num_slots, const KvPlace &place, int32_t *err,
+                         cudaStream_t stream);
 
 // ref[e] = mean over n rows of the bf16 matrix k[n][row_elems], as float32.
 int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,

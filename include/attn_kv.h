@@ -77,6 +77,11 @@ typedef enum {
 } attn_cache_kind;
 
 typedef enum {
+    ATTN_LAYOUT_BSHD = 0, /* slot-major: element (slot, head, d) at (slot*n_kv_heads + head)*head_dim + d */
+    ATTN_LAYOUT_BHSD = 1  /* head-major inside each block of `rows` slots (see attn_kv_cache) */
+} attn_kv_layout;
+
+typedef enum {
     ATTN_KV_BF16 = 0,    /* 16-bit bf16 elements */
     ATTN_KV_FP8_E4M3 = 1 /* 8-bit E4M3 elements, K stored relative to k_ref */
 } attn_kv_dtype;
@@ -106,7 +111,18 @@ typedef enum {
  * first prefill chunk's keys (attn_kv_reference).  Subtracting one vector from
  * every key of a head adds the same amount to all of a query row's scores, so
  * attention reads the stored keys as they are and needs no k_ref.  FP8 caches
- * require head_dim 128.  A zero-initialised struct is a bf16 cache.
+ * require head_dim 128.
+ *
+ * layout ATTN_LAYOUT_BHSD (Voxtral notes, "KV cache": the CUDA path keeps its
+ * static and ring caches as [B, H, S, D]): the slots form blocks of `rows`
+ * consecutive slots -- rows = slots_per_seq for LINEAR and RING (a block is a
+ * request), block_size for PAGED (a block is a page) -- and each block stores
+ * its heads one after another: element (slot s, head h, d) lives at
+ *     ((s / rows) * n_kv_heads + h) * rows + s % rows) * head_dim + d.
+ * Slot numbers, slot_mapping and block tables mean exactly what they mean for
+ * the slot-major layout; only the placement differs, so one KV head's keys of
+ * a block are contiguous.  num_slots must be a multiple of rows.
+ * A zero-initialised struct is a bf16, slot-major cache.
  */
 typedef struct {
     int32_t kind;               /* attn_cache_kind */
@@ -119,6 +135,7 @@ typedef struct {
     int32_t max_blocks_per_seq; /* PAGED only: row length of block_table */
     int32_t dtype;              /* attn_kv_dtype */
     const float *k_ref;         /* FP8 only: float32 [n_kv_heads, head_dim], device, or NULL */
+    int32_t layout;             /* attn_kv_layout */
 } attn_kv_cache;
 
 /*
@@ -136,7 +153,8 @@ typedef struct {
  *                 its row and stores ATTN_ERR_BOUNDS in *err_word
  *   n             rows to write (0 is a no-op)
  * Copies are bit-exact.  With a slot repeated inside one call, which row lands
- * is unspecified.  Does not read cache->kind: slots are absolute.  For an FP8
+ * is unspecified.  Slots are absolute: cache->kind matters only for the
+ * head-major layout, whose block size it selects.  For an FP8
  * cache the rows are converted as attn_kv_cache states (bit-exact against
  * that definition), and k_new / v_new stay bf16.
  */

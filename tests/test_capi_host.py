@@ -197,3 +197,19 @@ def test_kv_reference_validation(lib):
     assert f(None, 4, 8, 128, 32, None) == gq.ATTN_ERR_NULL
     assert f(16, 4, 8, 128, None, None) == gq.ATTN_ERR_NULL
     assert f(18, 4, 8, 128, 32, None) == gq.ATTN_ERR_ALIGN
+
+
+def test_layout_validation(lib):
+    """Head-major caches need whole blocks; unknown layouts are refused."""
+    c = cache()
+    c.layout = 7
+    assert decode_rc(lib, c) == gq.ATTN_ERR_UNSUPPORTED
+    c = cache(slots=1000, sps=300)   # 1000 slots are not whole blocks of 300
+    c.layout = gq.ATTN_LAYOUT_BHSD
+    assert decode_rc(lib, c, B=2) == gq.ATTN_ERR_SHAPE
+    cs = c.struct()
+    assert lib.attn_kv_append(16, 32, 48, 4, ctypes.byref(cs), 8, 128, None,
+                              None) == gq.ATTN_ERR_SHAPE
+    c = cache(slots=1024, sps=512)
+    c.layout = gq.ATTN_LAYOUT_BHSD
+    assert decode_rc(lib, c, B=0) == gq.ATTN_OK
