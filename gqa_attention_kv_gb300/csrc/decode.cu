@@ -618,6 +618,45 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 uint8_t *kst = stages + st * G::kStageBytes;
                 uint8_t *vst = kst + G::kTileBytes;
                 const int chunk0 = sg.c_begin + it * kWarps;
+                // Fast path: a linear or ring tile of four present chunks whose 64
+                // positions sit in 64 consecutive slots and hold none of the
+                // step's new rows is one box per tensor.  Every lane reaches the
+                // same decision with a few integer operations: no ballots, so
+                // the producer keeps ahead of the stream (its general path costs
+                // ~1,000 cycles a tile).
+                if (!paged && chunk0 + kWarps <= sg.c_end) {
+                    const int T0 = chunk0 * kChunk;
+                    const bool no_new = !fused || T0 + kTileRows <= new_lo || T0 >= seq_len;
+                    int j0 = T0;
+                    bool fits = !bhsd || T0 + kTileRows <= p.slots_per_seq;
+                    if (p.kind == ATTN_CACHE_RING) {
+                        j0 = T0 % p.slots_per_seq;
+                        fits = j0 + kTileRows <= p.slots_per_seq;
+                    }
+                    const int64_t s00 = (int64_t)bg * p.slots_per_seq + j0;
+                    if (no_new && fits && s00 + kTileRows <= p.num_slots) {
+                        if (lane == 0) info_whole[st] = 1;
+                        if (lane < kWarps) {
+                            info_t0[st * kWarps + lane] = T0 + lane * kChunk;
+                            info_mask[st * kWarps + lane] = 0xFFFFu;
+                        }
+                        if (lane == 0) mbar_expect_tx(&full[st], 2 * G::kTileBytes);
+                        __syncwarp();
+                        if (lane < 2) {
+                            if (bhsd)  // block = request, row = position in its window
+                                tma_load_4d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, j0,
+                                                 0, bg * p.n_kv_heads + sg.kvh, &full[st],
+                                                 kv_policy);
+                            else
+                                tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
+                                                 (int)s00, sg.kvh * G::kHalves, &full[st],
+                                                 kv_policy);
+                        }
+                        __syncwarp();
+                        mbar_arrive(&full[st]);
+                        continue;
+                    }
+                }
                 const int chunk = chunk0 + c;
                 const int t0 = chunk * kChunk;
                 // slot0 >= 0: first of 16 consecutive slots (TMA box); -1: a
