@@ -122,13 +122,19 @@ struct Geo {
     static constexpr int kElem = FP8 ? 1 : 2;               // bytes per cache element
     static constexpr int kHalves = HD * kElem / 128;        // 128-byte column blocks
     static constexpr int kChunkBytes = kHalves * kChunk * 128;
-    static constexpr int kTileBytes = kWarps * kChunkBytes;  // K (or V) of one tile
+    // chunks per tile: E4M3 rows are half as wide, so an FP8 tile holds 128
+    // keys (each consumer warp takes two chunks of it) and a producer step
+    // moves as many bytes as a bf16 one
+    static constexpr int kCPT = FP8 ? 2 * kWarps : kWarps;
+    static constexpr int kSubs = kCPT / kWarps;   // chunks of a tile per consumer warp
+    static constexpr int kTileRows = kCPT * kChunk;
+    static constexpr int kTileBytes = kCPT * kChunkBytes;  // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     // At the end of a segment each warp parks its O rows (RB x HD fp32) in
     // its own rows of the stage that held the segment's last tile (K and V,
     // 2 * kHalves pieces of 16 x 128 B, which it has finished reading); only
     // 32-row units need a dedicated area.  Row maxima and sums always have one.
-    static constexpr bool kParkInStage = RB * HD * 4 <= 2 * kHalves * kChunk * 128;
+    static constexpr bool kParkInStage = RB * HD * 4 <= 2 * kSubs * kHalves * kChunk * 128;
     // + per row and warp: max, sum, combined weight; per row: log-sum-exp
     static constexpr int kMergeBytes = (kParkInStage ? 0 : kWarps * RB * HD * 4) + (3 * kWarps + 1) * RB * 4;
     static constexpr int kTableBytes = (4 * kMaxTableEntries + 1) * 4;
@@ -145,8 +151,8 @@ struct Geo {
     static constexpr int kOffBars = kOffMerge + kMergeBytes;
     // full[kStages], empty[kStages], q_full[2], q_empty[2]
     static constexpr int kOffInfo = kOffBars + (2 * kStages + 4) * 8;
-    // info: t0[kStages][kWarps], mask[kStages][kWarps], whole[kStages], last[4]
-    static constexpr int kOffTable = kOffInfo + ((2 * kStages * kWarps + kStages + 4) * 4 + 15) / 16 * 16;
+    // info: t0[kStages][kCPT], mask[kStages][kCPT], whole[kStages], last[4]
+    static constexpr int kOffTable = kOffInfo + ((2 * kStages * kCPT + kStages + 4) * 4 + 15) / 16 * 16;
     // tables: cnt[E], clo[E], seqlen[B], Pb[B + 1] with E, B <= kMaxTableEntries
     static constexpr int kOffQ = (kOffTable + kTableBytes + 15) / 16 * 16;
     static constexpr size_t kSmem = 1024 + kOffQ + kQBytes;
@@ -155,7 +161,7 @@ struct Geo {
     static_assert(!FP8 || HD == 128, "FP8 caches have 128-element heads");
 };
 
-constexpr int kTileRows = kWarps * kChunk;  // 64 key positions per tile
+constexpr int kTileRows = kWarps * kChunk;  // key positions of a bf16 tile (64)
 
 // 4D tiled TMA load / L2 prefetch (head-major caches: {columns, rows, halves,
 // block x head}).
@@ -204,8 +210,9 @@ template <int HALVES>
 __device__ __forceinline__ uint32_t chunk_base(bool whole, int c) {
     return whole ? (uint32_t)c * (kChunk * 128) : (uint32_t)c * (HALVES * kChunk * 128);
 }
+template <int TILE_ROWS>
 __device__ __forceinline__ uint32_t half_stride(bool whole) {
-    return whole ? (uint32_t)(kTileRows * 128) : (uint32_t)(kChunk * 128);
+    return whole ? (uint32_t)(TILE_ROWS * 128) : (uint32_t)(kChunk * 128);
 }
 // Offset of 16-byte piece c16 (0 .. row bytes / 16 - 1) of row `key` (0 .. 15)
 // of a chunk.
@@ -420,9 +427,10 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     uint8_t *qbuf = smem + G::kOffQ;     // [2][RB][kQStride]
     int *posbuf = reinterpret_cast<int *>(qbuf + 2 * RB * G::kQStride);  // [2][RB]
     float *rope_if = reinterpret_cast<float *>(posbuf + 2 * RB);        // [HD / 2]
-    int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kWarps]
-    uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kWarps);
-    int *info_whole = reinterpret_cast<int *>(info_mask + kStages * kWarps);  // [kStages]
+    constexpr int kCPT = G::kCPT;
+    int *info_t0 = reinterpret_cast<int *>(smem + G::kOffInfo);  // [kStages][kCPT]
+    uint32_t *info_mask = reinterpret_cast<uint32_t *>(info_t0 + kStages * kCPT);
+    int *info_whole = reinterpret_cast<int *>(info_mask + kStages * kCPT);  // [kStages]
     int *s_last = info_whole + kStages;
     Tables tb;
     tb.cnt = reinterpret_cast<int *>(smem + G::kOffTable);
@@ -506,15 +514,15 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
             while (issued < kPrefetchTiles && walk.next(p, tb, sg)) {
                 const int bg = p.b_base + sg.b;
                 for (int c = sg.c_begin; c < sg.c_end && issued < kPrefetchTiles;
-                     c += kWarps, ++issued) {
+                     c += kCPT, ++issued) {
                     const int z = sg.kvh * G::kHalves;
                     int j = c * kChunk;  // first position of the tile
                     if (p.kind == ATTN_CACHE_RING) {
                         j %= p.slots_per_seq;
-                        if (j + kTileRows > p.slots_per_seq) continue;  // wraps: gathered later
+                        if (j + G::kTileRows > p.slots_per_seq) continue;  // wraps: gathered later
                     }
                     if (p.place.rows != 0) {  // head-major: block = request
-                        if (j + kTileRows > p.slots_per_seq) continue;
+                        if (j + G::kTileRows > p.slots_per_seq) continue;
                         const int w = bg * p.n_kv_heads + sg.kvh;
                         tma_prefetch_4d(&tm_k64, 0, j, 0, w);
                         tma_prefetch_4d(&tm_v64, 0, j, 0, w);
@@ -549,14 +557,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        // Lane c (mod kWarps) describes chunk c of each tile; the warp agrees
+        // Lane c (mod kCPT) describes chunk c of each tile; the warp agrees
         // on the tile's form with ballots, so a tile costs a few dozen
         // instructions on the issuing path.
         const bool paged = p.kind == ATTN_CACHE_PAGED;
         const bool paged_tma = paged && (p.block_size % kChunk == 0);
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const bool bhsd = p.place.rows != 0;  // head-major: boxes stay inside one block
-        const int c = lane & (kWarps - 1);
+        const int c = lane & (kCPT - 1);
         const bool fused = !FP8 && p.k_new != nullptr;
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
         SegmentWalker walk{g0, g1, L};
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
             };
             const int seq_len = tb.seqlen[sg.b];
             const int new_lo = seq_len - p.q_rows;  // first of the step's new keys
-            const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
+            const int n_tiles = (sg.c_end - sg.c_begin + kCPT - 1) / kCPT;
             // page ids of two consecutive 32-page windows, one per lane; the
             // second is fetched a window ahead of its use
             int win = -1, pg_cur = -1, pg_next = -1;
@@ -617,28 +625,29 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 if (!ok) break;
                 uint8_t *kst = stages + st * G::kStageBytes;
                 uint8_t *vst = kst + G::kTileBytes;
-                const int chunk0 = sg.c_begin + it * kWarps;
+                const int chunk0 = sg.c_begin + it * kCPT;
                 // Fast path: a linear or ring tile of four present chunks whose 64
                 // positions sit in 64 consecutive slots and hold none of the
                 // step's new rows is one box per tensor.  Every lane reaches the
                 // same decision with a few integer operations: no ballots, so
                 // the producer keeps ahead of the stream (its general path costs
                 // ~1,000 cycles a tile).
-                if (!paged && chunk0 + kWarps <= sg.c_end) {
+                if (!paged && chunk0 + kCPT <= sg.c_end) {
+                    constexpr int kRows = G::kTileRows;
                     const int T0 = chunk0 * kChunk;
-                    const bool no_new = !fused || T0 + kTileRows <= new_lo || T0 >= seq_len;
+                    const bool no_new = !fused || T0 + kRows <= new_lo || T0 >= seq_len;
                     int j0 = T0;
-                    bool fits = !bhsd || T0 + kTileRows <= p.slots_per_seq;
+                    bool fits = !bhsd || T0 + kRows <= p.slots_per_seq;
                     if (p.kind == ATTN_CACHE_RING) {
                         j0 = T0 % p.slots_per_seq;
-                        fits = j0 + kTileRows <= p.slots_per_seq;
+                        fits = j0 + kRows <= p.slots_per_seq;
                     }
                     const int64_t s00 = (int64_t)bg * p.slots_per_seq + j0;
-                    if (no_new && fits && s00 + kTileRows <= p.num_slots) {
+                    if (no_new && fits && s00 + kRows <= p.num_slots) {
                         if (lane == 0) info_whole[st] = 1;
-                        if (lane < kWarps) {
-                            info_t0[st * kWarps + lane] = T0 + lane * kChunk;
-                            info_mask[st * kWarps + lane] = 0xFFFFu;
+                        if (lane < kCPT) {
+                            info_t0[st * kCPT + lane] = T0 + lane * kChunk;
+                            info_mask[st * kCPT + lane] = 0xFFFFu;
                         }
                         if (lane == 0) mbar_expect_tx(&full[st], 2 * G::kTileBytes);
                         __syncwarp();
@@ -704,8 +713,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 }
                 // head-major: a box must not cross the end of its block
                 if (bhsd && slot0 >= 0 && slot0 % p.place.rows + kChunk > p.place.rows) slot0 = -2;
-                if (lane < kWarps && slot0 == -1 && t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
-                const unsigned lanes = (1u << kWarps) - 1;
+                if (lane < kCPT && slot0 == -1 && t0 < seq_len) report_error(p.err, ATTN_ERR_BOUNDS);
+                const unsigned lanes = (1u << kCPT) - 1;
                 const unsigned boxed = __ballot_sync(0xffffffffu, slot0 >= -1) & lanes;
                 const unsigned gathered = __ballot_sync(0xffffffffu, slot0 == -2) & lanes;
                 const int64_t slot00 = __shfl_sync(0xffffffffu, slot0, 0);
@@ -713,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 // 64 columns; otherwise each boxed chunk is a 16-row box
                 const bool whole_tile =
                     __all_sync(0xffffffffu, slot0 == slot00 + (int64_t)c * kChunk) && slot00 >= 0 &&
-                    (!bhsd || slot00 % p.place.rows + kTileRows <= p.place.rows);
+                    (!bhsd || slot00 % p.place.rows + G::kTileRows <= p.place.rows);
                 // gathered chunks: lane l copies row l % 16 of K (l < 16) or V
                 uint32_t gmask = 0;
                 bool issued_cp = false;
@@ -741,14 +750,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD * G::kElem / 16; ++c16)
                         cp_async_16_hint(dst + chunk_base<G::kHalves>(false, gc) +
-                                        piece_offset(half_stride(false), r, c16),
+                                        piece_offset(half_stride<G::kTileRows>(false), r, c16),
                                     src + c16 * 16, kv_policy);
                     issued_cp = true;
                 }
                 if (lane == 0) info_whole[st] = whole_tile ? 1 : 0;
-                if (lane < kWarps) {
-                    info_t0[st * kWarps + lane] = slot0 == -3 ? -1 : t0;
-                    info_mask[st * kWarps + lane] =
+                if (lane < kCPT) {
+                    info_t0[st * kCPT + lane] = slot0 == -3 ? -1 : t0;
+                    info_mask[st * kCPT + lane] =
                         slot0 >= 0 ? 0xFFFFu : (slot0 == -1 ? 0u : gmask);
                 }
                 const uint32_t tma_bytes = __popc(boxed) * 2 * G::kChunkBytes;
@@ -769,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                                              (int)slot00, sg.kvh * G::kHalves, &full[st],
                                              kv_policy);
                     }
-                } else if (lane < kWarps && slot0 >= -1) {
+                } else if (lane < kCPT && slot0 >= -1) {
                     const uint32_t off = chunk_base<G::kHalves>(false, lane);
                     if (bhsd) {
                         // an out-of-range page aims above row 0: zero-filled
@@ -862,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         const int seq_len = tb.seqlen[b];
         const int ring_lo = p.kind == ATTN_CACHE_RING ? seq_len - p.slots_per_seq : 0;
         const int window = p.window;
-        const int n_tiles = (sg.c_end - sg.c_begin + kWarps - 1) / kWarps;
+        const int n_tiles = (sg.c_end - sg.c_begin + kCPT - 1) / kCPT;
         // the stage of the segment's last tile: its consumers keep it until
         // the warps' states have been merged through it
         const int st_last = (tile + n_tiles - 1) % kStages;
@@ -871,11 +880,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
             if constexpr (!G::kParkInStage) {
                 return mo + ((size_t)w * RB + row) * HD;
             } else {
+                // pieces: (chunk of the warp, K / V, half) of 16 x 128 B each
                 constexpr int kRowsPerPiece = kChunk * 128 / (HD * 4);
                 const int piece = row / kRowsPerPiece;
-                const int tensor = piece / G::kHalves, h = piece - tensor * G::kHalves;
+                const int sub = piece / (2 * G::kHalves), rest = piece - sub * 2 * G::kHalves;
+                const int tensor = rest / G::kHalves, h = rest - tensor * G::kHalves;
                 uint8_t *base = stages + st_last * G::kStageBytes + tensor * G::kTileBytes +
-                                chunk_base<G::kHalves>(wl, w) + h * half_stride(wl);
+                                chunk_base<G::kHalves>(wl, w + sub * kWarps) +
+                                h * half_stride<G::kTileRows>(wl);
                 return reinterpret_cast<float *>(base + (row - piece * kRowsPerPiece) * HD * 4);
             }
         };
@@ -936,13 +948,16 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
                 __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
                 if (!ok) break;
-                const int t0 = info_t0[st * kWarps + warp];
+#pragma unroll 1
+                for (int sub = 0; sub < G::kSubs; ++sub) {  // this warp's chunks of the tile
+                const int ci = warp + sub * kWarps;
+                const int t0 = info_t0[st * kCPT + ci];
                 if (t0 >= 0) {
-                    const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const uint32_t mask16 = info_mask[st * kCPT + ci];
                     const bool whole = info_whole[st] != 0;
-                    const uint32_t hs = half_stride(whole);
+                    const uint32_t hs = half_stride<G::kTileRows>(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, warp);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, ci);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
                         // new keys of the step, gathered unrotated from k_new:
@@ -1075,6 +1090,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                     }
                     }
                 }
+                }  // sub
                 __syncwarp();
                 if (lane == 0 && it + 1 < n_tiles) mbar_arrive(&empty[st]);
             }
@@ -1177,13 +1193,16 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 ok = mbar_wait(&full[st], (tile / kStages) & 1, p.err);
                 __syncwarp();  // reconverge before the warp-collective ldmatrix / mma
                 if (!ok) break;
-                const int t0 = info_t0[st * kWarps + warp];
+#pragma unroll 1
+                for (int sub = 0; sub < G::kSubs; ++sub) {  // this warp's chunks of the tile
+                const int ci = warp + sub * kWarps;
+                const int t0 = info_t0[st * kCPT + ci];
                 if (t0 >= 0) {
-                    const uint32_t mask16 = info_mask[st * kWarps + warp];
+                    const uint32_t mask16 = info_mask[st * kCPT + ci];
                     const bool whole = info_whole[st] != 0;
-                    const uint32_t hs = half_stride(whole);
+                    const uint32_t hs = half_stride<G::kTileRows>(whole);
                     const uint32_t kbase =
-                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, warp);
+                        smem_u32(stages + st * G::kStageBytes) + chunk_base<G::kHalves>(whole, ci);
                     const uint32_t vbase = kbase + G::kTileBytes;
                     if (rope && t0 + kChunk > seq_len - p.q_rows && t0 < seq_len) {
                         // new keys of the step, gathered unrotated from k_new:
@@ -1339,6 +1358,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                         }
                     }
                 }
+                }  // sub
                 __syncwarp();
                 if (lane == 0 && it + 1 < n_tiles) mbar_arrive(&empty[st]);
             }
@@ -1710,13 +1730,15 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
     const int halves = plan.head_dim * esize / 128;
     const uint32_t cols = 128 / esize;
     const KvPlace place = kv_place(cache, n_kv_heads, plan.head_dim, esize);
+    // rows of a whole-tile box: 64 keys (bf16), 128 (E4M3, whose tiles hold 8 chunks)
+    const uint32_t tile_rows = fp8 ? 2 * dec::kTileRows : dec::kTileRows;
     CUtensorMap tk, tv, tk64, tv64;
     bool maps_ok;
     if (place.rows == 0) {
         const uint64_t dims[3] = {cols, (uint64_t)cache->num_slots, (uint64_t)n_kv_heads * halves};
         const uint64_t strides[2] = {(uint64_t)n_kv_heads * plan.head_dim * esize, 128};
         const uint32_t box[3] = {cols, (uint32_t)dec::kChunk, (uint32_t)halves};
-        const uint32_t box64[3] = {cols, (uint32_t)dec::kTileRows, (uint32_t)halves};
+        const uint32_t box64[3] = {cols, tile_rows, (uint32_t)halves};
         maps_ok = encode_tensor_map(&tk, cache->k, 3, dims, strides, box, true, fp8) &&
                   encode_tensor_map(&tv, cache->v, 3, dims, strides, box, true, fp8) &&
                   encode_tensor_map(&tk64, cache->k, 3, dims, strides, box64, true, fp8) &&
@@ -1732,7 +1754,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                                   (uint64_t)(cache->num_slots / place.rows) * n_kv_heads};
         const uint64_t strides[3] = {row_bytes, 128, rows * row_bytes};
         const uint32_t r16 = (uint32_t)std::min<uint64_t>(rows, dec::kChunk);
-        const uint32_t r64 = (uint32_t)std::min<uint64_t>(rows, dec::kTileRows);
+        const uint32_t r64 = (uint32_t)std::min<uint64_t>(rows, tile_rows);
         const uint32_t box[4] = {cols, r16, (uint32_t)halves, 1};
         const uint32_t box64[4] = {cols, r64, (uint32_t)halves, 1};
         maps_ok = encode_tensor_map(&tk, cache->k, 4, dims, strides, box, true, fp8) &&
