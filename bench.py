@@ -432,8 +432,8 @@ class DecodeOnlyWorkload(Workload):
         self.out = torch.empty_like(base.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
-        # fused append + decode (bf16), or append then decode (FP8)
-        self.launches_per_step = (2 if self.fp8 else 1) + merge_kernel_launched(
+        # the step's append fused into the decode launch (bf16 and FP8)
+        self.launches_per_step = 1 + merge_kernel_launched(
             self.max_seq, base.window, base.q_rows,
             base.slots_per_seq if base.kind == synth.RING else None)
         # valid keys per (request, row) summed over rows' union per request
@@ -475,16 +475,10 @@ class DecodeOnlyWorkload(Workload):
         c = self.case
         for layer in range(self.layers):
             cache = self.caches[(s * self.layers + layer) % self.ncopy]
-            if self.fp8:
-                self.gq.attn_kv_append(c.k_new, c.v_new, c.slot_mapping, cache, err=self.err)
-                self.gq.attn_decode(c.q, cache, c.seq_lens, c.positions, self.max_seq,
-                                    c.window, c.scale, out=self.out, workspace=self.ws,
-                                    err=self.err)
-            else:
-                self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
-                                           c.seq_lens, c.positions, self.max_seq, c.window,
-                                           c.scale, out=self.out, workspace=self.ws,
-                                           err=self.err, tables_early=True)
+            self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
+                                       c.seq_lens, c.positions, self.max_seq, c.window,
+                                       c.scale, out=self.out, workspace=self.ws,
+                                       err=self.err, tables_early=True)
 
     def capture(self, stream, e2e=False):
         torch = self.torch

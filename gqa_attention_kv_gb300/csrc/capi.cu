@@ -233,7 +233,11 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
     if (rc != ATTN_OK) return rc;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
     if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return ATTN_ERR_UNSUPPORTED;
-    if (cache->dtype != ATTN_KV_BF16) return ATTN_ERR_UNSUPPORTED;
+    // FP8 caches: the rows are encoded as attn_kv_append encodes them; the
+    // rotary embedding is not combined with them here
+    if (cache->dtype == ATTN_KV_FP8_E4M3 && rope_inv_freq) return ATTN_ERR_UNSUPPORTED;
+    if (cache->dtype == ATTN_KV_FP8_E4M3 && cache->k_ref && !aligned16(cache->k_ref))
+        return ATTN_ERR_ALIGN;
     if (batch == 0) return ATTN_OK;
     if (!q || !k_new || !v_new || !slot_mapping || !seq_lens || !positions || !out ||
         !cache->k || !cache->v)

@@ -104,6 +104,7 @@ struct Params {
     const __nv_bfloat16 *v_new;
     const int64_t *slot_mapping;
     const float *rope_inv_freq;  // [HD / 2] (nullptr: no rotary embedding)
+    const float *k_ref;          // FP8 fused append: the cache's key reference [Hkv][HD], or nullptr
     // seq_lens, positions and block_table may be read before the previous
     // kernel completes (ATTN_DECODE_TABLES_EARLY)
     bool tables_early;
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         const int64_t num_pages = paged ? p.num_slots / p.block_size : 0;
         const bool bhsd = p.place.rows != 0;  // head-major: boxes stay inside one block
         const int c = lane & (kCPT - 1);
-        const bool fused = !FP8 && p.k_new != nullptr;
+        const bool fused = p.k_new != nullptr;
         const uint64_t kv_policy = l2_policy_evict_first();  // every K/V byte is read once
         SegmentWalker walk{g0, g1, L};
         Segment sg;
@@ -725,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                     (!bhsd || slot00 % p.place.rows + G::kTileRows <= p.place.rows);
                 // gathered chunks: lane l copies row l % 16 of K (l < 16) or V
                 uint32_t gmask = 0;
-                bool issued_cp = false;
+                bool issued_cp = false, issued_st = false;
                 for (unsigned bits = gathered; bits; bits &= bits - 1) {
                     const int gc = __ffs(bits) - 1;
                     const int gt0 = (chunk0 + gc) * kChunk;
@@ -747,12 +748,63 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                                : reinterpret_cast<const uint8_t *>(tensor ? p.v_cache : p.k_cache) +
                                      p.place.head_offset(s < 0 ? 0 : s, sg.kvh);
                     uint8_t *dst = tensor ? vst : kst;
+                    if (FP8 && is_new) continue;  // encoded below, a piece per lane
 #pragma unroll 4
                     for (int c16 = 0; c16 < HD * G::kElem / 16; ++c16)
                         cp_async_16_hint(dst + chunk_base<G::kHalves>(false, gc) +
                                         piece_offset(half_stride<G::kTileRows>(false), r, c16),
                                     src + c16 * 16, kv_policy);
                     issued_cp = true;
+                }
+                if (FP8 && fused) {
+                    // E4M3 cache: the step's new rows of the gathered chunks are
+                    // encoded on the way in, as the FP8 append encodes them (K minus
+                    // the reference, the difference in fp32; nearest even,
+                    // saturating): one 16-element piece of one row per lane
+                    for (unsigned bits = gathered; bits; bits &= bits - 1) {
+                        const int gc = __ffs(bits) - 1;
+                        const int gt0 = (chunk0 + gc) * kChunk;
+                        const int n0 = max(gt0, new_lo), n1 = min(gt0 + kChunk, seq_len);
+                        constexpr int kPieces = HD / 16;
+                        for (int task = lane; task < max(0, n1 - n0) * 2 * kPieces; task += 32) {
+                            const int pc = task % kPieces, tr = task / kPieces;
+                            const int tensor = tr & 1, t = n0 + (tr >> 1);
+                            const uint4 *src = reinterpret_cast<const uint4 *>(
+                                (tensor ? p.v_new : p.k_new) +
+                                ((int64_t)(sg.b * p.q_rows + (t - new_lo)) * p.n_kv_heads + sg.kvh) *
+                                    HD + pc * 16);
+                            const uint4 a = __ldg(src), b = __ldg(src + 1);
+                            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                            float x[16];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                x[2 * i] = __uint_as_float(w[i] << 16);
+                                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                            }
+                            if (tensor == 0 && p.k_ref) {
+                                const float4 *r4 =
+                                    reinterpret_cast<const float4 *>(p.k_ref + sg.kvh * HD + pc * 16);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 rv = __ldg(r4 + i);
+                                    x[4 * i] = __fsub_rn(x[4 * i], rv.x);
+                                    x[4 * i + 1] = __fsub_rn(x[4 * i + 1], rv.y);
+                                    x[4 * i + 2] = __fsub_rn(x[4 * i + 2], rv.z);
+                                    x[4 * i + 3] = __fsub_rn(x[4 * i + 3], rv.w);
+                                }
+                            }
+                            uint32_t code[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                code[i] = f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1]) |
+                                          (f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]) << 16);
+                            *reinterpret_cast<uint4 *>(
+                                (tensor ? vst : kst) + chunk_base<G::kHalves>(false, gc) +
+                                piece_offset(half_stride<G::kTileRows>(false), t - gt0, pc)) =
+                                make_uint4(code[0], code[1], code[2], code[3]);
+                            issued_st = true;
+                        }
+                    }
                 }
                 if (lane == 0) info_whole[st] = whole_tile ? 1 : 0;
                 if (lane < kCPT) {
@@ -796,10 +848,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                     }
                 }
                 __syncwarp();
-                if (issued_cp)
+                if (issued_cp && !issued_st) {
                     cp_async_arrive_noinc(&full[st]);
-                else
+                } else {
+                    // rows stored by this thread itself are published by a
+                    // release arrive (after its own copies, if any, have landed)
+                    if (issued_cp) asm volatile("cp.async.wait_all;" ::: "memory");
                     mbar_arrive(&full[st]);
+                }
             }
         }
         // the gathered rows of this thread must land before it leaves
@@ -815,6 +871,47 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     if (rope) {
         for (int i = ctid; i < HD / 2; i += kWarps * 32) rope_if[i] = p.rope_inv_freq[i];
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    }
+    if (FP8 && p.k_new != nullptr) {
+        // fused append into an E4M3 cache: each thread encodes 16 elements of
+        // a row into one 16-byte piece, as the FP8 append does
+        const int pieces = p.n_kv_heads * HD / 16;  // of one row of one tensor
+        const int64_t total = (int64_t)p.batch * p.q_rows * pieces * 2;
+        for (int64_t idx = (int64_t)blockIdx.x * (kWarps * 32) + ctid; idx < total;
+             idx += (int64_t)p.grid * (kWarps * 32)) {
+            const int64_t row = idx / (2 * pieces);
+            const int rem = (int)(idx - row * 2 * pieces);
+            const int tensor = rem / pieces, pc = rem - tensor * pieces;
+            const int64_t slot = p.slot_mapping[row];
+            if (slot < 0 || slot >= p.num_slots) {
+                if (rem == 0) report_error(p.err, ATTN_ERR_BOUNDS);
+                continue;
+            }
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(tensor ? p.v_new : p.k_new) + (row * pieces + pc) * 2;
+            const uint4 a = __ldg(src), b = __ldg(src + 1);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[2 * i] = __uint_as_float(w[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+            if (tensor == 0 && p.k_ref) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], __ldg(p.k_ref + pc * 16 + i));
+            }
+            uint32_t code[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                code[i] = f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1]) |
+                          (f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]) << 16);
+            const int h = pc / (HD / 16), pp = pc - h * (HD / 16);
+            uint8_t *dst = reinterpret_cast<uint8_t *>(
+                               const_cast<__nv_bfloat16 *>(tensor ? p.v_cache : p.k_cache)) +
+                           p.place.head_offset(slot, h) + pp * 16;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(code[0], code[1], code[2], code[3]);
+        }
     }
     if (!FP8 && p.k_new != nullptr) {
         // fused append: the step's rows into their cache slots, for later
@@ -1791,6 +1888,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.v_new = v_new ? static_cast<const __nv_bfloat16 *>(v_new) + new_off : nullptr;
         p.slot_mapping = slot_mapping ? slot_mapping + (int64_t)b0 * q_rows : nullptr;
         p.rope_inv_freq = rope_inv_freq;
+        p.k_ref = fp8 ? cache->k_ref : nullptr;
         p.tables_early = tables_early;
         p.batch = nb;
         p.b_base = b0;

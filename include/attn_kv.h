@@ -272,8 +272,9 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *                  under programmatic dependent launch.  Everything else is
  *                  still read after it completes.
  *   Every other argument, the workspace and the statuses are attn_decode's.
- *   An FP8 cache returns ATTN_ERR_UNSUPPORTED: append with attn_kv_append,
- *   then call attn_decode.
+ *   An FP8 cache receives the rows encoded exactly as attn_kv_append encodes
+ *   them (K minus k_ref), and the decode reads those codes; rope_inv_freq must
+ *   then be NULL (ATTN_ERR_UNSUPPORTED otherwise).
  */
 #define ATTN_DECODE_TABLES_EARLY 1u
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,

@@ -169,7 +169,8 @@ def test_decode_append_validation(lib):
 
 
 def test_fp8_cache_validation(lib):
-    """FP8 caches: head_dim 128 only, no fused append yet, an aligned k_ref;
+    """FP8 caches: head_dim 128 only, no rotary embedding in the fused append,
+    an aligned k_ref;
     an unknown dtype is refused."""
     fp8 = gq.ATTN_KV_FP8_E4M3
     assert decode_rc(lib, cache(dtype=fp8, D=64), D=64) == gq.ATTN_ERR_UNSUPPORTED
@@ -186,7 +187,8 @@ def test_fp8_cache_validation(lib):
     assert f(16, 32, 48, 4, ctypes.byref(cs), 8, 64, None, None) == gq.ATTN_ERR_UNSUPPORTED
     cs = cache(dtype=fp8, slots=4096 * 4, sps=4096).struct()
     need = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 32, 8, 128, 4096, 0)
-    assert lib.attn_decode_append(16, 32, 48, 64, None, ctypes.byref(cs), 80, 96, 2, 1, 4096,
+    # the fused append takes FP8 caches, but not with the rotary embedding
+    assert lib.attn_decode_append(16, 32, 48, 64, 128, ctypes.byref(cs), 80, 96, 2, 1, 4096,
                                   0, 32, 8, 128, 0.1, 112, 1 << 20, need, None, 0,
                                   None) == gq.ATTN_ERR_UNSUPPORTED
 

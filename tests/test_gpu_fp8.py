@@ -250,3 +250,50 @@ def test_fp8_batch_split_over_launches():
 def test_fp8_one_unit_over_many_ctas():
     case = synth.decode_case(9102, LINEAR, 1, 1, 8, 1, 128, [16000])
     check_case(case, where="fp8 one unit, 16000 keys")
+
+
+@pytest.mark.parametrize("kind,B,R,Hq,Hkv,seq,extra", [
+    (LINEAR, 3, 1, 28, 4, [513, 1, 4097], {}),
+    (PAGED, 4, 4, 32, 8, [64, 100, 1030, 17], {"block_size": 16}),
+    (PAGED, 3, 2, 16, 4, [37, 300, 129], {"block_size": 5, "num_blocks": 200}),
+    (RING, 4, 1, 32, 8, [9000, 300, 16390, 8193], {"window": 8192, "ring": 16384}),
+])
+@pytest.mark.parametrize("with_ref", [False, True])
+def test_fp8_fused_append_equals_append_then_decode(kind, B, R, Hq, Hkv, seq, extra, with_ref):
+    """attn_decode_append over an FP8 cache encodes the step's rows on the way
+    into the decode and into the cache: same codes and same output bits as
+    the FP8 append followed by the decode, and the oracle's result."""
+    case = synth.decode_case(9200 + B * R + int(kind), kind, B, R, Hq, Hkv, 128, seq, **extra)
+    ref = (np.random.default_rng(B).standard_normal((Hkv, 128)) * 3).astype(np.float32) \
+        if with_ref else None
+    kc, vc = fp8_codes(case.k_cache, case.v_cache, ref)
+    want, kc2, vc2 = oracle_fp8_step(case, kc, vc, ref)
+    out_u, cache_u = gpu_fp8_step(case, kc, vc, ref)
+    cache = gq.KVCache(case.kind, torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV),
+                       slots_per_seq=case.slots_per_seq,
+                       block_table=None if case.block_table is None else case.block_table.to(DEV),
+                       block_size=case.block_size, dtype=FP8,
+                       k_ref=None if ref is None else torch.from_numpy(ref).to(DEV))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out_f = gq.attn_decode_append(case.q.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV),
+                                  case.slot_mapping.to(DEV), cache, case.seq_lens.to(DEV),
+                                  case.positions.to(DEV), case.max_seq_len(), case.window,
+                                  case.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(cache.k.cpu().numpy(), kc2) and np.array_equal(cache.v.cpu().numpy(), vc2)
+    assert torch.equal(out_f, out_u), "fused and two-launch FP8 results differ"
+    compare(out_f, want, f"fp8 fused {kind}")
+
+
+def test_fp8_fused_append_refuses_rope():
+    case = synth.decode_case(9300, LINEAR, 1, 1, 8, 2, 128, [40])
+    kc, vc = fp8_codes(case.k_cache, case.v_cache)
+    cache = gq.KVCache(LINEAR, torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV),
+                       slots_per_seq=case.slots_per_seq, dtype=FP8)
+    inv = torch.ones(64, dtype=torch.float32, device=DEV)
+    with pytest.raises(gq.AttnError) as e:
+        gq.attn_decode_append(case.q.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV),
+                              case.slot_mapping.to(DEV), cache, case.seq_lens.to(DEV),
+                              case.positions.to(DEV), 40, 0, case.scale, rope_inv_freq=inv)
+    assert e.value.status == gq.ATTN_ERR_UNSUPPORTED
