@@ -22,22 +22,24 @@
 //     to the output; the others leave fp32 partial states in the workspace
 //     and are merged by the CTAs that store the last ones (atomic counters
 //     tell them): parts in CTA order, eight at a time, then those groups'
-//     states in order.  One launch.
-//   * A producer warp streams 64-key tiles (four 16-key chunks).  A tile
-//     whose 64 slots are consecutive (linear cache; a ring away from its wrap
-//     point) is one TMA box of 64 rows per tensor; otherwise a chunk whose 16
-//     slots are consecutive (a page of >= 16 slots) is a 16-row box; any
-//     other chunk is gathered row by row with 16-byte cp.async.  Boxes are
-//     3D, {64 columns, rows, halves of the head}, so one box brings a whole
-//     head row; they land 128-byte-swizzled.  Page ids are fetched 32 at a time, one
-//     per lane, ahead of the tiles that use them.
-//   * Four consumer warps each own one chunk of every tile: S = Q K^T and
-//     O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-//     accumulate), the mask and online softmax in fp32 registers with quad
-//     shuffles, exp2 with log2(e) folded into the scale.  P enters P V as two
-//     bf16 halves, hi + lo (vibevoice.c, "Attention backends": one rounding
-//     of P is too coarse), so P keeps ~16 bits.  At the end of a segment the
-//     four warps merge through shared memory.
+//     states in order.  Launches whose units may span very many CTAs leave
+//     those units to a small merge kernel instead.
+//   * A producer warp streams tiles of 16-key chunks: 64 keys for bf16, 128
+//     for E4M3 (whose rows are half as wide).  A tile whose slots are
+//     consecutive (linear cache; a ring away from its wrap point) is one TMA
+//     box per tensor; otherwise a chunk whose 16 slots are consecutive (a page
+//     of >= 16 slots) is a 16-row box; any other chunk is gathered row by row
+//     with 16-byte cp.async.  Boxes bring whole head rows (128-byte blocks,
+//     the "halves" of a bf16 row of 128) and land 128-byte-swizzled.  Page ids
+//     are fetched 32 at a time, one per lane, ahead of the tiles that use them.
+//   * Four consumer warps each own one chunk (two for E4M3) of every tile:
+//     S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16, bf16 in
+//     -- f16 for E4M3 caches, converted in registers -- fp32 accumulate), the
+//     mask and online softmax in fp32 registers with quad shuffles, exp2 with
+//     log2(e) folded into the scale.  For bf16 caches P enters P V as two bf16
+//     halves, hi + lo (vibevoice.c, "Attention backends": one rounding of P is
+//     too coarse), so P keeps ~16 bits; for E4M3 one f16 rounding (11 bits).
+//     At the end of a segment the four warps merge through shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -202,10 +204,11 @@ __device__ __forceinline__ uint32_t rope_pair(uint32_t w, int pos, float inv_fre
     return pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
 }
 
-// A stage holds the K and V of one 64-key tile, each in one of two
-// 128-byte-swizzled layouts (an 8-row group always spans 1024 aligned bytes):
-//   whole tile (one TMA box of 64 rows): [half][64 rows][128 B]
-//   chunked    (16-row boxes / rows)   : [chunk][half][16 rows][128 B]
+// A stage holds the K and V of one tile (64 keys bf16, 128 keys E4M3), each in
+// one of two 128-byte-swizzled layouts (an 8-row group always spans 1024
+// aligned bytes):
+//   whole tile (one TMA box of all rows): [half][tile rows][128 B]
+//   chunked    (16-row boxes / rows)    : [chunk][half][16 rows][128 B]
 // Chunk c's rows start at chunk_base() and its halves are half_stride() apart.
 template <int HALVES>
 __device__ __forceinline__ uint32_t chunk_base(bool whole, int c) {
@@ -719,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 const unsigned boxed = __ballot_sync(0xffffffffu, slot0 >= -1) & lanes;
                 const unsigned gathered = __ballot_sync(0xffffffffu, slot0 == -2) & lanes;
                 const int64_t slot00 = __shfl_sync(0xffffffffu, slot0, 0);
-                // a tile whose 64 slots are consecutive is one 64-row box per
-                // 64 columns; otherwise each boxed chunk is a 16-row box
+                // a tile whose slots are consecutive is one box per tensor;
+                // otherwise each boxed chunk is a 16-row box
                 const bool whole_tile =
                     __all_sync(0xffffffffu, slot0 == slot00 + (int64_t)c * kChunk) && slot00 >= 0 &&
                     (!bhsd || slot00 % p.place.rows + G::kTileRows <= p.place.rows);
