@@ -670,6 +670,59 @@ def cpu_sample(workload_name, steps=1, warmup=0, budget_s=None, max_rows=160):
     return res
 
 
+def dist_env():
+    """(rank, local_rank, world_size) as torchrun exports them (1 process: 0, 0, 1)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+class Replicas:
+    """The N-GPU run: one process per GPU, each running the whole workload on
+    its own GPU with nothing crossing between them (the decode and prefill
+    units are independent, so the library has no exchange step; this is the
+    only multi-GPU form the path has).  It supplies the bench's barrier, the
+    max over ranks of each time, and the whole-job value: the units all ranks
+    processed over the slowest rank's time."""
+
+    def __init__(self, world, backend="nccl", device=None):
+        self.world, self.device = world, device
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        import torch
+
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        if self.device is not None and self.device.type == "cuda":
+            torch.cuda.synchronize()
+
+    def reduce_max(self, x):
+        if self.world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def whole_job_rate(self, units_per_rank, seconds):
+        """Aggregate throughput: every rank processed units_per_rank in at
+        most `seconds` (already the max over ranks)."""
+        return self.world * units_per_rank / seconds
+
+    def close(self):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -687,9 +740,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, local_rank, world = dist_env()
     peaks, peak_src = load_peaks()
     metric = "decode-attn KV GB/s (% of HBM peak); prefill-attn TFLOP/s (% bf16 peak)"
 
@@ -719,23 +770,13 @@ def main():
 
     build.build()
     gq.lib()
-    if world > 1:
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
     dev = torch.device("cuda", local_rank if world > 1 else 0)
     torch.cuda.set_device(dev)
+    reps = Replicas(world, "nccl", dev)
     wl = make_workload(args.workload, dev, 1 if args.layout == "bhsd" else 0)
     stream = torch.cuda.Stream(device=dev)
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-
-            dist.barrier()
-        torch.cuda.synchronize()
-
+    barrier = reps.barrier
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier()
     clocks.start()
@@ -746,15 +787,7 @@ def main():
     if err != 0:
         raise SystemExit(f"device error word {err} ({gq.attn_status_string(err)})")
 
-    def reduce_max(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
+    reduce_max = reps.reduce_max
     K = args.steps
     total_ms = reduce_max(total_ms)
     dec_ms = reduce_max(groups.get("decode", 0.0))
@@ -762,8 +795,8 @@ def main():
     app_ms = reduce_max(groups.get("prompt_append", 0.0))
     dbytes = wl.decode_bytes_per_step()
     pflops = wl.prefill_flops_per_step()
-    dec_gbs = world * dbytes * K / (dec_ms / 1e3) / 1e9 if dec_ms > 0 else None
-    pre_tf = world * pflops * K / (pre_ms / 1e3) / 1e12 if pre_ms > 0 else None
+    dec_gbs = reps.whole_job_rate(dbytes * K, dec_ms / 1e3) / 1e9 if dec_ms > 0 else None
+    pre_tf = reps.whole_job_rate(pflops * K, pre_ms / 1e3) / 1e12 if pre_ms > 0 else None
 
     e2e = None
     if not args.no_e2e and hasattr(wl, "run_step_e2e"):
@@ -780,10 +813,7 @@ def main():
                "ms_per_step": round(reduce_max(etot) / K, 4)}
 
     if rank != 0:
-        if world > 1:
-            import torch.distributed as dist
-
-            dist.destroy_process_group()
+        reps.close()
         return 0
 
     if pre_tf is not None:
@@ -849,10 +879,7 @@ def main():
                                 "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
                                 "prefill_tflops": round(r["prefill_tflops"], 6)}
     print(json.dumps(line))
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+    reps.close()
     return 0
 
 
