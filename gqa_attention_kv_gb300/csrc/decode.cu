@@ -97,7 +97,6 @@ struct Params {
     float *ws_lse;
     int32_t *ws_count;   // per unit: merged groups so far (zero between calls)
     int32_t *ws_gcount;  // per partial slot that starts a group: parts stored so far
-    int2 *ws_parts;      // per unit: (first, last) CTA of its chunks; (0, -1) if it has none
     KvPlace place;       // where a head's row of a slot lives (slot-major or head-major)
     bool merge_kernel;   // units of more than kGroupParts parts go to the merge kernel
     // fused append (nullptr: none): the step's rows, bf16 [batch * q_rows][n_kv_heads][HD],
@@ -273,6 +272,47 @@ __device__ __forceinline__ void unit_range(const Params &p, int b, int rb, int &
 struct Tables {
     int *cnt, *clo, *seqlen, *Pb;
 };
+
+// Builds the tables every CTA of a launch computes alike: each (request, row
+// block)'s chunk count and first chunk, each request's effective seq_len, and
+// the prefix Pb.  All nthreads threads of the block take part; ends with a
+// block barrier.  report: this block reports out-of-range seq_lens.
+__device__ __forceinline__ void build_tables(const Params &p, const Tables &tb, int nthreads,
+                                             bool report) {
+    const int B = p.batch, RBc = p.row_blocks;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < B * RBc; i += nthreads) {
+        const int b = i / RBc, rb = i - (i / RBc) * RBc;
+        int clo, chi, sl;
+        unit_range(p, b, rb, clo, chi, sl, report && rb == 0);
+        tb.cnt[i] = chi - clo;
+        tb.clo[i] = clo;
+        if (rb == 0) tb.seqlen[b] = sl;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        if (lane == 0) tb.Pb[0] = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int b = base + lane;
+            int v = 0;
+            if (b < B)
+                for (int rb = 0; rb < RBc; ++rb) {
+                    const int n = tb.cnt[b * RBc + rb];
+                    v += n > 0 ? n + kUnitGapChunks : 0;
+                }
+            v *= p.n_kv_heads;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += n;
+            }
+            if (b < B) tb.Pb[b + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+}
 
 // One contiguous piece of one unit's chunks handled by this CTA.
 struct Segment {
@@ -468,37 +508,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
 
     // ---- tables: chunk counts of every (request, row block), then Pb
     const int B = p.batch, RBc = p.row_blocks;
-    for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
-        const int b = i / RBc, rb = i - (i / RBc) * RBc;
-        int clo, chi, sl;
-        unit_range(p, b, rb, clo, chi, sl, blockIdx.x == 0 && rb == 0);
-        tb.cnt[i] = chi - clo;
-        tb.clo[i] = clo;
-        if (rb == 0) tb.seqlen[b] = sl;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        if (lane == 0) tb.Pb[0] = 0;
-        for (int base = 0; base < B; base += 32) {
-            const int b = base + lane;
-            int v = 0;
-            if (b < B)
-                for (int rb = 0; rb < RBc; ++rb) {
-                    const int n = tb.cnt[b * RBc + rb];
-                    v += n > 0 ? n + kUnitGapChunks : 0;
-                }
-            v *= p.n_kv_heads;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += n;
-            }
-            if (b < B) tb.Pb[b + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-    }
-    __syncthreads();
+    build_tables(p, tb, kThreads, blockIdx.x == 0);
     const int N = tb.Pb[B];
     // equal shares, but at least kMinChunksPerCta so small problems do not
     // spread a few keys over every SM
@@ -546,8 +556,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
             if (tb.cnt[i] != 0) continue;
             const int b = i / RBc, rb = i - (i / RBc) * RBc;
-            for (int kvh = 0; kvh < p.n_kv_heads; ++kvh)
-                p.ws_parts[(b * p.n_kv_heads + kvh) * RBc + rb] = make_int2(0, -1);
             for (int row = rb * RB; row < min(p.rows, (rb + 1) * RB); ++row) {
                 const int r = row / p.group, g = row - r * p.group;
                 for (int kvh = 0; kvh < p.n_kv_heads; ++kvh) {
@@ -964,8 +972,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     int n_pend = 0;
     while (ok && walk.next(p, tb, sg)) {
         const int b = sg.b, kvh = sg.kvh;
-        if (sg.head && ctid == 0)  // for the merge kernel: the CTAs holding the unit
-            p.ws_parts[sg.unit] = make_int2(sg.first, sg.last);
         const int row0 = sg.rb * RB;
         const int row1 = min(p.rows, row0 + RB);
         const int seq_len = tb.seqlen[b];
@@ -1645,8 +1651,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     constexpr int PER = HD / 32;
     __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
     __shared__ __align__(16) float sm_o[kMergeWarps][HD];
-    pdl_wait();  // the partial states and tables come from the split kernel
-    pdl_launch_dependents();
+    __shared__ int t_cnt[kMaxTableEntries], t_clo[kMaxTableEntries], t_seq[kMaxTableEntries],
+        t_pb[kMaxTableEntries + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const int b = cta / (p.rows * p.n_kv_heads);
@@ -1655,8 +1661,31 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int i = rem - kvh * p.rows;
     const int rb = i / RB, row = i - rb * RB;
     const int unit = (b * p.n_kv_heads + kvh) * p.row_blocks + rb;
-    const int2 parts = __ldcg(p.ws_parts + unit);
-    const int first = parts.x, last = parts.y;
+    // The CTAs that hold the unit, from the split kernel's own tables: this
+    // kernel's predecessor is that split kernel, which releases it only after
+    // waiting for its own predecessor, so seq_lens and positions are final and
+    // the tables can be built while the split kernel is still running.
+    const Tables tb{t_cnt, t_clo, t_seq, t_pb};
+    build_tables(p, tb, kMergeWarps * 32, false);
+    int first = 0, last = -1;
+    {
+        const int RBc = p.row_blocks;
+        const int N = tb.Pb[p.batch];
+        const int L = max(kMinChunksPerCta, (N + p.grid - 1) / p.grid);
+        const int n_u = tb.cnt[b * RBc + rb];
+        if (n_u > 0) {
+            const int per_head = (tb.Pb[b + 1] - tb.Pb[b]) / p.n_kv_heads;
+            int start = tb.Pb[b] + kvh * per_head;
+            for (int r = 0; r < rb; ++r) {
+                const int n = tb.cnt[b * RBc + r];
+                start += n > 0 ? n + kUnitGapChunks : 0;
+            }
+            first = start / L;
+            last = (start + n_u - 1) / L;
+        }
+    }
+    pdl_wait();  // the partial states come from the split kernel
+    pdl_launch_dependents();
     // no keys (zero-filled) or few parts (merged by the split kernel)
     if (last - first < kGroupParts) return;
     // Each warp takes parts first + warp + kMergeWarps * k; a batch of kBatch
@@ -1803,8 +1832,7 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
     plan->counter_offset = (partial + 255) & ~size_t(255);
     plan->counter_bytes = (units + slots) * sizeof(int32_t);
-    plan->meta_offset = plan->counter_offset + ((plan->counter_bytes + 255) & ~size_t(255));
-    plan->workspace = plan->meta_offset + units * sizeof(int2);
+    plan->workspace = plan->counter_offset + plan->counter_bytes;
     // How many CTAs can a unit span?  Its chunks are at most the key bound /
     // 16 + 1 and every CTA takes at least kMinChunksPerCta.
     int64_t keys = max_seq_len;
@@ -1913,8 +1941,6 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                  plan.counter_offset);
         p.ws_gcount = p.ws_count + units;
-        p.ws_parts = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) +
-                                              plan.meta_offset);
         p.merge_kernel = plan.merge_kernel;
         p.place = place;
         int rc;

@@ -92,7 +92,6 @@ struct DecodePlan {
     int batch_per_launch;
     size_t workspace;     // bytes of scratch: fp32 partial states + merge counters
     size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
-    size_t meta_offset;   // per unit (first, last) CTA of its chunks, for the merge kernel
     bool merge_kernel;    // units spanning very many CTAs are merged by a second kernel
 };
 
