@@ -165,3 +165,49 @@ def test_bhsd_same_result_as_slot_major():
     a, _ = gpu_decode(case)
     b, _ = run_bhsd(case)
     assert torch.equal(a, b)
+
+
+def test_bhsd_fused_append_with_rope():
+    """Head-major cache, the step's rows rotated and appended by the decode
+    launch: the same cache bits and output bits as the slot-major launch
+    (the layout moves bytes only)."""
+    from helpers import to_device
+
+    case = synth.decode_case(11800, PAGED, 3, 4, 32, 8, 128, [2000, 37, 1503], block_size=16)
+    inv = (10000.0 ** (-torch.arange(0, 64, dtype=torch.float32) / 64)).to(DEV)
+    args = (case.seq_lens.to(DEV), case.positions.to(DEV), case.max_seq_len(), 0, case.scale)
+    slot_major = to_device(case, DEV)
+    a = gq.attn_decode_append(case.q.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV),
+                              case.slot_mapping.to(DEV), slot_major, *args, rope_inv_freq=inv)
+    head_major = device_cache(case, case.k_cache, case.v_cache)
+    b = gq.attn_decode_append(case.q.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV),
+                              case.slot_mapping.to(DEV), head_major, *args, rope_inv_freq=inv)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.equal(from_bhsd(head_major.k).cpu(), slot_major.k.cpu())
+    assert torch.equal(from_bhsd(head_major.v).cpu(), slot_major.v.cpu())
+
+
+def test_bhsd_fp8_fused_append():
+    case = synth.decode_case(11900, LINEAR, 3, 2, 28, 4, 128, [3000, 64, 1029])
+    S, Hkv, D = case.k_cache.shape
+    kc = np.zeros((S, Hkv, D), dtype=np.uint8)
+    vc = np.zeros((S, Hkv, D), dtype=np.uint8)
+    oracle.kv_append_fp8(kc, vc, bits(case.k_cache), bits(case.v_cache), np.arange(S))
+    want_k, want_v = kc.copy(), vc.copy()
+    oracle.kv_append_fp8(want_k, want_v, bits(case.k_new), bits(case.v_new),
+                         case.slot_mapping.numpy())
+    cache = device_cache(case, torch.from_numpy(kc), torch.from_numpy(vc),
+                         dtype=gq.ATTN_KV_FP8_E4M3)
+    out = gq.attn_decode_append(case.q.to(DEV), case.k_new.to(DEV), case.v_new.to(DEV),
+                                case.slot_mapping.to(DEV), cache, case.seq_lens.to(DEV),
+                                case.positions.to(DEV), case.max_seq_len(), 0, case.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_bhsd(cache.k).cpu().numpy(), want_k)
+    assert np.array_equal(from_bhsd(cache.v).cpu().numpy(), want_v)
+    cd = {"kind": LINEAR, "k": oracle.fp8_to_bf16_bits(want_k), "v": oracle.fp8_to_bf16_bits(want_v),
+          "slots_per_seq": case.slots_per_seq}
+    rc, ref = oracle.decode(bits(case.q), cd, case.seq_lens.numpy(), case.positions.numpy(), 0,
+                            case.scale, Hkv)
+    assert rc == 0
+    compare(out, ref, "bhsd fp8 fused")
