@@ -704,6 +704,37 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                         slot0 = (v < 0 || v >= num_pages)
                                     ? -1
                                     : (int64_t)v * p.block_size + t0 % p.block_size;
+                    // Fast path: pages smaller than a tile, every chunk of the
+                    // tile present, on a page in range and without the step's
+                    // new rows: one 16-row box per chunk and tensor, with no
+                    // ballots (head-major coordinates straight from the page id)
+                    const bool plain = chunk < sg.c_end && v >= 0 && v < num_pages &&
+                                       !(fused && t0 + kChunk > new_lo && t0 < seq_len);
+                    if (p.block_size < G::kTileRows && __all_sync(0xffffffffu, plain)) {
+                        if (lane == 0) info_whole[st] = 0;
+                        if (lane < kCPT) {
+                            info_t0[st * kCPT + lane] = t0;
+                            info_mask[st * kCPT + lane] = 0xFFFFu;
+                        }
+                        if (lane == 0) mbar_expect_tx(&full[st], kCPT * 2 * G::kChunkBytes);
+                        __syncwarp();
+                        if (lane < kCPT) {
+                            const uint32_t off = chunk_base<G::kHalves>(false, lane);
+                            if (bhsd) {
+                                const int y = t0 % p.block_size, w = v * p.n_kv_heads + sg.kvh;
+                                tma_load_4d_hint(kst + off, &tm_k, 0, y, 0, w, &full[st], kv_policy);
+                                tma_load_4d_hint(vst + off, &tm_v, 0, y, 0, w, &full[st], kv_policy);
+                            } else {
+                                tma_load_3d_hint(kst + off, &tm_k, 0, (int)slot0, sg.kvh * G::kHalves,
+                                                 &full[st], kv_policy);
+                                tma_load_3d_hint(vst + off, &tm_v, 0, (int)slot0, sg.kvh * G::kHalves,
+                                                 &full[st], kv_policy);
+                            }
+                        }
+                        __syncwarp();
+                        mbar_arrive(&full[st]);
+                        continue;
+                    }
                 }
                 // a chunk holding any of the step's new keys (fused append) is
                 // gathered, the new rows taken from k_new / v_new
