@@ -79,19 +79,6 @@ def prefill_traffic(T):
     return PREFILL_TRAFFIC["bytes"] if h.hexdigest() == PREFILL_TRAFFIC["sha256"] else None
 
 
-def merge_kernel_launched(max_seq_len, window, q_rows, ring):
-    """1 if a decode call also launches the merge kernel: the library's rule
-    (a unit may span more than 128 CTAs of at least 8 chunks of 16 keys)."""
-    keys = max_seq_len
-    if window > 0:
-        keys = min(keys, window + q_rows - 1)
-    if ring:
-        keys = min(keys, ring)
-    max_chunks = (keys + 15) // 16 + 1
-    max_parts = (max_chunks + 7) // 8 + 1
-    return 1 if max_parts > 128 else 0
-
-
 def prefill_flops(T, Hq, D, window=0):
     """4 * D * Hq * (unmasked query-key pairs): QK^T and PV, 2 flops per MAC."""
     if window and window > 0:
@@ -254,10 +241,10 @@ class QwenWorkload(Workload):
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
-        # prefill, prompt append, per decode the split kernel (+ the merge
-        # kernel at these long contexts)
-        self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * (
-            1 + merge_kernel_launched(self.max_seq, 0, 1, None))
+        # prefill, prompt append, per decode the kernels the library plans
+        # (split kernel + merge kernel at these long contexts)
+        self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * gq.attn_decode_kernel_launches(
+            self.caches[0], self.B, 1, Hq, self.max_seq, 0)
         self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",
                          "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D,
                          "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
@@ -433,9 +420,8 @@ class DecodeOnlyWorkload(Workload):
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_i = 0
         # the step's append fused into the decode launch (bf16 and FP8)
-        self.launches_per_step = 1 + merge_kernel_launched(
-            self.max_seq, base.window, base.q_rows,
-            base.slots_per_seq if base.kind == synth.RING else None)
+        self.launches_per_step = gq.attn_decode_kernel_launches(
+            self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window)
         # valid keys per (request, row) summed over rows' union per request
         seq = base.seq_lens.cpu().tolist()
         keys = 0

@@ -194,6 +194,19 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
     return plan.workspace;
 }
 
+int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
+                                int n_kv_heads, int head_dim, int max_seq_len, int window) {
+    if (check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len,
+                           window) != ATTN_OK)
+        return -1;
+    if (batch == 0) return 0;
+    gqa::DecodePlan plan;
+    gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
+                     &plan);
+    const int splits = (batch + plan.batch_per_launch - 1) / plan.batch_per_launch;
+    return splits * (plan.merge_kernel ? 2 : 1);
+}
+
 int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
                 const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
                 int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,

@@ -70,7 +70,9 @@ constexpr int kMergeWarps = 4;  // merge kernel CTA: small enough to be resident
 // CTA per query row merges all parts with every load in flight, which beats
 // two levels of counters and L2 round trips inside the split kernel.
 constexpr int kMergeKernelParts = 128;
-constexpr int kPrefetchTiles = 4;            // tiles of a share fetched into L2 before the PDL wait
+// bf16 tiles of a share fetched into L2 before the PDL wait (FP8 tiles hold
+// twice the keys: half as many, the same first 512 key positions)
+constexpr int kPrefetchTiles = 8;
 
 struct Params {
     const __nv_bfloat16 *q;
@@ -522,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         // their latency.  A prefetch writes nothing; a line the previous
         // kernel rewrites is refetched.
         if (warp == kProducerWarp && lane == 0 && p.kind != ATTN_CACHE_PAGED) {
+            constexpr int kTiles = kPrefetchTiles / G::kSubs;
             SegmentWalker walk{g0, g1, L};
             Segment sg;
             int issued = 0;
-            while (issued < kPrefetchTiles && walk.next(p, tb, sg)) {
+            while (issued < kTiles && walk.next(p, tb, sg)) {
                 const int bg = p.b_base + sg.b;
-                for (int c = sg.c_begin; c < sg.c_end && issued < kPrefetchTiles;
+                for (int c = sg.c_begin; c < sg.c_end && issued < kTiles;
                      c += kCPT, ++issued) {
                     const int z = sg.kvh * G::kHalves;
                     int j = c * kChunk;  // first position of the tile
@@ -1692,6 +1695,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     const int i = rem - kvh * p.rows;
     const int rb = i / RB, row = i - rb * RB;
     const int unit = (b * p.n_kv_heads + kvh) * p.row_blocks + rb;
+    // Release the next kernel at once: a following split kernel then takes
+    // each SM as this call's split CTAs leave it and plans and prefetches its
+    // first tiles while this merge waits, and it waits itself for this
+    // kernel to complete, which comes after this call's split kernel has.
+    // Everything issued before that split kernel has completed before this
+    // kernel starts (the split kernel releases it only after its own wait).
+    pdl_launch_dependents();
     // The CTAs that hold the unit, from the split kernel's own tables: this
     // kernel's predecessor is that split kernel, which releases it only after
     // waiting for its own predecessor, so seq_lens and positions are final and
@@ -1716,7 +1726,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
         }
     }
     pdl_wait();  // the partial states come from the split kernel
-    pdl_launch_dependents();
     // no keys (zero-filled) or few parts (merged by the split kernel)
     if (last - first < kGroupParts) return;
     // Each warp takes parts first + warp + kMergeWarps * k; a batch of kBatch
@@ -1871,7 +1880,12 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     if (cache->kind == ATTN_CACHE_RING) keys = std::min<int64_t>(keys, cache->slots_per_seq);
     const int64_t max_chunks = (keys + dec::kChunk - 1) / dec::kChunk + 1;
     const int64_t max_parts = (max_chunks + dec::kMinChunksPerCta - 1) / dec::kMinChunksPerCta + 1;
-    plan->merge_kernel = max_parts > dec::kMergeKernelParts;
+    // Few units (fewer than one per kGroupParts CTAs) with more than
+    // kGroupParts parts each go to the merge kernel too: two levels of
+    // counters inside the split kernel cost more than the kernel boundary.
+    plan->merge_kernel = max_parts > dec::kMergeKernelParts ||
+                         (max_parts > dec::kGroupParts &&
+                          units * dec::kGroupParts <= (size_t)plan->grid);
     return ATTN_OK;
 }
 

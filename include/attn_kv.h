@@ -192,6 +192,17 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
                                   int window);
 
 /*
+ * attn_decode_kernel_launches -- how many kernels one attn_decode (or
+ * attn_decode_append) call with these arguments launches on the stream: one
+ * split kernel per group of requests the shared-memory tables hold, each
+ * followed by the merge kernel when units of this shape may be split over
+ * enough CTAs to need it.  Host only; nothing is launched.  Returns -1 for
+ * arguments attn_decode would reject, 0 for batch 0.
+ */
+int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
+                                int n_kv_heads, int head_dim, int max_seq_len, int window);
+
+/*
  * attn_decode -- causal decode attention for q_rows query rows per request.
  *
  * Source: vibevoice.c, "The kernels that matter" / "Attention backends"

@@ -30,6 +30,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("attn_kv_append", "attn_decode", "attn_decode_workspace_size", "attn_prefill",
+                 "attn_decode_kernel_launches",
                  "attn_decode_append", "attn_kv_reference", "attn_status_string",
                  "attn_version"):
         assert want in names, names
@@ -113,6 +114,30 @@ def test_decode_workspace_checks(lib):
     assert decode_rc(lib, c, L=4096, ws=1 << 20, ws_bytes=need - 1) == gq.ATTN_ERR_WORKSPACE
     bad = lib.attn_decode_workspace_size(ctypes.byref(cs), 2, 1, 30, 8, 128, 4096, 0)
     assert bad == ctypes.c_size_t(-1).value
+
+
+def test_decode_kernel_launches(lib):
+    """The plan query: -1 where attn_decode would refuse, 0 for no requests,
+    otherwise split launches x (1 + merge kernel).  Without a GPU the library
+    plans for 148 SMs (296 CTAs)."""
+    f = lib.attn_decode_kernel_launches
+    c = cache(slots=16384 * 40, sps=16384)
+    cs = c.struct()
+    assert f(ctypes.byref(cs), 2, 1, 30, 8, 128, 4096, 0) == -1  # 30 q heads over 8
+    assert f(None, 2, 1, 32, 8, 128, 4096, 0) == -1
+    assert f(ctypes.byref(cs), 0, 1, 32, 8, 128, 4096, 0) == 0
+    # short contexts: every unit spans at most 8 CTAs, merged in the split kernel
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 512, 0) == 1
+    # 16 units at 8,192 keys: few units over many CTAs -> merge kernel
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0) == 2
+    # 320 units at 8,192 keys: too many units for the merge kernel's rule
+    assert f(ctypes.byref(cs), 40, 1, 32, 8, 128, 8192, 0) == 1
+    # one unit that may span more than 128 CTAs: merge kernel
+    assert f(ctypes.byref(cs), 40, 1, 8, 1, 128, 16384, 0) == 2
+    # more (request, row block) pairs than one launch's tables hold: 2 launches
+    big = cache(slots=64 * 300, sps=64)
+    bs = big.struct()
+    assert f(ctypes.byref(bs), 300, 1, 8, 2, 128, 64, 0) == 2
 
 
 def test_prefill_validation(lib):

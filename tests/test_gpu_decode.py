@@ -12,7 +12,7 @@ import torch
 
 import gqa_attention_kv_gb300 as gq
 from gqa_attention_kv_gb300 import synth
-from helpers import compare, gpu_decode, oracle_decode
+from helpers import compare, gpu_decode, oracle_decode, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -229,15 +229,33 @@ def test_batch_split_over_launches(B, R, Hq, Hkv):
 
 @pytest.mark.parametrize("L", [8192, 8200, 16000])
 def test_one_unit_over_many_ctas(L):
-    """One (request, KV head) over 64-126 CTAs: its partial states are merged
-    inside the split kernel in groups of eight (a ragged last group), then
-    the groups; the largest of these bounds is the last one merged that way."""
-    case = synth.decode_case(7200 + L, LINEAR, 1, 1, 8, 1, 128, [L])
+    """One long (request, KV head) among 40 units (too many for the merge
+    kernel), over 64-126 CTAs: its partial states are merged inside the
+    split kernel in groups of eight (a ragged last group), then the groups;
+    the largest of these bounds is the last one merged that way."""
+    seq = [L] + [1 + (7 * i) % 40 for i in range(39)]
+    case = synth.decode_case(7200 + L, LINEAR, 40, 1, 8, 1, 128, seq, slots_per_seq=L)
+    cache = to_device(case)
+    assert gq.attn_decode_kernel_launches(cache, 40, 1, 8, case.max_seq_len()) == 1
     ref, _, _ = oracle_decode(case)
     a, _ = gpu_decode(case)
     b, _ = gpu_decode(case)
     assert torch.equal(a, b), "run-to-run results differ"
-    compare(a, ref, f"one unit, {L} keys")
+    compare(a, ref, f"one unit of 40, {L} keys")
+
+
+@pytest.mark.parametrize("L", [2000, 8192, 14449])
+def test_few_units_merge_kernel(L):
+    """Two requests x 4 KV heads (Qwen2-7B's grouping) at mid contexts: eight
+    units over 304 CTAs, so their parts go to the merge kernel."""
+    case = synth.decode_case(7250 + L, LINEAR, 2, 1, 28, 4, 128, [L, L - 77])
+    cache = to_device(case)
+    assert gq.attn_decode_kernel_launches(cache, 2, 1, 28, case.max_seq_len()) == 2
+    ref, _, _ = oracle_decode(case)
+    a, _ = gpu_decode(case)
+    b, _ = gpu_decode(case)
+    assert torch.equal(a, b), "run-to-run results differ"
+    compare(a, ref, f"few units, {L} keys")
 
 
 def test_merge_kernel_threshold():
