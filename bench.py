@@ -19,7 +19,8 @@ output (236 MB) exceed the L2 by themselves.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload qwen|voxtral|encoder|encoder-long|ring|paged|
-                              qwen-prefill|prefill-8k]
+                              stream-encoder|ring-fp8|paged-fp8|voxtral-fp8|
+                              qwen-prefill|prefill-8k|chunked] [--layout bshd|bhsd]
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload (the oracle is the only reference implementation there is).
@@ -369,7 +370,8 @@ class DecodeOnlyWorkload(Workload):
         which = which[:-4] if self.fp8 else which
         make = {"voxtral": synth.voxtral_decode_step, "ring": synth.ring_window_decode,
                 "stream-encoder": synth.streaming_encoder_step,
-                "paged": synth.paged_multirow_decode}[which]
+                "paged": synth.paged_multirow_decode,
+                "chunked": synth.chunked_prefill_step}[which]
         base = make(device=dev)
         self.case = base
         self.kv_elem = 1 if self.fp8 else 2
@@ -425,6 +427,7 @@ class DecodeOnlyWorkload(Workload):
         # valid keys per (request, row) summed over rows' union per request
         seq = base.seq_lens.cpu().tolist()
         keys = 0
+        pairs = 0  # (query row, key) pairs attended, per query head
         for b, L in enumerate(seq):
             lo = 0
             pos = base.positions.cpu().view(base.batch, base.q_rows)[b]
@@ -433,7 +436,14 @@ class DecodeOnlyWorkload(Workload):
             if base.kind == synth.RING:
                 lo = max(lo, L - base.slots_per_seq)
             keys += L - lo
+            for p_ in pos.tolist():
+                lo_r = 0 if base.window <= 0 else max(0, p_ - base.window + 1)
+                if base.kind == synth.RING:
+                    lo_r = max(lo_r, L - base.slots_per_seq)
+                pairs += p_ + 1 - lo_r
         self.keys = keys
+        # 4 D Hq flops per (row, key) pair: the score and P V contractions
+        self.chunk_flops = 4.0 * base.head_dim * base.n_q_heads * pairs
         # one step = one decode per decoder layer, each layer its own cache
         # (Voxtral decoder: 26 layers); bigger workloads: one layer per step
         self.layers = {"voxtral": 26, "stream-encoder": 32}.get(which, 1)
@@ -443,7 +453,9 @@ class DecodeOnlyWorkload(Workload):
                      "ring": "ring window decode B=16 32/8 D=128 ring 16384 window 8192",
                      "stream-encoder": "streaming encoder step, 4 frames over a 1500-slot ring, "
                                        "window 750, 32/32 D=64, 32 layers",
-                     "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16"}[which]
+                     "paged": "paged K=4 decode 64x4 rows 32/8 D=128 bs 16",
+                     "chunked": "chunked prefill: 2 requests x a 29-row chunk at positions "
+                                "14420..14448 of a linear cache, 28/4 D=128"}[which]
         if self.fp8:
             self.name += ", FP8 (E4M3) cache"
         self.describe = {"workload": self.name, "decode_cache_copies": self.ncopy,
@@ -538,7 +550,7 @@ def make_workload(name, dev, layout=0):
     if name == "qwen":
         return QwenWorkload(dev, layout)
     if name in ("voxtral", "ring", "paged", "stream-encoder", "ring-fp8", "paged-fp8",
-                "voxtral-fp8"):
+                "voxtral-fp8", "chunked"):
         return DecodeOnlyWorkload(dev, name, layout)
     if name in ("encoder", "encoder-long", "qwen-prefill", "prefill-8k"):
         return PrefillOnlyWorkload(dev, name)
@@ -721,7 +733,7 @@ def main():
     ap.add_argument("--workload", default="qwen",
                     choices=["qwen", "voxtral", "encoder", "encoder-long", "ring", "paged",
                              "stream-encoder", "ring-fp8", "paged-fp8", "voxtral-fp8",
-                             "qwen-prefill", "prefill-8k"])
+                             "qwen-prefill", "prefill-8k", "chunked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -857,6 +869,14 @@ def main():
         line["roofline_decode"] = {"bound": "hbm", "achieved": line["decode"]["value"] / world,
                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                    "frac": line["decode"]["frac_of_measured_hbm"]}
+    cflops = getattr(wl, "chunk_flops", 0.0) * getattr(wl, "layers", 1)
+    if getattr(wl, "name", "").startswith("chunked") and dec_ms > 0:
+        # the chunk's rows attend with the decode kernel's legacy mma.sync
+        # tiling: its rate against the measured dense bf16 peak
+        ctf = cflops / (dec_ms / K / 1e3) / 1e12
+        line["chunk"] = {"value": round(ctf * world, 2), "unit": "TFLOP/s",
+                         "flops_per_step": cflops,
+                         "frac_of_measured_bf16": round(ctf / peaks["bf16_tflops"], 4)}
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline and args.workload == "qwen":

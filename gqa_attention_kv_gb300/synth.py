@@ -253,6 +253,15 @@ def streaming_encoder_step(device="cpu", batch=1):
                        ring=1500, scale=0.125, device=device)
 
 
+def chunked_prefill_step(device="cpu", batch=2, chunk=29):
+    """A prompt arriving in 29-row chunks (vibevoice.c's streaming 7B backend)
+    on the Qwen2-7B decoder shape (28 q / 4 kv heads, D=128): the last chunk
+    of each request's 14,449-token prompt, rows at positions 14,420 ..
+    14,448, against a linear cache holding the earlier rows."""
+    return decode_case(20267, LINEAR, batch, chunk, 28, 4, 128, [QWEN_PROMPT] * batch,
+                       device=device)
+
+
 def paged_multirow_decode(device="cpu", batch=64):
     """Paged K=4 uniform decode: 64 requests x 4 rows, bs 16, 200k-slot pool
     (12,500 pages dealt from a seeded permutation), seq_lens in [64, 4,096]."""

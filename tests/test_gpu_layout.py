@@ -108,7 +108,7 @@ def test_bhsd_ring(ring, window, R):
     check(case, f"bhsd ring {ring}/{window} R={R}")
 
 
-@pytest.mark.parametrize("R,Hq,Hkv", [(8, 32, 4), (2, 7, 1)])
+@pytest.mark.parametrize("R,Hq,Hkv", [(8, 32, 4), (4, 28, 4), (2, 7, 1)])
 def test_bhsd_row_tilings(R, Hq, Hkv):
     case = synth.decode_case(11400 + R * Hq, PAGED, 5, R, Hq, Hkv, 128,
                              [64, 100, max(R, 4), 1030, 517], block_size=16)
