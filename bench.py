@@ -245,7 +245,7 @@ class QwenWorkload(Workload):
         # prefill, prompt append, per decode the kernels the library plans
         # (split kernel + merge kernel at these long contexts)
         self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * gq.attn_decode_kernel_launches(
-            self.caches[0], self.B, 1, Hq, self.max_seq, 0)
+            self.caches[0], self.B, 1, Hq, self.max_seq, 0, with_append=True)
         self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",
                          "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D,
                          "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
@@ -423,7 +423,8 @@ class DecodeOnlyWorkload(Workload):
         self.step_i = 0
         # the step's append fused into the decode launch (bf16 and FP8)
         self.launches_per_step = gq.attn_decode_kernel_launches(
-            self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window)
+            self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window,
+            with_append=True)
         # valid keys per (request, row) summed over rows' union per request
         seq = base.seq_lens.cpu().tolist()
         keys = 0

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libgqa_attn_kv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["capi.cu", "append.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu"]
+SOURCES = ["capi.cu", "append.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu", "chunk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

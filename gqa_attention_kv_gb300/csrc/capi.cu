@@ -195,7 +195,8 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
 }
 
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
-                                int n_kv_heads, int head_dim, int max_seq_len, int window) {
+                                int n_kv_heads, int head_dim, int max_seq_len, int window,
+                                int with_append, int with_rope) {
     if (check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len,
                            window) != ATTN_OK)
         return -1;
@@ -203,6 +204,8 @@ int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_row
     gqa::DecodePlan plan;
     gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
                      &plan);
+    if (plan.chunk && !with_rope)
+        return (with_append ? 1 : 0) + 1 + (plan.cp.n_split > 1 ? 1 : 0);
     const int splits = (batch + plan.batch_per_launch - 1) / plan.batch_per_launch;
     return splits * (plan.merge_kernel ? 2 : 1);
 }

@@ -1,0 +1,627 @@
+// chunk.cu -- a prefill chunk against a linear KV cache on tcgen05 tensor cores.
+//
+// What is computed (vibevoice.c, "Prefill attention" and its streaming
+// backend, which feeds the decoder 29 prompt rows at a time; talker_multiframe,
+// NarrowStep fields: several query rows per request at positions[r]): for
+// request b, chunk row r at position positions[b*R + r] and query head h, the
+// softmax over keys t <= position (t < seq_lens[b]; i - t < window when one is
+// set) of scale * q . k_t applied to v_t, with KV head h / G.  It is the
+// K-row decode of the same arguments; this kernel serves it when the rows of
+// one KV group are many (R x G >= 64) and the cache is linear and slot-major.
+//
+// GB300 mapping.  The R x G query rows of one (request, KV head) are packed
+// into the M dimension of 128-row tcgen05 tiles: tile row m holds chunk row
+// m / G of the tile's rows and group head m % G, so every K/V tile of the
+// group is loaded once for all its heads and rows (G rows per position; 128 /
+// G positions per tile, the remaining rows padding).  A CTA takes two such
+// tiles and a range of key tiles: the key range of a (request, KV head) is
+// split over CTAs so that the few groups of a chunk still fill the GPU; each
+// CTA leaves a partial state per row (O / l in fp32 and the base-2 log-sum-
+// exp), and chunk_merge_kernel combines the splits in a fixed order.  One
+// split writes the bf16 rows itself.
+//
+// The warp roles, rings, TMEM columns and the ping-pong of the two tiles are
+// those of the prefill kernel (prefill.cu): warp 0 issues TMA, warp 1 the
+// tcgen05.mma (S_a = Q_a K^T, O_a += P_a V with P as bf16 hi + lo halves),
+// warps 4..11 run the softmax of one tile row per thread.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace chk {
+
+constexpr int kBM = 128;       // rows per tile (two tiles per CTA)
+constexpr int kBN = 128;       // keys per tile
+constexpr int kThreads = 384;  // 3 warpgroups
+// Registers as in the prefill kernel: launched at 168 a thread, the TMA/MMA
+// warpgroup drops to 72 and the two softmax warpgroups rise to 216
+// (4x32x72 + 8x32x216 = 384x168).
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMergeWarps = 8;
+
+template <int HD>
+struct Cfg {
+    static constexpr int kHalves = HD / 64;
+    static constexpr int kKStages = HD == 128 ? 2 : 4;
+    static constexpr int kVStages = HD == 128 ? 3 : 4;
+    static constexpr int kQBytes = kBM * HD * 2;  // one Q tile
+    static constexpr int kKBytes = kBN * HD * 2;
+    static constexpr int kVBytes = kBN * HD * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + 2 * kQBytes;
+    static constexpr int kOffV = kOffK + kKStages * kKBytes;
+    static constexpr int kOffBar = kOffV + kVStages * kVBytes;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 10;
+    static constexpr size_t kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
+};
+
+struct Params {
+    int batch, q_rows, window, n_kv_heads, group, head_dim;
+    int rt;       // chunk rows per tile: 128 / group
+    int n_pairs;  // tile pairs along the chunk rows
+    int n_split;  // CTAs along the key range of one (request, KV head, pair)
+    int slots_per_seq, max_seq_len;
+    const int32_t *seq_lens;   // [batch]
+    const int32_t *positions;  // [batch * q_rows]
+    float scale_log2;
+    float *ws_o;    // n_split > 1: [slot][256][HD] fp32, slot = ((b*Hkv + kvh)*pairs + pair)*splits + s
+    float *ws_lse;  // [slot][256]
+    __nv_bfloat16 *out;  // [batch, q_rows, n_q_heads, HD]
+    int32_t *err;
+};
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            int w, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The request's keys: seq_lens[b], range-checked as the decode checks it.
+__device__ __forceinline__ int request_keys(const Params &p, int b, bool report) {
+    int n = p.seq_lens[b];
+    if (n < 0 || n > p.max_seq_len || n > p.slots_per_seq) {
+        if (report) report_error(p.err, ATTN_ERR_BOUNDS);
+        n = max(0, min(n, min(p.max_seq_len, p.slots_per_seq)));
+    }
+    return n;
+}
+
+// Key tiles [kt0, kt0 + n_kt) of split s for the rows whose positions span
+// [p_lo, p_hi] of a request holding n_keys keys.
+__device__ __forceinline__ void split_range(const Params &p, int p_lo, int p_hi, int n_keys,
+                                            int s, int &kt0, int &n_kt) {
+    const int key_hi = min(n_keys, p_hi + 1);
+    const int key_lo = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
+    const int lo = key_lo / kBN;
+    const int hi = key_hi > key_lo ? (key_hi + kBN - 1) / kBN : lo;
+    const int per = (hi - lo + p.n_split - 1) / p.n_split;
+    kt0 = lo + s * per;
+    n_kt = max(0, min(per, hi - kt0));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sK = smem + C::kOffK;
+    uint8_t *sV = smem + C::kOffV;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *k_full = bars;                   // [kKStages]
+    uint64_t *k_empty = k_full + C::kKStages;  // [kKStages]
+    uint64_t *v_full = k_empty + C::kKStages;  // [kVStages]
+    uint64_t *v_empty = v_full + C::kVStages;  // [kVStages]
+    uint64_t *q_full = v_empty + C::kVStages;
+    uint64_t *s_full = q_full + 1;  // [2]
+    uint64_t *p_full = s_full + 2;  // [2 tiles][2 key halves]
+    uint64_t *o_done = p_full + 4;
+    uint64_t *mma_done = o_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+    __shared__ int s_pos[2];  // min and max position of the CTA's rows
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // block: ((b * Hkv + kvh) * n_split + split) * n_pairs + pair
+    const int pair = (int)(blockIdx.x % p.n_pairs);
+    int rest = (int)(blockIdx.x / p.n_pairs);
+    const int split = rest % p.n_split;
+    rest /= p.n_split;
+    const int kvh = rest % p.n_kv_heads;
+    const int b = rest / p.n_kv_heads;
+    const int G = p.group, R = p.q_rows;
+    const int r_first = pair * 2 * p.rt;                 // first chunk row of the pair
+    const int r_end = min(R, r_first + 2 * p.rt);        // one past its last
+    const int used = p.rt * G;                           // tile rows that hold queries
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 128);
+        mbar_init(o_done, 1);
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+        s_pos[0] = INT32_MAX;
+        s_pos[1] = -1;
+    }
+    // Tile rows past the packed queries are never written by TMA: zero them
+    // (generic stores, made visible to the tensor core's proxy below).
+    if (used < kBM) {
+        for (int i = threadIdx.x; i < 2 * C::kHalves * (kBM - used) * 8; i += kThreads) {
+            const int piece = i & 7, row = used + (i >> 3) % (kBM - used);
+            const int th = (i >> 3) / (kBM - used);  // tile * halves + half
+            *reinterpret_cast<uint4 *>(sQ + th * (kBM * 128) + row * 128 + piece * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();  // q, the cache, seq_lens and positions may come from the previous kernel
+    pdl_launch_dependents();
+    // the span of positions of the pair's rows (bounds the key range)
+    for (int r = r_first + (int)threadIdx.x; r < r_end; r += kThreads) {
+        const int pos = p.positions[(int64_t)b * R + r];
+        atomicMin(&s_pos[0], pos);
+        atomicMax(&s_pos[1], pos);
+    }
+    const int n_keys = request_keys(p, b, kvh == 0 && split == 0 && pair == 0 && threadIdx.x == 0);
+    __syncthreads();
+    int kt0, n_kt;
+    split_range(p, s_pos[0], s_pos[1], n_keys, split, kt0, n_kt);
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            // both tiles' boxes of rt positions x G heads x 64 columns (rows
+            // past the chunk's end are zero-filled by the copy)
+            mbar_arrive_expect_tx(q_full, 2 * C::kHalves * used * 128);
+            for (int a = 0; a < 2; ++a)
+                for (int hf = 0; hf < C::kHalves; ++hf)
+                    tma_load_4d(sQ + a * C::kQBytes + hf * (kBM * 128), &tm_q, hf * 64, kvh * G,
+                                r_first + a * p.rt, b, q_full);
+            int kj = 0, vj = 0;
+            bool ok = true;
+            while (ok && (kj < n_kt || vj < n_kt)) {
+                if (kj < n_kt && (kj <= vj + 1 || vj >= n_kt)) {
+                    const int st = kj % C::kKStages;
+                    if (kj >= C::kKStages)
+                        ok = mbar_wait(&k_empty[st], ((kj / C::kKStages) - 1) & 1, p.err);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[st], C::kKBytes);
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        tma_load_3d(sK + st * C::kKBytes + hf * (kBN * 128), &tm_k,
+                                    kvh * HD + hf * 64, (kt0 + kj) * kBN, b, &k_full[st]);
+                    ++kj;
+                } else {
+                    const int st = vj % C::kVStages;
+                    if (vj >= C::kVStages)
+                        ok = mbar_wait(&v_empty[st], ((vj / C::kVStages) - 1) & 1, p.err);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v_full[st], C::kVBytes);
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        tma_load_3d(sV + st * C::kVBytes + hf * (kBN * 128), &tm_v,
+                                    kvh * HD + hf * 64, (kt0 + vj) * kBN, b, &v_full[st]);
+                    ++vj;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, 0, 1);
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sV), kBN * 128, 1024);
+            auto issue_qk = [&](int a, int kst) {
+                const uint64_t qd = q_desc + (uint64_t)((a * C::kQBytes) >> 4);
+                const uint64_t kd = k_desc0 + (uint64_t)((kst * C::kKBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                    tc_mma_ss(tmem + a * 128, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[a]);
+            };
+            auto issue_pv_half = [&](int a, int vst, int hh, bool first) {
+                const uint64_t vd = v_desc0 + (uint64_t)((vst * C::kVBytes) >> 4);
+                const uint32_t p_tmem = tmem + a * 128;
+                const uint32_t o_tmem = tmem + 256 + a * HD;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                        const int kk = hh * (kBN / 32) + k4;
+                        tc_mma_ts(o_tmem, p_tmem + part * 64 + kk * 8,
+                                  vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                                  (!first || k4 > 0 || part > 0) ? 1u : 0u);
+                    }
+            };
+            bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
+            if (ok && n_kt > 0) {
+                tc_fence_after();
+                issue_qk(0, 0);
+                issue_qk(1, 0);
+                tc_commit(&k_empty[0]);
+            }
+            int vst = 0, vph = 0, kst = 0, kph = 0;
+            for (int j = 0; j < n_kt && ok; ++j) {
+                ok = mbar_wait(&v_full[vst], vph, p.err);
+                const bool more = j + 1 < n_kt;
+                if (more && ++kst == C::kKStages) {
+                    kst = 0;
+                    kph ^= 1;
+                }
+                for (int a = 0; a < 2 && ok; ++a) {
+                    for (int hh = 0; hh < 2 && ok; ++hh) {
+                        ok = mbar_wait(&p_full[a * 2 + hh], j & 1, p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv_half(a, vst, hh, j == 0 && hh == 0);
+                    }
+                    if (!ok) break;
+                    if (a == 1) tc_commit(&v_empty[vst]);
+                    if (more) {
+                        if (a == 0) {
+                            ok = mbar_wait(&k_full[kst], kph, p.err);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_qk(a, kst);
+                        if (a == 1) tc_commit(&k_empty[kst]);
+                    }
+                }
+                if (++vst == C::kVStages) {
+                    vst = 0;
+                    vph ^= 1;
+                }
+            }
+            tc_commit(o_done);
+            tc_commit(mma_done);
+            mbar_wait(mma_done, 0, p.err);
+        }
+    }
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        // ---------------------------------------------------------- softmax
+        const int a = (warp - 4) >> 2;     // which tile
+        const int quad = warp & 3;         // TMEM lane quadrant of this warp
+        const int row = quad * 32 + lane;  // tile row = TMEM lane
+        int qi = -1;  // the row's position (-1: a padding row, which sees no key)
+        {
+            const int r = r_first + a * p.rt + row / G;  // chunk row
+            if (row < used && r < r_end) qi = p.positions[(int64_t)b * R + r];
+        }
+        const int key_cap = min(qi, n_keys - 1);  // last key this row may see
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint32_t s_tmem = tmem + a * 128 + lane_base;
+        const uint32_t o_tmem = tmem + 256 + a * HD + lane_base;
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            ok = mbar_wait(&s_full[a], j & 1, p.err);
+            __syncwarp();
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBN];
+            {
+                uint32_t(&u)[kBN] = *reinterpret_cast<uint32_t(*)[kBN]>(s);
+                tmem_ld_32x32b_x32(s_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(u + 0));
+                tmem_ld_32x32b_x32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+                tmem_ld_32x32b_x32(s_tmem + 64, *reinterpret_cast<uint32_t(*)[32]>(u + 64));
+                tmem_ld_32x32b_x32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 96));
+                tmem_wait_ld();
+            }
+            const int key0 = (kt0 + j) * kBN;
+            const bool needs_mask =
+                key0 + kBN - 1 > key_cap || (p.window > 0 && qi - key0 >= p.window);
+            if (needs_mask) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const int t = key0 + c;
+                    const bool valid = t <= key_cap && (p.window <= 0 || qi - t < p.window);
+                    s[c] = valid ? s[c] : -INFINITY;
+                }
+            }
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int c = 4; c < kBN; c += 8) {
+                mx0 = max3(mx0, s[c], s[c + 1]);
+                mx1 = max3(mx1, s[c + 2], s[c + 3]);
+                mx2 = max3(mx2, s[c + 4], s[c + 5]);
+                mx3 = max3(mx3, s[c + 6], s[c + 7]);
+            }
+            const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+            float alpha = 1.f;
+            if (mx > m_run + kRescaleThreshold || m_run == -INFINITY) {
+                const float m_new = mx == -INFINITY ? m_run : mx;
+                alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+                m_run = m_new;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t orow[32];
+                    tmem_ld_32x32b_x32(o_tmem + c0, orow);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+                    tmem_st_32x32b_x32(o_tmem + c0, orow);
+                }
+            }
+            const float mref = m_run == -INFINITY ? 0.f : m_run;
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float x0, x1;
+                    fma2(x0, x1, s[c0 + 2 * e], s[c0 + 2 * e + 1], sl2, sl2, -mref, -mref);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    add2(sum0, sum1, sum0, sum1, p0, p1);
+                    split_trunc_bf16x2(p0, p1, hi[e], lo[e]);
+                }
+                tmem_st_32x32b_x16(s_tmem + c0 / 2, hi);
+                tmem_st_32x32b_x16(s_tmem + 64 + c0 / 2, lo);
+                if (c0 == kBN / 2 - 32 || c0 == kBN - 32) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&p_full[a * 2 + (c0 >= kBN / 2 ? 1 : 0)]);
+                }
+            }
+            l_run = l_run * alpha + (sum0 + sum1);
+        }
+        // epilogue: the row's O / l (bf16 when the key range is not split,
+        // else an fp32 partial state with its base-2 log-sum-exp)
+        if (ok) ok = mbar_wait(o_done, 0, p.err);
+        __syncwarp();
+        tc_fence_after();
+        const bool any = l_run > 0.f;  // O in TMEM was written (n_kt > 0, a key seen)
+        const float inv = any ? 1.f / l_run : 0.f;
+        const int64_t slot = (((int64_t)b * p.n_kv_heads + kvh) * p.n_pairs + pair) * p.n_split +
+                             split;
+        const int m = a * kBM + row;
+        const int r = r_first + a * p.rt + row / G, gh = row % G;  // chunk row, group head
+        const bool live = row < used && r < r_end;
+        __nv_bfloat16 *dst =
+            p.out + (((int64_t)b * R + r) * (p.n_kv_heads * G) + kvh * G + gh) * HD;
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t orow[32];
+            if (n_kt > 0) {  // CTA-uniform: the TMEM rows were accumulated into
+                tmem_ld_32x32b_x32(o_tmem + c0, orow);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) orow[e] = 0u;
+            }
+            // O / l of this row (zero when no key was seen: inv is 0)
+            auto v = [&](int e) { return any ? __uint_as_float(orow[e]) * inv : 0.f; };
+            if (p.n_split == 1) {
+                if (live) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<uint4 *>(dst + c0 + q4 * 8) =
+                            make_uint4(pack_bf16x2(v(8 * q4), v(8 * q4 + 1)),
+                                       pack_bf16x2(v(8 * q4 + 2), v(8 * q4 + 3)),
+                                       pack_bf16x2(v(8 * q4 + 4), v(8 * q4 + 5)),
+                                       pack_bf16x2(v(8 * q4 + 6), v(8 * q4 + 7)));
+                }
+            } else {
+                float *o = p.ws_o + (slot * 2 * kBM + m) * HD + c0;
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4 *>(o + 4 * q4) =
+                        make_float4(v(4 * q4), v(4 * q4 + 1), v(4 * q4 + 2), v(4 * q4 + 3));
+            }
+        }
+        if (p.n_split > 1) p.ws_lse[slot * 2 * kBM + m] = any ? m_run + __log2f(l_run) : -INFINITY;
+    }
+    __syncwarp();  // lanes 1..31 of the TMA and MMA warps wait here for lane 0
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// One warp per packed row of a (request, KV head, pair): the splits' partial
+// states in split order, weights from the log-sum-exps, one bf16 rounding.
+template <int HD>
+__global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Params p) {
+    constexpr int PER = HD / 32;
+    pdl_wait();  // the partial states come from the chunk kernel
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kMergeWarps + warp;  // (group slot, m)
+    const int m = (int)(gw % (2 * kBM));
+    const int64_t grp = gw / (2 * kBM);  // ((b * Hkv + kvh) * pairs + pair)
+    const int pair = (int)(grp % p.n_pairs);
+    const int64_t bk = grp / p.n_pairs;
+    if (bk >= (int64_t)p.batch * p.n_kv_heads) return;
+    const int kvh = (int)(bk % p.n_kv_heads), b = (int)(bk / p.n_kv_heads);
+    const int G = p.group;
+    const int a = m / kBM, row = m % kBM;
+    const int r = pair * 2 * p.rt + a * p.rt + row / G, gh = row % G;
+    if (row >= p.rt * G || r >= p.q_rows) return;
+    float M = -INFINITY;
+    for (int s = 0; s < p.n_split; ++s)
+        M = fmaxf(M, __ldcg(p.ws_lse + (grp * p.n_split + s) * 2 * kBM + m));
+    float L = 0.f, acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < p.n_split; ++s) {
+            const int64_t slot = grp * p.n_split + s;
+            const float lse = __ldcg(p.ws_lse + slot * 2 * kBM + m);
+            if (lse == -INFINITY) continue;
+            const float f = fast_exp2(lse - M);
+            L += f;
+            const float *src = p.ws_o + (slot * 2 * kBM + m) * HD + lane * PER;
+            if constexpr (PER == 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                acc[0] += f * t.x;
+                acc[1] += f * t.y;
+                acc[2] += f * t.z;
+                acc[3] += f * t.w;
+            } else {
+                const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                acc[0] += f * t.x;
+                acc[1] += f * t.y;
+            }
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16 *dst =
+        p.out + (((int64_t)b * p.q_rows + r) * (p.n_kv_heads * G) + kvh * G + gh) * HD + lane * PER;
+    if constexpr (PER == 4) {
+        uint2 w;
+        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = w;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+template <int HD>
+int launch(const Params &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+           cudaStream_t stream) {
+    auto kern = chunk_kernel<HD>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<HD>::kSmem);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return ATTN_ERR_CUDA;
+        }
+        configured_device = dev;
+    }
+    const int64_t groups = (int64_t)p.batch * p.n_kv_heads * p.n_pairs;
+    const unsigned grid = (unsigned)(groups * p.n_split);
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg<HD>::kSmem, stream, tq, tk, tv, p) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (p.n_split > 1) {
+        const unsigned mgrid = (unsigned)((groups * 2 * kBM + kMergeWarps - 1) / kMergeWarps);
+        if (launch_pdl(chunk_merge_kernel<HD>, dim3(mgrid), dim3(kMergeWarps * 32), 0, stream,
+                       p) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace chk
+
+// Chunk plan: rows per tile, pairs and splits (see kernels.h).
+void plan_chunk(int batch, int q_rows, int n_q_heads, int n_kv_heads, int head_dim,
+                int max_seq_len, int window, ChunkPlan *plan) {
+    const int G = n_q_heads / n_kv_heads;
+    plan->rt = chk::kBM / G;
+    plan->n_pairs = (q_rows + 2 * plan->rt - 1) / (2 * plan->rt);
+    const int64_t groups = (int64_t)batch * n_kv_heads * plan->n_pairs;
+    // key tiles a pair may need: its rows' keys (bounded by max_seq_len, and
+    // by the window plus the pair's rows)
+    int64_t keys = max_seq_len;
+    if (window > 0) keys = std::min<int64_t>(keys, (int64_t)window + 2 * plan->rt + chk::kBN);
+    const int64_t tiles = (keys + chk::kBN - 1) / chk::kBN + 1;
+    // enough CTAs to fill the SMs (one CTA each), at least two key tiles apiece
+    int64_t split = std::max<int64_t>(1, device_sm_count() / std::max<int64_t>(groups, 1));
+    split = std::min<int64_t>(split, std::max<int64_t>(1, tiles / 2));
+    plan->n_split = (int)split;
+    plan->workspace = plan->n_split > 1 ? (size_t)groups * plan->n_split * 2 * chk::kBM *
+                                              ((size_t)head_dim + 1) * sizeof(float)
+                                        : 0;
+}
+
+int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cache,
+                 const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
+                 int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
+                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream) {
+    chk::Params p;
+    p.batch = batch;
+    p.q_rows = q_rows;
+    p.window = window;
+    p.n_kv_heads = n_kv_heads;
+    p.group = n_q_heads / n_kv_heads;
+    p.head_dim = head_dim;
+    p.rt = plan.rt;
+    p.n_pairs = plan.n_pairs;
+    p.n_split = plan.n_split;
+    p.slots_per_seq = cache->slots_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.seq_lens = seq_lens;
+    p.positions = positions;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const size_t groups = (size_t)batch * n_kv_heads * plan.n_pairs;
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_lse = p.ws_o ? p.ws_o + groups * plan.n_split * 2 * chk::kBM * head_dim : nullptr;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.err = err;
+    // q viewed as {head_dim, n_q_heads, q_rows, batch}: a box of {64, G, rt, 1}
+    // lands as rt x G rows of 128 bytes, the packed tile rows.
+    CUtensorMap tq, tk, tv;
+    const uint64_t dq[4] = {(uint64_t)head_dim, (uint64_t)n_q_heads, (uint64_t)q_rows,
+                            (uint64_t)batch};
+    const uint64_t sq[3] = {(uint64_t)head_dim * 2, (uint64_t)n_q_heads * head_dim * 2,
+                            (uint64_t)q_rows * n_q_heads * head_dim * 2};
+    const uint32_t bq[4] = {64, (uint32_t)p.group, (uint32_t)plan.rt, 1};
+    // the linear cache viewed per request: {Hkv * D, slots_per_seq, batch}
+    const uint64_t dk[3] = {(uint64_t)n_kv_heads * head_dim, (uint64_t)cache->slots_per_seq,
+                            (uint64_t)batch};
+    const uint64_t sk[2] = {(uint64_t)n_kv_heads * head_dim * 2,
+                            (uint64_t)cache->slots_per_seq * n_kv_heads * head_dim * 2};
+    const uint32_t bk[3] = {64, (uint32_t)chk::kBN, 1};
+    if (!encode_tensor_map(&tq, q, 4, dq, sq, bq, true) ||
+        !encode_tensor_map(&tk, cache->k, 3, dk, sk, bk, true) ||
+        !encode_tensor_map(&tv, cache->v, 3, dk, sk, bk, true)) {
+        note_cuda_error(cudaErrorInvalidValue);
+        return ATTN_ERR_CUDA;
+    }
+    return head_dim == 128 ? chk::launch<128>(p, tq, tk, tv, stream)
+                           : chk::launch<64>(p, tq, tk, tv, stream);
+}
+
+}  // namespace gqa

@@ -1890,6 +1890,16 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->merge_kernel = max_parts > dec::kMergeKernelParts ||
                          (max_parts > dec::kGroupParts &&
                           units * dec::kGroupParts <= (size_t)plan->grid);
+    // A group of 64 or more query rows (a prefill chunk) over a linear
+    // slot-major bf16 cache is a dense contraction: the tcgen05 chunk kernel.
+    plan->chunk = cache->kind == ATTN_CACHE_LINEAR && cache->layout == ATTN_LAYOUT_BSHD &&
+                  cache->dtype == ATTN_KV_BF16 && plan->rows >= 64 && group <= 128;
+    plan->chunk_offset = (plan->workspace + 255) & ~size_t(255);
+    if (plan->chunk) {
+        plan_chunk(batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
+                   &plan->cp);
+        plan->workspace = plan->chunk_offset + plan->cp.workspace;
+    }
     return ATTN_OK;
 }
 
@@ -1899,6 +1909,19 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
                   const float *rope_inv_freq, bool tables_early) {
+    if (plan.chunk && rope_inv_freq == nullptr) {
+        // the step's rows first (every CTA of the chunk kernel may read them)
+        if (k_new) {
+            const KvPlace place = kv_place(cache, n_kv_heads, plan.head_dim, 2);
+            const int rc = launch_kv_append(k_new, v_new, slot_mapping, (int64_t)batch * q_rows,
+                                            cache->k, cache->v, cache->num_slots, place, err,
+                                            stream);
+            if (rc != ATTN_OK) return rc;
+        }
+        return launch_chunk(plan.cp, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
+                            window, n_q_heads, n_kv_heads, plan.head_dim, scale, out,
+                            static_cast<uint8_t *>(workspace) + plan.chunk_offset, err, stream);
+    }
     // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][cols]
     // (a half is 128 bytes of one head's row: 64 bf16 or 128 E4M3 columns): a
     // box of {cols, rows, halves} brings the whole head row of `rows` slots.

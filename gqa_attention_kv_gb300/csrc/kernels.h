@@ -80,6 +80,23 @@ int launch_kv_append_fp8(const void *k_new, const void *v_new, const float *k_re
 int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,
                         cudaStream_t stream);
 
+// Chunk plan (many query rows per KV group over a linear slot-major bf16
+// cache, chunk.cu): rt chunk rows per 128-row tcgen05 tile, n_pairs tile
+// pairs, n_split CTAs along each key range, and the fp32 partial states
+// (n_split > 1) the merge combines.
+struct ChunkPlan {
+    int rt, n_pairs, n_split;
+    size_t workspace;
+};
+
+void plan_chunk(int batch, int q_rows, int n_q_heads, int n_kv_heads, int head_dim,
+                int max_seq_len, int window, ChunkPlan *plan);
+
+int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cache,
+                 const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
+                 int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
+                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream);
+
 // Decode plan: a persistent grid of one CTA per SM; requests are processed
 // in launches of at most batch_per_launch (the per-request tables live in
 // shared memory).
@@ -93,6 +110,12 @@ struct DecodePlan {
     size_t workspace;     // bytes of scratch: fp32 partial states + merge counters
     size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
     bool merge_kernel;    // units spanning very many CTAs are merged by a second kernel
+    // Many rows per KV group over a linear slot-major bf16 cache go to the
+    // tcgen05 chunk kernel instead (not with a fused rotary embedding, which
+    // stays on the split kernel: the workspace covers both).
+    bool chunk;
+    ChunkPlan cp;
+    size_t chunk_offset;  // the chunk's partial states, after the split kernel's scratch
 };
 
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,

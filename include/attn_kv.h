@@ -192,15 +192,22 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
                                   int window);
 
 /*
- * attn_decode_kernel_launches -- how many kernels one attn_decode (or
- * attn_decode_append) call with these arguments launches on the stream: one
+ * attn_decode_kernel_launches -- how many kernels one call with these
+ * arguments launches on the stream (host only; nothing is launched):
+ * attn_decode when with_append is 0, attn_decode_append when it is 1, with a
+ * rotary embedding when with_rope is 1.  A split-kernel call launches one
  * split kernel per group of requests the shared-memory tables hold, each
  * followed by the merge kernel when units of this shape may be split over
- * enough CTAs to need it.  Host only; nothing is launched.  Returns -1 for
- * arguments attn_decode would reject, 0 for batch 0.
+ * enough CTAs to need it.  A group of 64 or more query rows (q_rows x
+ * n_q_heads / n_kv_heads) over a linear slot-major bf16 cache, without a
+ * rotary embedding, is a prefill chunk: the append kernel (attn_decode_append
+ * only), the tcgen05 chunk kernel, and its merge kernel when the key range is
+ * split over CTAs.  Returns -1 for arguments attn_decode would reject, 0 for
+ * batch 0.
  */
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
-                                int n_kv_heads, int head_dim, int max_seq_len, int window);
+                                int n_kv_heads, int head_dim, int max_seq_len, int window,
+                                int with_append, int with_rope);
 
 /*
  * attn_decode -- causal decode attention for q_rows query rows per request.

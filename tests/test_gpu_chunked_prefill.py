@@ -7,13 +7,26 @@ K-row causal decode: the chunk's R rows sit at positions seq_len - R .. seq_len
 before it in the chunk.  The library runs it through attn_kv_append +
 attn_decode with q_rows = R; the row blocks of a long GQA group (R x G rows)
 split into several units.
+
+A group of 64 or more rows over a linear slot-major bf16 cache runs on the
+tcgen05 chunk kernel (the rows of a KV group packed into 128-row tiles, the
+key range split over CTAs); the rest on the decode's split kernel.  Both are
+checked against the oracle.
 """
 import pytest
+import torch
 
+import gqa_attention_kv_gb300 as gq
 from gqa_attention_kv_gb300 import synth
-from helpers import compare, gpu_decode, oracle_decode
+from helpers import compare, gpu_decode, oracle_decode, to_device
 
 pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def launches(case, **kw):
+    return gq.attn_decode_kernel_launches(to_device(case, DEV), case.batch, case.q_rows,
+                                          case.n_q_heads, case.max_seq_len(), case.window, **kw)
 
 
 @pytest.mark.parametrize("R,Hq,Hkv", [(29, 28, 4), (29, 32, 8), (64, 32, 8), (16, 16, 16)])
@@ -37,3 +50,41 @@ def test_chunk_in_sliding_window_ring():
     ref, _, _ = oracle_decode(case)
     out, _ = gpu_decode(case)
     compare(out, ref, "ring chunk R=29 W=750")
+
+
+@pytest.mark.parametrize("R,Hq,Hkv,D", [(29, 28, 4, 128), (64, 32, 8, 128), (16, 16, 4, 64),
+                                        (10, 56, 8, 128), (40, 12, 2, 64)])
+def test_chunk_kernel_packings(R, Hq, Hkv, D):
+    """Groups of 7 (18 rows a tile, two padding rows), 4 (32), 6 (21), and a
+    chunk shorter than one tile's rows; requests of very different lengths, so
+    some key splits are empty."""
+    seq = [R + 5000, R, R + 300, 3 * R]
+    case = synth.decode_case(8300 + R * Hq + D, synth.LINEAR, len(seq), R, Hq, Hkv, D, seq)
+    assert launches(case) >= 1
+    ref, _, _ = oracle_decode(case)
+    a, _ = gpu_decode(case)
+    b, _ = gpu_decode(case)
+    assert torch.equal(a, b), "run-to-run results differ"
+    compare(a, ref, f"chunk kernel R={R} {Hq}/{Hkv} D={D}")
+
+
+def test_chunk_kernel_window():
+    """A 29-row chunk with a 750-key window over a long linear cache."""
+    R = 29
+    case = synth.decode_case(8400, synth.LINEAR, 2, R, 28, 4, 128, [6000, 2000], window=750)
+    ref, _, _ = oracle_decode(case)
+    out, _ = gpu_decode(case)
+    compare(out, ref, "chunk kernel, window 750")
+
+
+def test_chunk_kernel_fused_append_and_rope_fallback():
+    """attn_decode_append on a chunk: the append kernel, then the chunk
+    kernel (and its merge); with a rotary embedding the split kernel."""
+    from test_gpu_decode_append import _run
+
+    case = synth.decode_case(8500, synth.LINEAR, 2, 29, 28, 4, 128, [14449, 3000])
+    assert launches(case, with_append=True) == 3
+    assert launches(case, with_append=True, with_rope=True) == 1
+    fused, _ = _run(case, fused=True)
+    ref, _, _ = oracle_decode(case)
+    compare(fused, ref, "fused chunk")
