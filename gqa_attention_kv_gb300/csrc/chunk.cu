@@ -466,9 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // One warp per packed row of a (request, KV head, pair): the splits' partial
 // states in split order, weights from the log-sum-exps, one bf16 rounding.
+// The lanes read 32 splits' log-sum-exps at once; the output pieces of eight
+// splits are in flight together.
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Params p) {
     constexpr int PER = HD / 32;
+    constexpr int kBatch = 8;
     pdl_wait();  // the partial states come from the chunk kernel
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -483,30 +486,51 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
     const int a = m / kBM, row = m % kBM;
     const int r = pair * 2 * p.rt + a * p.rt + row / G, gh = row % G;
     if (row >= p.rt * G || r >= p.q_rows) return;
+    const float *lse = p.ws_lse + grp * p.n_split * 2 * kBM + m;  // split s at s * 2 kBM
+    const float *o = p.ws_o + (grp * p.n_split * 2 * kBM + m) * HD + lane * PER;
     float M = -INFINITY;
-    for (int s = 0; s < p.n_split; ++s)
-        M = fmaxf(M, __ldcg(p.ws_lse + (grp * p.n_split + s) * 2 * kBM + m));
+    for (int s0 = 0; s0 < p.n_split; s0 += 32)
+        if (s0 + lane < p.n_split) M = fmaxf(M, __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
     float L = 0.f, acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < p.n_split; ++s) {
-            const int64_t slot = grp * p.n_split + s;
-            const float lse = __ldcg(p.ws_lse + slot * 2 * kBM + m);
-            if (lse == -INFINITY) continue;
-            const float f = fast_exp2(lse - M);
-            L += f;
-            const float *src = p.ws_o + (slot * 2 * kBM + m) * HD + lane * PER;
-            if constexpr (PER == 4) {
-                const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-                acc[0] += f * t.x;
-                acc[1] += f * t.y;
-                acc[2] += f * t.z;
-                acc[3] += f * t.w;
-            } else {
-                const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-                acc[0] += f * t.x;
-                acc[1] += f * t.y;
+        for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+            // this lane's split weight (0 for an empty split or past the end)
+            float w = 0.f;
+            if (s0 + lane < p.n_split) {
+                const float l = __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM);
+                w = l == -INFINITY ? 0.f : fast_exp2(l - M);
+            }
+            const int n = min(32, p.n_split - s0);
+            for (int k0 = 0; k0 < n; k0 += kBatch) {
+                float v[kBatch][PER];
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) v[k][e] = 0.f;
+                    if (k0 + k < n) {
+                        const float *src = o + (int64_t)(s0 + k0 + k) * 2 * kBM * HD;
+                        if constexpr (PER == 4) {
+                            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                            v[k][0] = t.x, v[k][1] = t.y, v[k][2] = t.z, v[k][3] = t.w;
+                        } else {
+                            const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                            v[k][0] = t.x, v[k][1] = t.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const float f = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                    if (k0 + k < n) {
+                        L += f;
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) acc[e] += f * v[k][e];
+                    }
+                }
             }
         }
     }
@@ -514,10 +538,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
     __nv_bfloat16 *dst =
         p.out + (((int64_t)b * p.q_rows + r) * (p.n_kv_heads * G) + kvh * G + gh) * HD + lane * PER;
     if constexpr (PER == 4) {
-        uint2 w;
-        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(dst) = w;
+        uint2 w2;
+        w2.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w2.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = w2;
     } else {
         *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
