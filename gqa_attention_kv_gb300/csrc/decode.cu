@@ -1870,13 +1870,22 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
     plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
     const size_t units = (size_t)plan->batch_per_launch * n_kv_heads * plan->row_blocks;
-    // partial slots: unit + cta < units + grid; then one counter per unit and
-    // one per partial slot (a group's counter sits at its first part's slot)
+    // partial slots: unit + cta < units + grid; one counter per unit and one
+    // per partial slot (a group's counter sits at its first part's slot).
+    // The counters come first, in a region sized by a bound that depends on
+    // n_kv_heads and the GPU alone (units <= max(tables, row blocks) x Hkv,
+    // grid <= 2 x SMs): every shape of one model then keeps its counters
+    // inside the same region, which every call leaves at zero, and its
+    // partial states after it, so one workspace serves calls of any shape.
     const size_t slots = units + plan->grid;
+    const size_t units_bound =
+        (size_t)std::max(dec::kMaxTableEntries, plan->row_blocks) * n_kv_heads;
+    const size_t slots_bound = units_bound + 2 * (size_t)device_sm_count();
+    plan->counter_offset = 0;
+    plan->counter_bytes = ((units_bound + slots_bound) * sizeof(int32_t) + 255) & ~size_t(255);
+    plan->partial_offset = plan->counter_bytes;
     const size_t partial = slots * rb_rows * ((size_t)head_dim + 1) * sizeof(float);
-    plan->counter_offset = (partial + 255) & ~size_t(255);
-    plan->counter_bytes = (units + slots) * sizeof(int32_t);
-    plan->workspace = plan->counter_offset + plan->counter_bytes;
+    plan->workspace = plan->partial_offset + partial;
     // How many CTAs can a unit span?  Its chunks are at most the key bound /
     // 16 + 1 and every CTA takes at least kMinChunksPerCta.
     int64_t keys = max_seq_len;
@@ -2008,7 +2017,8 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.grid = plan.grid;
         p.out = static_cast<__nv_bfloat16 *>(out) + qo;
         p.err = err;
-        p.ws_o = static_cast<float *>(workspace);
+        p.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                           plan.partial_offset);
         p.ws_lse = p.ws_o + slots * rb_rows * plan.head_dim;
         p.ws_count = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                  plan.counter_offset);

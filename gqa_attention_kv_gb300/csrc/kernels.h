@@ -107,8 +107,9 @@ struct DecodePlan {
     int row_blocks;       // units along the query rows of one KV head
     int grid;             // CTAs of the split kernel
     int batch_per_launch;
-    size_t workspace;     // bytes of scratch: fp32 partial states + merge counters
+    size_t workspace;     // bytes of scratch: merge counters + fp32 partial states
     size_t counter_offset, counter_bytes;  // the counters, which must be zero between calls
+    size_t partial_offset;                 // the partial states (after the counters)
     bool merge_kernel;    // units spanning very many CTAs are merged by a second kernel
     // Many rows per KV group over a linear slot-major bf16 cache go to the
     // tcgen05 chunk kernel instead (not with a fused rotary embedding, which

@@ -177,15 +177,18 @@ int attn_kv_reference(const void *k, int64_t n, int n_kv_heads, int head_dim, fl
 
 /*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
- * this shape: fp32 partial softmax states of the keys pieces different CTAs
- * handle, plus one counter per (request, KV head, row block).  The same
- * arguments must be passed to attn_decode.  Returns (size_t)-1 for arguments
- * attn_decode would reject.
+ * this shape: merge counters, then fp32 partial softmax states of the key
+ * pieces different CTAs handle.  A call accepts any workspace at least this
+ * large.  Returns (size_t)-1 for arguments attn_decode would reject.
  *
  * The workspace must be zero-filled before its first use; every call that
  * completes leaves the counters at zero again, so a workspace kept for later
  * calls needs no clearing (after a call that reported ATTN_ERR_TIMEOUT,
- * zero it again).
+ * zero it again).  The counters sit at the start, in a region whose size
+ * depends only on n_kv_heads and the GPU (for groups of up to 256 row
+ * blocks), with the partial states after it: one workspace, sized for the
+ * largest shape, serves calls of every batch size, row count and context of
+ * a model without clearing.
  */
 size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_rows,
                                   int n_q_heads, int n_kv_heads, int head_dim, int max_seq_len,

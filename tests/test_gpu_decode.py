@@ -267,3 +267,40 @@ def test_merge_kernel_threshold():
     b, _ = gpu_decode(case, max_seq_len=16512)
     assert torch.equal(a, b), "run-to-run results differ"
     compare(a, ref, "merge kernel threshold")
+
+
+def test_one_workspace_serves_every_shape():
+    """A serving loop keeps one workspace, sized for its largest shape, and
+    calls the decode with whatever batch it has: the merge counters of every
+    shape sit in one region at the start that every call leaves at zero, and
+    the partial states after it, so a call that writes more partial states
+    never leaves garbage where another shape counts."""
+    g = torch.Generator().manual_seed(7500)
+    small = synth.decode_case(7501, LINEAR, 40, 1, 32, 8, 128,
+                              torch.randint(600, 1500, (40,), generator=g).tolist())
+    large = synth.decode_case(7502, LINEAR, 64, 4, 32, 8, 128,
+                              torch.randint(64, 2000, (64,), generator=g).tolist())
+    sizes = []
+    for c in (small, large):
+        sizing = gq.KVCache(c.kind, c.k_cache, c.v_cache, slots_per_seq=c.slots_per_seq)
+        sizes.append(gq.attn_decode_workspace_size(sizing, c.batch, c.q_rows, c.n_q_heads,
+                                                   c.max_seq_len(), 0))
+    ws = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
+
+    def run(case):
+        cache = to_device(case)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gq.attn_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), cache,
+                          err=err)
+        out = gq.attn_decode(case.q.cuda(), cache, case.seq_lens.cuda(), case.positions.cuda(),
+                             case.max_seq_len(), 0, case.scale, workspace=ws, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        return out
+
+    first = run(small)
+    run(large)
+    again = run(small)
+    assert torch.equal(first, again), "a call of another shape disturbed the workspace"
+    ref, _, _ = oracle_decode(small)
+    compare(again, ref, "small batch after a large one, one workspace")
