@@ -9,10 +9,14 @@
 // states are merged in a fixed order.  Both are exact reformulations.
 //
 // GB300 mapping:
-//   * Work unit = (request, KV head, row block): all query rows of the GQA
-//     group (q_rows x group, padded to 16 or 32) are the M dimension of one
-//     mma.sync tile, so every cache position is read from HBM once per group.
-//   * The kernel is persistent: one CTA per SM.  Every CTA computes, from the
+//   * Work unit = (request, KV head, row block): the query rows of the GQA
+//     group (q_rows x group: up to 8 as the N dimension of one mma.sync tile,
+//     up to 32 as its M dimension; a larger group is cut into 16-row units)
+//     share every K/V tile, so every cache position is read from HBM once per
+//     unit.  Groups of 64 or more rows over a linear slot-major bf16 cache
+//     (prefill chunks) go to the tcgen05 chunk kernel (chunk.cu) instead.
+//   * The kernel is persistent: two CTAs per SM (one for 32-row units).
+//     Every CTA computes, from the
 //     device-side seq_lens and positions, how many 16-key chunks each unit
 //     needs, and takes an equal contiguous share of all units' chunks laid end
 //     to end.  The share is balanced whatever the lengths are (ragged batches
@@ -22,8 +26,9 @@
 //     to the output; the others leave fp32 partial states in the workspace
 //     and are merged by the CTAs that store the last ones (atomic counters
 //     tell them): parts in CTA order, eight at a time, then those groups'
-//     states in order.  Launches whose units may span very many CTAs leave
-//     those units to a small merge kernel instead.
+//     states in order.  Launches whose units may span very many CTAs, or
+//     whose few units may each span more than eight, leave those units to a
+//     small merge kernel instead.
 //   * A producer warp streams tiles of 16-key chunks: 64 keys for bf16, 128
 //     for E4M3 (whose rows are half as wide).  A tile whose slots are
 //     consecutive (linear cache; a ring away from its wrap point) is one TMA
@@ -64,7 +69,10 @@ constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per
 // much less real work.
 constexpr int kUnitGapChunks = 12;
 constexpr int kGroupParts = 8;               // partial states merged by one CTA at a time
-constexpr int kMergeWarps = 4;  // merge kernel CTA: small enough to be resident beside the split kernel
+// merge kernel CTA: four warps.  Beside two split CTAs (165 registers, three
+// warps on two of the SM's four sub-partitions) one no longer fits, so merge
+// CTAs take SMs as split CTAs leave them.
+constexpr int kMergeWarps = 4;
 // A launch whose units may span more CTAs than this (by the host's bound)
 // leaves units of more than kGroupParts parts to the merge kernel: there one
 // CTA per query row merges all parts with every load in flight, which beats
