@@ -892,12 +892,17 @@ def main():
                                    "frac": line["decode"]["frac_of_measured_hbm"]}
     cflops = getattr(wl, "chunk_flops", 0.0) * getattr(wl, "layers", 1)
     if getattr(wl, "name", "").startswith("chunked") and dec_ms > 0:
-        # the chunk's rows attend with the decode kernel's legacy mma.sync
-        # tiling: its rate against the measured dense bf16 peak
+        # a prefill chunk is a dense contraction (the tcgen05 chunk kernel):
+        # its rate against the measured dense bf16 peak is the roofline
         ctf = cflops / (dec_ms / K / 1e3) / 1e12
         line["chunk"] = {"value": round(ctf * world, 2), "unit": "TFLOP/s",
                          "flops_per_step": cflops,
                          "frac_of_measured_bf16": round(ctf / peaks["bf16_tflops"], 4)}
+        line["roofline"] = {"kernel": "gqa::chk::chunk_kernel<128> (+ append, merge)",
+                            "bound": "tensor", "achieved": round(ctf, 2),
+                            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": round(ctf / peaks["bf16_tflops"], 4), "traffic": None,
+                            "peak_source": f"{peak_src} bf16_tflops (burst)"}
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline and args.workload == "qwen":
