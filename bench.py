@@ -118,11 +118,14 @@ class ClockSampler:
         except Exception:
             pass
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = None
 
     def start(self):
+        import tempfile
+
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            fd, self.path = tempfile.mkstemp(prefix=f"gqa_clocks_{os.getpid()}_", suffix=".csv")
+            os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -158,6 +161,10 @@ class ClockSampler:
                 rows.append((float(parts[1]), float(parts[2]), float(parts[4]), parts[5:9]))
             except ValueError:
                 continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         loaded = [r for r in rows if r[2] >= 50.0] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
@@ -689,6 +696,103 @@ def cpu_sample(workload_name, steps=1, warmup=0, budget_s=None, max_rows=160):
     return res
 
 
+# The other configurations of the path, measured after the headline step by
+# the default run (fixed step counts: each timed region a fraction of a
+# second).  name -> (what it is, steps)
+SWEEP = [
+    ("voxtral", "Voxtral decoder step: B=1, 1 row, 32/8, D=128, linear cache of 512 keys; "
+                "26 layers per step", 1000),
+    ("encoder", "speech-encoder causal prefill T=750, 32/32, D=64; 32 layers per step", 300),
+    ("encoder-long", "speech-encoder prefill T=1500, window 750; 32 layers per step", 200),
+    ("ring", "ring decode: ring 16,384, window 8,192, B=16, 32/8, D=128", 2000),
+    ("paged", "paged K=4 decode: 64 x 4 rows, 32/8, D=128, block size 16", 2000),
+    ("chunked", "prefill chunk: 2 requests x 29 rows at 14,420..14,448, 28/4, D=128", 2000),
+    ("ring-fp8", "ring decode over an E4M3 cache", 2000),
+    ("paged-fp8", "paged K=4 decode over an E4M3 cache", 2000),
+    ("stream-encoder", "streaming encoder: 4 frames over a 1,500-slot ring, window 750, "
+                       "32/32, D=64; 32 layers per step", 1000),
+]
+
+
+def launch_floor_us(stream, n=26, reps=200):
+    """Per-launch time of n back-to-back one-element torch kernels replayed
+    from a CUDA graph: the floor any launch of this size pays."""
+    import torch
+
+    x = torch.zeros(1, device=stream.device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        x.add_(1.0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                x.add_(1.0)
+        for _ in range(5):
+            g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * n)
+
+
+def measure_config(name, dev, stream, reps, peaks, peak_src, steps, layout=0):
+    """One configuration of SWEEP: its own workload object, warm-up, graph
+    capture and timed steps; returns its sub-object for the JSON line."""
+    import torch
+
+    wl = make_workload(name, dev, layout)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    reps.barrier()
+    clocks.start()
+    groups, total_ms = timed_steps(wl, steps, 3, stream)
+    reps.barrier()
+    clk = clocks.stop()
+    err = int(wl.err.item())
+    if err != 0:
+        raise SystemExit(f"{name}: device error word {err}")
+    dec_ms = reps.reduce_max(groups.get("decode", 0.0))
+    pre_ms = reps.reduce_max(groups.get("prefill", 0.0))
+    total_ms = reps.reduce_max(total_ms)
+    world = reps.world
+    out = {"workload": wl.name, "steps": steps, "ms_per_step": round(total_ms / steps, 5),
+           "launches_per_step": wl.launches_per_step, "clocks": clk}
+    if pre_ms > 0:
+        fl = wl.prefill_flops_per_step()
+        tf = fl / (pre_ms / steps / 1e3) / 1e12
+        out.update({"value": round(world * tf, 2), "unit": "TFLOP/s", "flops_per_step": fl,
+                    "bound": "tensor", "peak": peaks["bf16_tflops"],
+                    "frac_of_measured_peak": round(tf / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{peak_src} bf16_tflops (burst)"})
+    else:
+        by = wl.decode_bytes_per_step()
+        gbs = by / (dec_ms / steps / 1e3) / 1e9
+        out.update({"value": round(world * gbs, 2), "unit": "GB/s", "bytes_per_step": int(by),
+                    "bound": "hbm", "peak": peaks["hbm_gbs"],
+                    "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4),
+                    "frac_of_nominal_hbm": round(gbs / NOMINAL_HBM_GBS, 4),
+                    "peak_source": f"{peak_src} hbm_gbs",
+                    "us_per_launch": round(1e3 * dec_ms / steps / wl.launches_per_step, 3)})
+        cf = getattr(wl, "chunk_flops", 0.0) * getattr(wl, "layers", 1)
+        if name == "chunked" and cf:
+            ctf = cf / (dec_ms / steps / 1e3) / 1e12
+            out["chunk"] = {"value": round(world * ctf, 2), "unit": "TFLOP/s",
+                            "flops_per_step": cf, "bound": "tensor",
+                            "frac_of_measured_bf16": round(ctf / peaks["bf16_tflops"], 4)}
+    if name == "voxtral":
+        out["launch_floor_us"] = round(launch_floor_us(stream), 3)
+        out["launch_floor"] = ("per-launch time of 26 one-element torch kernels replayed "
+                               "from one CUDA graph, CUDA events")
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
 def dist_env():
     """(rank, local_rank, world_size) as torchrun exports them (1 process: 0, 0, 1)."""
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
@@ -757,6 +861,8 @@ def main():
                              "qwen-prefill", "prefill-8k", "chunked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="default workload only: skip the other configurations")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     rank, local_rank, world = dist_env()
@@ -830,6 +936,14 @@ def main():
                "h2d_bytes_per_step": wl.h2d_prefill + wl.h2d_decode,
                "d2h_bytes_per_step": wl.d2h_prefill + wl.d2h_decode,
                "ms_per_step": round(reduce_max(etot) / K, 4)}
+
+    sweep = None
+    if args.workload == "qwen" and not args.no_sweep:
+        sweep = {}
+        for name, what, steps in SWEEP:
+            sweep[name] = {"config": what} | measure_config(
+                name, dev, stream, reps, peaks, peak_src, steps,
+                1 if args.layout == "bhsd" else 0)
 
     if rank != 0:
         reps.close()
@@ -905,6 +1019,8 @@ def main():
                             "peak_source": f"{peak_src} bf16_tflops (burst)"}
     if e2e is not None:
         line["e2e"] = e2e
+    if sweep is not None:
+        line["configs"] = sweep
     if world == 1 and not args.no_cpu_baseline and args.workload == "qwen":
         r = cpu_sample(args.workload, steps=1, warmup=0)
         line["cpu_baseline"] = {"value": round(r["decode_gbs"], 4), "unit": "GB/s",

@@ -210,11 +210,14 @@ int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_row
     return splits * (plan.merge_kernel ? 2 : 1);
 }
 
-int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
-                const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
-                int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,
-                void *workspace, size_t workspace_bytes, int32_t *err_word,
-                attn_stream_t stream) {
+}  // extern "C"
+
+namespace gqa {
+
+int validate_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
+                    const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
+                    int n_q_heads, int n_kv_heads, int head_dim, float scale, const void *out,
+                    DecodePlan *plan) {
     int rc = check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim,
                                 max_seq_len, window);
     if (rc != ATTN_OK) return rc;
@@ -224,9 +227,24 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
     if (cache->kind == ATTN_CACHE_PAGED && !cache->block_table) return ATTN_ERR_NULL;
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache->k) || !aligned16(cache->v))
         return ATTN_ERR_ALIGN;
+    plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window, plan);
+    return ATTN_OK;
+}
+
+}  // namespace gqa
+
+extern "C" {
+
+int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
+                const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
+                int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,
+                void *workspace, size_t workspace_bytes, int32_t *err_word,
+                attn_stream_t stream) {
     gqa::DecodePlan plan;
-    gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
-                     &plan);
+    const int rc = gqa::validate_decode(q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
+                                        window, n_q_heads, n_kv_heads, head_dim, scale, out,
+                                        &plan);
+    if (rc != ATTN_OK || batch == 0) return rc;
     if (plan.workspace > 0) {
         if (!workspace) return ATTN_ERR_NULL;
         if (workspace_bytes < plan.workspace) return ATTN_ERR_WORKSPACE;

@@ -240,6 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++vj;
                 }
             }
+            // No copy may still be landing when the CTA exits: the last K and
+            // V tile of each stage have completed (normally the MMAs have
+            // read them already; after a wait that gave up, bounded too).
+            bool landed = true;
+            for (int j = max(0, kj - C::kKStages); landed && j < kj; ++j)
+                landed = mbar_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1, p.err);
+            for (int j = max(0, vj - C::kVStages); landed && j < vj; ++j)
+                landed = mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, p.err);
+            if (landed) mbar_wait(q_full, 0, p.err);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer

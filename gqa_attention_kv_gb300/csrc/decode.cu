@@ -913,6 +913,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         }
         // the gathered rows of this thread must land before it leaves
         asm volatile("cp.async.wait_all;" ::: "memory");
+        // No box may still be landing when the CTA exits: the last tile of
+        // each stage has completed (normally the consumers have waited for it
+        // already; after a wait that gave up, this wait is bounded too).
+        if (lane == 0)
+            for (int t = max(0, tile - kStages); t < tile; ++t)
+                if (!mbar_wait(&full[t % kStages], (t / kStages) & 1, p.err)) break;
         __syncwarp();
         return;
     }

@@ -122,6 +122,13 @@ struct DecodePlan {
 int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads, int n_kv_heads,
                 int head_dim, int max_seq_len, int window, DecodePlan *plan);
 
+// Every host-side check attn_decode makes before it looks at the workspace;
+// on success (and batch > 0) fills *plan.  Returns the attn_status.
+int validate_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
+                    const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
+                    int n_q_heads, int n_kv_heads, int head_dim, float scale, const void *out,
+                    DecodePlan *plan);
+
 // k_new / v_new / slot_mapping non-null: the step's rows are appended by the
 // same launch (attn_decode_append).
 int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *cache,

@@ -12,24 +12,27 @@
 // 256 query rows, and the two tiles ping-pong: while one softmax warpgroup
 // works on its scores the tensor core computes the other tile's QK^T and PV.
 //
-//   warp 0      TMA producer: Q0, Q1 once; then K tiles (3-stage ring) and V
-//               tiles (2-stage ring) of 128 keys, 128-byte swizzled, through
+//   warp 0      TMA producer: Q0, Q1 once; then K tiles (2-stage ring) and V
+//               tiles (3-stage ring) of 128 keys, 128-byte swizzled, through
 //               3D tensor maps (rows past the sequence end are zero-filled).
 //   warp 1      allocates all 512 TMEM columns; lane 0 issues every
-//               tcgen05.mma (kind::f16, bf16 in, fp32 accumulate):
-//                 S_a = Q_a K^T            M=128 N=128 K=D   A, B from smem
-//                 O_a += P_a V (hi, lo)    M=128 N=D   K=128 A from TMEM
+//               tcgen05.mma (kind::f16, fp32 accumulate):
+//                 S_a = Q_a K^T            M=128 N=128 K=D   bf16, A, B from smem
+//                 O_a += P_a V             M=128 N=D   K=128 f16, A from TMEM
 //               TMEM columns: S_a/P_a at 128a, O_a at 256 + D a.
-//   warps 2..3  idle (they complete the first warpgroup).
+//   warps 2..3  rewrite every V tile in place from bf16 to f16 (same
+//               positions, so the swizzle is unchanged) before P V reads it.
 //   warps 4..7  softmax for Q0, warps 8..11 for Q1.  Thread = query row = TMEM
 //               lane.  tcgen05.ld of its S row, mask (only on tiles that
 //               cross the diagonal or the window edge), running max / sum in
-//               fp32, P written back over its S columns as two bf16 halves
-//               (hi + lo, vibevoice.c "Attention backends": one rounding of P
-//               is too coarse), O rescaled in TMEM only when the running max
-//               grew by more than 2^8 (the result is unchanged; rescaling is
-//               lazy).  P is released in two halves of 64 keys, so PV on
-//               the first half runs while the second is exponentiated.
+//               fp32, P written back over its S columns rounded once to f16
+//               (vibevoice.c, "Attention backends": P V takes its operands in
+//               FP16, because one bf16 rounding of P is too coarse; f16 keeps
+//               11 significant bits), O rescaled in TMEM only when the running
+//               max grew by more than 2^8 (the result is unchanged; rescaling
+//               is lazy; P stays below 2^8).  P is released in two halves of
+//               64 keys, so PV on the first half runs while the second is
+//               exponentiated.
 //               Epilogue: O / l -> bf16 -> shared (over Q_a) -> TMA store,
 //               clipped at the sequence end.
 //
@@ -52,12 +55,12 @@ constexpr int kBM = 128;          // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;          // keys per tile
 constexpr int kThreads = 384;     // 3 warpgroups
 // Registers: launched at 168 per thread (384 x 168 = 64,512; three warps of
-// 168 fit one SM sub-partition's 16,384).  The TMA/MMA warpgroup then drops
-// to 72 and the two softmax warpgroups rise to 216: 4x32x72 + 8x32x216 =
-// 64,512, exactly the launch total, and 72 + 216 + 216 <= 512 per
-// sub-partition lane slot.
-constexpr uint32_t kRegsControl = 72;
-constexpr uint32_t kRegsSoftmax = 216;
+// 168 fit one SM sub-partition's 16,384).  The TMA / MMA / V-conversion
+// warpgroup then drops to 88 and the two softmax warpgroups rise to 208:
+// 4x32x88 + 8x32x208 = 64,512, exactly the launch total, and 88 + 208 + 208
+// <= 512 per sub-partition lane slot.
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -73,7 +76,7 @@ struct Cfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
     static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 10;
+    static constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 10;
     static constexpr size_t kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 };
 
@@ -106,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + 2;                    // [2 tiles][2 key halves]
     uint64_t *o_done = p_full + 4;
     uint64_t *mma_done = o_done + 1;
+    uint64_t *v_conv = mma_done + 1;                  // [kVStages]: V tile now f16
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
+            mbar_init(&v_conv[s], 64);  // every thread of warps 2 and 3
         }
         mbar_init(q_full, 1);
         mbar_init(&s_full[0], 1);
@@ -196,12 +201,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++vj;
                 }
             }
+            // No copy may still be landing when the CTA exits: the last K and
+            // V tile of each stage have completed (normally the MMAs have
+            // read them already; after a wait that gave up, bounded too).
+            bool landed = true;
+            for (int j = max(0, kj - C::kKStages); landed && j < kj; ++j)
+                landed = mbar_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1, p.err);
+            for (int j = max(0, vj - C::kVStages); landed && j < vj; ++j)
+                landed = mbar_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1, p.err);
+            if (landed) mbar_wait(q_full, 0, p.err);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, 0, 1);
+            constexpr uint32_t idesc_pv = idesc_f16_f32(kBM, HD, 0, 1);
             // Descriptors are built once; a k-step adds its byte offset >> 4 to
             // the start-address field (no carry: shared addresses < 256 KB).
             const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
@@ -218,20 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&s_full[a]);
             };
-            // O_a += P_a V for keys 64h .. 64h+63 of the tile (P hi, then P lo)
+            // O_a += P_a V for keys 64h .. 64h+63 of the tile (P as f16: 16
+            // keys per 8 TMEM columns)
             auto issue_pv_half = [&](int a, int vst, int hh, bool first) {
                 const uint64_t vd = v_desc0 + (uint64_t)((vst * C::kVBytes) >> 4);
                 const uint32_t p_tmem = tmem + a * 128;
                 const uint32_t o_tmem = tmem + 256 + a * HD;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
-                        const int kk = hh * (kBN / 32) + k4;
-                        tc_mma_ts(o_tmem, p_tmem + part * 64 + kk * 8,
-                                  vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
-                                  (!first || k4 > 0 || part > 0) ? 1u : 0u);
-                    }
+                for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                    const int kk = hh * (kBN / 32) + k4;
+                    tc_mma_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                              idesc_pv, (!first || k4 > 0) ? 1u : 0u);
+                }
             };
             bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
             if (ok && n_kt > 0) {
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage indices and phases of the K and V rings, stepped without division
             int vst = 0, vph = 0, kst = 0, kph = 0;
             for (int j = 0; j < n_kt && ok; ++j) {
-                ok = mbar_wait(&v_full[vst], vph, p.err);
+                ok = mbar_wait(&v_conv[vst], vph, p.err);  // V(j) landed and is f16
                 const bool more = j + 1 < n_kt;
                 if (more && ++kst == C::kKStages) {
                     kst = 0;
@@ -278,6 +290,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // All issued MMAs complete before TMEM is released.
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, p.err);
+        }
+    } else {
+        // ---------------------------------------------------------- V to f16
+        // Each V tile is rewritten in place, bf16 -> f16 (exact for
+        // magnitudes in [2^-14, 2^16); below that f16 keeps 2^-24 absolute
+        // precision).  A magnitude of 2^16 or more has no f16: it saturates to
+        // 65504 and the error word gets ATTN_ERR_UNSUPPORTED.  The writes are
+        // made visible to the tensor core's proxy before the arrive.
+        const int ct = threadIdx.x - 64;  // 0 .. 63
+        int vst = 0, vph = 0;
+        bool ok = true;
+        for (int j = 0; j < n_kt && ok; ++j) {
+            ok = mbar_wait(&v_full[vst], vph, p.err);
+            __syncwarp();
+            if (!ok) break;
+            const uint32_t base = smem_u32(sV + vst * C::kVBytes);
+            float amax = 0.f;
+#pragma unroll 4
+            for (int i = ct; i < C::kVBytes / 16; i += 64) {
+                uint4 w = ld_shared_v4(base + i * 16);
+                uint32_t *u = &w.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = __uint_as_float(u[e] << 16);
+                    const float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
+                    amax = max3(amax, fabsf(x0), fabsf(x1));
+                    u[e] = pack_f16x2_sat(x0, x1);
+                }
+                st_shared_v4(base + i * 16, w);
+            }
+            if (!(amax < 65536.f)) report_error(p.err, ATTN_ERR_UNSUPPORTED);
+            fence_proxy_async_smem();
+            mbar_arrive(&v_conv[vst]);
+            if (++vst == C::kVStages) {
+                vst = 0;
+                vph ^= 1;
+            }
         }
     }
     } else {
@@ -353,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < kBN; c0 += 32) {
-                uint32_t hi[16], lo[16];
+                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float x0, x1;
@@ -361,11 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = fast_exp2(x0);
                     const float p1 = fast_exp2(x1);
                     add2(sum0, sum1, sum0, sum1, p0, p1);
-                    split_trunc_bf16x2(p0, p1, hi[e], lo[e]);
+                    pk[e] = pack_f16x2(p0, p1);
                 }
-                // P over its own S columns: hi at [0, 64), lo at [64, 128)
-                tmem_st_32x32b_x16(s_tmem + c0 / 2, hi);
-                tmem_st_32x32b_x16(s_tmem + 64 + c0 / 2, lo);
+                // P over its own S columns: 32 keys in 16 columns
+                tmem_st_32x32b_x16(s_tmem + c0 / 2, pk);
                 if (c0 == kBN / 2 - 32 || c0 == kBN - 32) {
                     // keys of this half are in TMEM: let PV start on them
                     tmem_wait_st();

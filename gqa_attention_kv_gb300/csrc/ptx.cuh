@@ -267,9 +267,28 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return d;
 }
 
+// Two fp32 values -> f16x2 (lo in the low half), rounded to nearest even;
+// magnitudes beyond the largest finite f16 become +-65504, not infinity.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // bf16x2 -> f16x2, each value rounded to the nearest f16.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// bf16x2 -> f16x2 as bf16x2_to_f16x2, magnitudes beyond 65504 saturated.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w) {
+    return pack_f16x2_sat(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 // ------------------------------------------------------------ 8-bit E4M3 floats
@@ -474,6 +493,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, f16 A and B (the
+// format fields hold 0), otherwise as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4)  // D format: fp32
+           | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,

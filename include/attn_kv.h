@@ -62,7 +62,8 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_NULL = 1,        /* a required pointer is NULL */
     ATTN_ERR_SHAPE = 2,       /* sizes inconsistent or out of range */
-    ATTN_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
+    ATTN_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement; on the device
+                                 (err_word): a value outside the range a kernel supports */
     ATTN_ERR_WORKSPACE = 4,   /* workspace smaller than attn_decode_workspace_size */
     ATTN_ERR_BOUNDS = 5,      /* device: slot / page / position outside its buffer */
     ATTN_ERR_TIMEOUT = 6,     /* device: a bounded wait gave up */
@@ -320,13 +321,18 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
  *
  *   Returns ATTN_ERR_WORKSPACE, before any launch, when
  *   attn_decode_workspace_size(...) for these arguments exceeds that size;
- *   otherwise the same statuses as attn_decode.
- *   The first call on a device looks up the array's device address; make it
- *   before capturing a stream into a CUDA graph.
+ *   otherwise the same statuses as attn_decode, every host check made before
+ *   anything is enqueued.
+ *   The array used is the CURRENT device's: the stream must belong to the
+ *   current device.  The first call on a device looks up the array's device
+ *   address, which belongs to the device's current context (a replaced
+ *   context, after cudaDeviceReset for instance, is looked up again); make
+ *   that first call before capturing a stream into a CUDA graph.
  *   All calls share the array: calls whose kernels overlap on the GPU race
  *   and give wrong results, so order them (one stream, or events).  Each
- *   call clears the part of the array that must start at zero (a stream
- *   memset, no allocation) before its kernel runs.
+ *   call enqueues one memset on the stream (no allocation), clearing the
+ *   part of the array that must start at zero, before its kernels; that
+ *   memset is not counted by attn_decode_kernel_launches.
  */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int attn_decode_noalloc(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
@@ -348,6 +354,13 @@ int attn_decode_noalloc(const void *q, const attn_kv_cache *cache, const int32_t
  *   Query i of a sequence attends keys t of the same sequence with t <= i and,
  *   when window > 0, i - t < window.  scale (finite, > 0) multiplies q.k.
  *   out  bf16 [batch, seq_len, n_q_heads, head_dim], device, rounded once.
+ *   Q K^T takes q and k as bf16.  P V takes the softmax weights rounded once to
+ *   f16 and v converted to f16 (vibevoice.c, "Attention backends": P V in
+ *   FP16, since one bf16 rounding of P is too coarse); fp32 accumulation.  The
+ *   conversion of v is exact for magnitudes in [2^-14, 2^16) and keeps an
+ *   absolute precision of 2^-24 below; a v element of magnitude 2^16 or more
+ *   has no f16 value: it is saturated to +-65504 and ATTN_ERR_UNSUPPORTED is
+ *   stored in *err_word.
  */
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,
                  int n_q_heads, int n_kv_heads, int head_dim, float scale, void *out,

@@ -87,3 +87,40 @@ def test_deterministic():
     b = gq.attn_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), 0, p.scale)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_large_values_within_f16_range():
+    """V with magnitudes up to ~2^15 (N(0,1) x 2^12): converting V to f16 for
+    P V is exact there and a power-of-two scale commutes with every rounding
+    of the path, so each output is exactly 2^12 times the unscaled one, and
+    the unscaled output meets the stated tolerance."""
+    p = synth.prefill_case(410, 1, 300, 8, 2, 128)
+    dev = "cuda"
+    q, k, v = p.q.to(dev), p.k.to(dev), p.v.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    small = gq.attn_prefill(q, k, v, 0, p.scale, err=err)
+    big = gq.attn_prefill(q, k, v * 4096.0, 0, p.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(big, small * 4096.0)
+    rc, ref = oracle.prefill(bits(p.q), bits(p.k), bits(p.v), 0, p.scale)
+    assert rc == 0
+    compare(small, ref, "V unscaled")
+
+
+def test_v_beyond_f16_is_reported():
+    """A V element of magnitude 2^16 or more has no f16 value: the kernel
+    saturates it, keeps every output finite and stores ATTN_ERR_UNSUPPORTED
+    in the error word (it never faults)."""
+    p = synth.prefill_case(411, 1, 200, 4, 4, 64)
+    p.v[0, 150, 2, 7] = 1.0e5
+    dev = "cuda"
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gq.attn_prefill(p.q.to(dev), p.k.to(dev), p.v.to(dev), 0, p.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == gq.ATTN_ERR_UNSUPPORTED
+    assert torch.isfinite(out.float()).all()
+    # rows before position 150 never see the large value: unchanged parity
+    rc, ref = oracle.prefill(bits(p.q), bits(p.k), bits(p.v), 0, p.scale, rows=list(range(150)))
+    assert rc == 0
+    compare(out[:, :150], ref, "rows before the large value")
