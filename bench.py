@@ -252,7 +252,7 @@ class QwenWorkload(Workload):
         # prefill, prompt append, per decode the kernels the library plans
         # (split kernel + merge kernel at these long contexts)
         self.launches_per_step = 1 + 1 + len(self.CONTEXTS) * gq.attn_decode_kernel_launches(
-            self.caches[0], self.B, 1, Hq, self.max_seq, 0, with_append=True)
+            self.caches[0], self.B, 1, Hq, self.max_seq, 0, with_append=True, tables_early=True)
         self.describe = {"workload": self.name, "model": "Qwen2-7B-shaped decoder attention",
                          "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D,
                          "prefill_tokens": self.T, "decode_batch": self.B, "q_rows": 1,
@@ -431,7 +431,7 @@ class DecodeOnlyWorkload(Workload):
         # the step's append fused into the decode launch (bf16 and FP8)
         self.launches_per_step = gq.attn_decode_kernel_launches(
             self.caches[0], base.batch, base.q_rows, base.n_q_heads, self.max_seq, base.window,
-            with_append=True)
+            with_append=True, tables_early=True)
         # valid keys per (request, row) summed over rows' union per request
         seq = base.seq_lens.cpu().tolist()
         keys = 0
@@ -1000,6 +1000,14 @@ def main():
                            "frac_of_measured_bf16": round(pre_tf / world / peaks["bf16_tflops"], 4),
                            "frac_of_measured_bf16_sustained":
                                round(pre_tf / world / peaks["bf16_tflops_sustained"], 4)}
+    if app_ms > 0 and hasattr(wl, "prompt_append_bytes"):
+        # the prompt's 14,449 rows appended (K and V read from the prefill
+        # inputs, written to their slots): an HBM-bound copy
+        ab = wl.prompt_append_bytes()
+        agbs = ab / (app_ms / K / 1e3) / 1e9
+        line["append"] = {"value": round(world * agbs, 2), "unit": "GB/s", "bytes_per_step": ab,
+                          "kernel": "gqa::kv_append_kernel",
+                          "frac_of_measured_hbm": round(agbs / peaks["hbm_gbs"], 4)}
     if dec_gbs is not None and pre_tf is not None:
         line["roofline_decode"] = {"bound": "hbm", "achieved": line["decode"]["value"] / world,
                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",

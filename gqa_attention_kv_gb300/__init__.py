@@ -67,7 +67,7 @@ def lib():
             L.attn_decode_workspace_size.argtypes = [cp, i32, i32, i32, i32, i32, i32, i32]
             L.attn_decode_workspace_size.restype = sz
             L.attn_decode_kernel_launches.argtypes = [cp, i32, i32, i32, i32, i32, i32, i32,
-                                                      i32, i32]
+                                                      i32, i32, ctypes.c_uint]
             L.attn_decode_kernel_launches.restype = i32
             L.attn_decode.argtypes = [p, cp, p, p, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, p, p, sz, p, p]
@@ -195,14 +195,16 @@ def attn_decode_workspace_size(cache: KVCache, batch, q_rows, n_q_heads, max_seq
 
 
 def attn_decode_kernel_launches(cache: KVCache, batch, q_rows, n_q_heads, max_seq_len,
-                                window=0, with_append=False, with_rope=False) -> int:
+                                window=0, with_append=False, with_rope=False,
+                                tables_early=False) -> int:
     """Kernels one attn_decode (with_append: attn_decode_append; with_rope:
-    with a rotary embedding) call of this shape launches (host-side plan;
-    nothing runs on the device)."""
+    with a rotary embedding; tables_early: with ATTN_DECODE_TABLES_EARLY)
+    call of this shape launches (host-side plan; nothing runs on the device)."""
     c = cache.struct()
     n = lib().attn_decode_kernel_launches(ctypes.byref(c), batch, q_rows, n_q_heads,
                                           cache.n_kv_heads, cache.head_dim, max_seq_len, window,
-                                          int(bool(with_append)), int(bool(with_rope)))
+                                          int(bool(with_append)), int(bool(with_rope)),
+                                          ATTN_DECODE_TABLES_EARLY if tables_early else 0)
     if n < 0:
         raise AttnError(ATTN_ERR_SHAPE, "attn_decode_kernel_launches")
     return int(n)

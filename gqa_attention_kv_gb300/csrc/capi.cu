@@ -196,7 +196,8 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
 
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
                                 int n_kv_heads, int head_dim, int max_seq_len, int window,
-                                int with_append, int with_rope) {
+                                int with_append, int with_rope, unsigned flags) {
+    if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return -1;
     if (check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len,
                            window) != ATTN_OK)
         return -1;

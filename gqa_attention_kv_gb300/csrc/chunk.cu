@@ -22,8 +22,9 @@
 //
 // The warp roles, rings, TMEM columns and the ping-pong of the two tiles are
 // those of the prefill kernel (prefill.cu): warp 0 issues TMA, warp 1 the
-// tcgen05.mma (S_a = Q_a K^T, O_a += P_a V with P as bf16 hi + lo halves),
-// warps 4..11 run the softmax of one tile row per thread.
+// tcgen05.mma (S_a = Q_a K^T in bf16, O_a += P_a V in f16 with P rounded once
+// and V rewritten to f16 in shared memory by warps 2 and 3), warps 4..11 run
+// the softmax of one tile row per thread.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,11 +41,11 @@ namespace chk {
 constexpr int kBM = 128;       // rows per tile (two tiles per CTA)
 constexpr int kBN = 128;       // keys per tile
 constexpr int kThreads = 384;  // 3 warpgroups
-// Registers as in the prefill kernel: launched at 168 a thread, the TMA/MMA
-// warpgroup drops to 72 and the two softmax warpgroups rise to 216
-// (4x32x72 + 8x32x216 = 384x168).
-constexpr uint32_t kRegsControl = 72;
-constexpr uint32_t kRegsSoftmax = 216;
+// Registers as in the prefill kernel: launched at 168 a thread, the TMA / MMA
+// / V-conversion warpgroup drops to 88 and the two softmax warpgroups rise to
+// 208 (4x32x88 + 8x32x208 = 384x168).
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMergeWarps = 8;
@@ -61,7 +62,7 @@ struct Cfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
     static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 10;
+    static constexpr int kNumBars = 2 * kKStages + 3 * kVStages + 10;
     static constexpr size_t kSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 };
 
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + 2;  // [2 tiles][2 key halves]
     uint64_t *o_done = p_full + 4;
     uint64_t *mma_done = o_done + 1;
+    uint64_t *v_conv = mma_done + 1;  // [kVStages]: V tile now f16
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
     __shared__ int s_pos[2];  // min and max position of the CTA's rows
 
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
+            mbar_init(&v_conv[s], 64);  // every thread of warps 2 and 3
         }
         mbar_init(q_full, 1);
         mbar_init(&s_full[0], 1);
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, 0, 1);
+            constexpr uint32_t idesc_pv = idesc_f16_f32(kBM, HD, 0, 1);
             const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sV), kBN * 128, 1024);
@@ -273,14 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t p_tmem = tmem + a * 128;
                 const uint32_t o_tmem = tmem + 256 + a * HD;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
-                        const int kk = hh * (kBN / 32) + k4;
-                        tc_mma_ts(o_tmem, p_tmem + part * 64 + kk * 8,
-                                  vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
-                                  (!first || k4 > 0 || part > 0) ? 1u : 0u);
-                    }
+                for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                    const int kk = hh * (kBN / 32) + k4;
+                    tc_mma_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                              idesc_pv, (!first || k4 > 0) ? 1u : 0u);
+                }
             };
             bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
             if (ok && n_kt > 0) {
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int vst = 0, vph = 0, kst = 0, kph = 0;
             for (int j = 0; j < n_kt && ok; ++j) {
-                ok = mbar_wait(&v_full[vst], vph, p.err);
+                ok = mbar_wait(&v_conv[vst], vph, p.err);  // V(j) landed and is f16
                 const bool more = j + 1 < n_kt;
                 if (more && ++kst == C::kKStages) {
                     kst = 0;
@@ -324,6 +324,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(o_done);
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, p.err);
+        }
+    } else {
+        // ---------------------------------------------------------- V to f16
+        // as in the prefill kernel: each V tile rewritten in place, a
+        // magnitude of 2^16 or more saturated and reported
+        const int ct = threadIdx.x - 64;  // 0 .. 63
+        int vst = 0, vph = 0;
+        bool ok = true;
+        for (int j = 0; j < n_kt && ok; ++j) {
+            ok = mbar_wait(&v_full[vst], vph, p.err);
+            __syncwarp();
+            if (!ok) break;
+            const uint32_t base = smem_u32(sV + vst * C::kVBytes);
+            float amax = 0.f;
+#pragma unroll 4
+            for (int i = ct; i < C::kVBytes / 16; i += 64) {
+                uint4 w = ld_shared_v4(base + i * 16);
+                uint32_t *u = &w.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = __uint_as_float(u[e] << 16);
+                    const float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
+                    amax = max3(amax, fabsf(x0), fabsf(x1));
+                    u[e] = pack_f16x2_sat(x0, x1);
+                }
+                st_shared_v4(base + i * 16, w);
+            }
+            if (!(amax < 65536.f)) report_error(p.err, ATTN_ERR_UNSUPPORTED);
+            fence_proxy_async_smem();
+            mbar_arrive(&v_conv[vst]);
+            if (++vst == C::kVStages) {
+                vst = 0;
+                vph ^= 1;
+            }
         }
     }
     } else {
@@ -400,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < kBN; c0 += 32) {
-                uint32_t hi[16], lo[16];
+                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float x0, x1;
@@ -408,10 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = fast_exp2(x0);
                     const float p1 = fast_exp2(x1);
                     add2(sum0, sum1, sum0, sum1, p0, p1);
-                    split_trunc_bf16x2(p0, p1, hi[e], lo[e]);
+                    pk[e] = pack_f16x2(p0, p1);
                 }
-                tmem_st_32x32b_x16(s_tmem + c0 / 2, hi);
-                tmem_st_32x32b_x16(s_tmem + 64 + c0 / 2, lo);
+                // P over its own S columns: 32 keys in 16 columns
+                tmem_st_32x32b_x16(s_tmem + c0 / 2, pk);
                 if (c0 == kBN / 2 - 32 || c0 == kBN - 32) {
                     tmem_wait_st();
                     tc_fence_before();

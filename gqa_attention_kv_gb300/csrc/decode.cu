@@ -1648,8 +1648,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     // a unit's last group (per-unit counter) merges the groups in order into
     // the bf16 output.  A unit of at most kGroupParts parts is one group
     // merged straight to the output.  The ring is drained, so the stages
-    // are free for staging.
-    __threadfence();
+    // are free for staging.  Ordering: the consumer barrier puts every
+    // thread's partial stores before thread 0's counter update, whose release
+    // (gpu scope, cumulative) publishes them; the CTA whose update completes a
+    // group acquires the others' by the same update, and the barrier after it
+    // orders its threads' loads after that acquire.
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
     float *sl = reinterpret_cast<float *>(stages);  // [parts][RB] log-sum-exps
     for (int k = 0; k < n_pend; ++k) {
@@ -1662,27 +1665,25 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         // reading one flag never sees the next decision
         if (ctid == 0) {
             int32_t *cnt = n <= kGroupParts ? p.ws_count + u.unit : p.ws_gcount + gslot;
-            s_last[2 * k] = atomicAdd(cnt, 1) == gl - gf ? 1 : 0;
+            s_last[2 * k] = atom_add_acq_rel_gpu(cnt, 1) == gl - gf ? 1 : 0;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         if (!s_last[2 * k]) continue;  // uniform across the consumer warps
-        __threadfence();
         if (n <= kGroupParts) {
             merge_partials<HD, RB>(p, u, gslot, 1, n, true, sl, ctid);
             if (ctid == 0) p.ws_count[u.unit] = 0;  // ready for the next call
             continue;
         }
         merge_partials<HD, RB>(p, u, gslot, 1, gl - gf + 1, false, sl, ctid);
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+        // (merge_partials ends with the consumer barrier: its stores precede
+        // the release below)
         const int groups = (n + kGroupParts - 1) / kGroupParts;
         if (ctid == 0) {
             p.ws_gcount[gslot] = 0;
-            s_last[2 * k + 1] = atomicAdd(p.ws_count + u.unit, 1) == groups - 1 ? 1 : 0;
+            s_last[2 * k + 1] = atom_add_acq_rel_gpu(p.ws_count + u.unit, 1) == groups - 1 ? 1 : 0;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         if (!s_last[2 * k + 1]) continue;
-        __threadfence();
         merge_partials<HD, RB>(p, u, (int64_t)u.unit + u.first, kGroupParts, groups, true, sl,
                                ctid);
         if (ctid == 0) p.ws_count[u.unit] = 0;
@@ -1884,6 +1885,20 @@ int plan_decode(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads
     plan->batch_per_launch = std::max(1, dec::kMaxTableEntries / plan->row_blocks);
     plan->batch_per_launch = std::min(plan->batch_per_launch, std::max(batch, 1));
     const size_t units = (size_t)plan->batch_per_launch * n_kv_heads * plan->row_blocks;
+    // A launch whose keys (by the host bound) give fewer than kMinChunksPerCta
+    // chunks to every CTA of the full grid launches only the CTAs that can get
+    // work: the others would still be launched, plan and wait for the previous
+    // kernel, and hold their SMs from the next launch meanwhile.
+    {
+        int64_t keys_bound = max_seq_len;
+        if (window > 0) keys_bound = std::min<int64_t>(keys_bound, (int64_t)window + q_rows - 1);
+        if (cache->kind == ATTN_CACHE_RING)
+            keys_bound = std::min<int64_t>(keys_bound, cache->slots_per_seq);
+        const int64_t chunks_bound =
+            (int64_t)units * ((keys_bound + dec::kChunk - 1) / dec::kChunk + 1 + dec::kUnitGapChunks);
+        const int64_t needed = (chunks_bound + dec::kMinChunksPerCta - 1) / dec::kMinChunksPerCta;
+        plan->grid = (int)std::max<int64_t>(1, std::min<int64_t>(plan->grid, needed));
+    }
     // partial slots: unit + cta < units + grid; one counter per unit and one
     // per partial slot (a group's counter sits at its first part's slot).
     // The counters come first, in a region sized by a bound that depends on

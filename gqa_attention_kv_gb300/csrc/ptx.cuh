@@ -86,6 +86,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return true;
 }
 
+// Atomic add with acquire-release semantics at GPU scope: it publishes the
+// memory operations ordered before it (a CTA barrier before it orders the
+// other threads' too) and makes visible those published by earlier updates of
+// the same word.  Returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ------------------------------------------------------ register reallocation
 // Every warp of a warpgroup executes these together.  The launch's register
 // total must cover the sum of the warpgroups' new shares.

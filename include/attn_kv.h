@@ -199,10 +199,11 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  * attn_decode_kernel_launches -- how many kernels one call with these
  * arguments launches on the stream (host only; nothing is launched):
  * attn_decode when with_append is 0, attn_decode_append when it is 1, with a
- * rotary embedding when with_rope is 1.  A split-kernel call launches one
- * split kernel per group of requests the shared-memory tables hold, each
- * followed by the merge kernel when units of this shape may be split over
- * enough CTAs to need it.  A group of 64 or more query rows (q_rows x
+ * rotary embedding when with_rope is 1, with attn_decode_append's flags (no
+ * flag changes the count today; an unknown flag gives -1).  A split-kernel
+ * call launches one split kernel per group of requests the shared-memory
+ * tables hold, each followed by the merge kernel when units of this shape may
+ * be split over enough CTAs to need it.  A group of 64 or more query rows (q_rows x
  * n_q_heads / n_kv_heads) over a linear slot-major bf16 cache, without a
  * rotary embedding, is a prefill chunk: the append kernel (attn_decode_append
  * only), the tcgen05 chunk kernel, and its merge kernel when the key range is
@@ -211,7 +212,7 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  */
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
                                 int n_kv_heads, int head_dim, int max_seq_len, int window,
-                                int with_append, int with_rope);
+                                int with_append, int with_rope, unsigned flags);
 
 /*
  * attn_decode -- causal decode attention for q_rows query rows per request.
@@ -252,6 +253,11 @@ int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_row
  *   and values to f16 (exact), takes q in f16 (|q| must stay below 65504;
  *   magnitudes under 2^-14 lose precision) and the softmax weights in f16,
  *   and accumulates in fp32.
+ *   A group of 64 or more query rows (q_rows x n_q_heads / n_kv_heads) over a
+ *   linear slot-major bf16 cache is a prefill chunk and computes as
+ *   attn_prefill does: P V from f16 softmax weights and f16 values, with the
+ *   same range rule for v (a magnitude of 2^16 or more is saturated and
+ *   reported as ATTN_ERR_UNSUPPORTED in *err_word).
  */
 int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_lens,
                 const int32_t *positions, int batch, int q_rows, int max_seq_len, int window,
@@ -288,11 +294,13 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *                  rotated keys.  q row (b, r) uses positions[b*q_rows + r],
  *                  new key row b*q_rows + r the position seq_lens[b] - q_rows + r.
  *   flags          0, or ATTN_DECODE_TABLES_EARLY: seq_lens, positions and the
- *                  block table were not written by the kernel issued just
- *                  before this call on the stream, so the launch may read
- *                  them (and plan its work) while that kernel finishes,
- *                  under programmatic dependent launch.  Everything else is
- *                  still read after it completes.
+ *                  block table are not written by any kernel that may still
+ *                  be running when this call is issued (normally: not by the
+ *                  kernel issued just before it), so the call may read them
+ *                  (and plan its work) while that kernel finishes, under
+ *                  programmatic dependent launch, and bring the first tiles
+ *                  of its cache reads into L2 meanwhile.  Everything else is
+ *                  still read after the previous kernel completes.
  *   Every other argument, the workspace and the statuses are attn_decode's.
  *   An FP8 cache receives the rows encoded exactly as attn_kv_append encodes
  *   them (K minus k_ref), and the decode reads those codes; rope_inv_freq must

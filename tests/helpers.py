@@ -11,9 +11,13 @@ REL_L2 = 2e-3    # ||out - ref|| / ||ref||
 # The output is rounded once to bf16.  Below |o| = 4 every real lies within
 # half a bf16 step (at most 1/128) of a bf16 value, so max-abs 1e-2 holds
 # literally; from 4 up half a step is 1/64 or more, and no bf16 result can be
-# within 1e-2 of every exact value.  There the element must be one of the two
-# bf16 values around the exact one (within one step of it).
+# within 1e-2 of every exact value.  There an element may differ from the
+# exact value by half a bf16 step (the final rounding) plus ACCUM_SLACK * |o|:
+# the kernels' own error before that rounding (P rounded once to f16, at most
+# 2^-11 of the largest value a row attends, which in the few-key rows where
+# |o| >= 4 occurs is about |o|; fp32 accumulation far less).
 FAITHFUL_FROM = 4.0
+ACCUM_SLACK = 2.0 ** -9
 
 
 def bf16_step(x):
@@ -23,7 +27,8 @@ def bf16_step(x):
 
 
 def element_bound(ref):
-    return np.where(np.abs(ref) >= FAITHFUL_FROM, bf16_step(ref), MAX_ABS)
+    big = 0.5 * bf16_step(ref) + ACCUM_SLACK * np.abs(ref)
+    return np.where(np.abs(ref) >= FAITHFUL_FROM, big, MAX_ABS)
 
 
 def bits(t):
@@ -83,6 +88,6 @@ def compare(out, ref, where=""):
         worst = ""
     ok = bool((over <= 1.0).all()) if diff.size else True
     assert ok and rel <= REL_L2, \
-        f"{where}: max-abs {max_abs:.3e} (<= {MAX_ABS} below |o| {FAITHFUL_FROM}, one bf16 " \
-        f"step above), rel-L2 {rel:.3e} (<= {REL_L2}); {worst}"
+        f"{where}: max-abs {max_abs:.3e} (<= {MAX_ABS} below |o| {FAITHFUL_FROM}, half a bf16 " \
+        f"step + {ACCUM_SLACK:.3g} |o| above), rel-L2 {rel:.3e} (<= {REL_L2}); {worst}"
     return max_abs, rel

@@ -123,29 +123,33 @@ def test_decode_kernel_launches(lib):
     f = lib.attn_decode_kernel_launches
     c = cache(slots=16384 * 40, sps=16384)
     cs = c.struct()
-    assert f(ctypes.byref(cs), 2, 1, 30, 8, 128, 4096, 0, 0, 0) == -1  # 30 q heads over 8
-    assert f(None, 2, 1, 32, 8, 128, 4096, 0, 0, 0) == -1
-    assert f(ctypes.byref(cs), 0, 1, 32, 8, 128, 4096, 0, 0, 0) == 0
+    assert f(ctypes.byref(cs), 2, 1, 30, 8, 128, 4096, 0, 0, 0, 0) == -1  # 30 q heads over 8
+    assert f(None, 2, 1, 32, 8, 128, 4096, 0, 0, 0, 0) == -1
+    assert f(ctypes.byref(cs), 0, 1, 32, 8, 128, 4096, 0, 0, 0, 0) == 0
     # short contexts: every unit spans at most 8 CTAs, merged in the split kernel
-    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 512, 0, 0, 0) == 1
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 512, 0, 0, 0, 0) == 1
     # 16 units at 8,192 keys: few units over many CTAs -> merge kernel
-    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0) == 2
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 0) == 2
     # 320 units at 8,192 keys: too many units for the merge kernel's rule
-    assert f(ctypes.byref(cs), 40, 1, 32, 8, 128, 8192, 0, 1, 0) == 1
+    assert f(ctypes.byref(cs), 40, 1, 32, 8, 128, 8192, 0, 1, 0, 0) == 1
     # one unit that may span more than 128 CTAs: merge kernel
-    assert f(ctypes.byref(cs), 40, 1, 8, 1, 128, 16384, 0, 0, 0) == 2
+    assert f(ctypes.byref(cs), 40, 1, 8, 1, 128, 16384, 0, 0, 0, 0) == 2
     # more (request, row block) pairs than one launch's tables hold: 2 launches
     big = cache(slots=64 * 300, sps=64)
     bs = big.struct()
-    assert f(ctypes.byref(bs), 300, 1, 8, 2, 128, 64, 0, 0, 0) == 2
+    assert f(ctypes.byref(bs), 300, 1, 8, 2, 128, 64, 0, 0, 0, 0) == 2
+    # ATTN_DECODE_TABLES_EARLY plans the same kernels
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 1) == 2
+    assert f(ctypes.byref(bs), 300, 1, 8, 2, 128, 64, 0, 1, 0, 1) == 2
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 2) == -1  # unknown flag
     # a 29-row chunk of a 28/4 group (203 rows) over a linear cache: the chunk
     # kernel (+ its merge: 2 x 4 groups split over the key range; + the
     # append for attn_decode_append); with a rotary embedding the split kernel
     ch = cache(slots=14464 * 2, sps=14464, Hkv=4)
     hs = ch.struct()
-    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 0, 0) == 2
-    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 0) == 3
-    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 1) == 1
+    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 0, 0, 0) == 2
+    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 0, 0) == 3
+    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 1, 0) == 1
 
 
 def test_prefill_validation(lib):

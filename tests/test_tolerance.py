@@ -1,6 +1,7 @@
 """The comparison rule the parity tests apply (no GPU): literal max-abs 1e-2
-where bf16 can meet it, one bf16 step where its spacing cannot, rel-L2 2e-3
-throughout."""
+where bf16 can meet it; where its spacing cannot (|o| >= 4), half a bf16
+step plus 2^-9 |o| of slack for the kernels' error before the final
+rounding; rel-L2 2e-3 throughout."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +24,18 @@ def test_correct_rounding_passes_where_one_e_minus_two_cannot():
     assert float(out[0]) == -4.0625
     compare(out, ref)
     out[0] = -4.09375  # two steps away is not a rounding of it
+    with pytest.raises(AssertionError):
+        compare(out, ref)
+
+
+def test_one_step_off_above_four_fails():
+    # exact 6.0001: correctly rounded 6.0; a result one step (1/32) away, 6.03125,
+    # exceeds half a step (1/64) plus 2^-9 x 6 of slack
+    ref = np.ones(2000)
+    ref[0] = 6.0001
+    out = torch.tensor(ref).to(torch.bfloat16)
+    compare(out, ref)
+    out[0] = 6.03125
     with pytest.raises(AssertionError):
         compare(out, ref)
 
