@@ -284,10 +284,13 @@ class QwenWorkload(Workload):
                     d[key].copy_(hd[key], non_blocking=True)
             c = self.caches[(s * 6 + 1 + i) % self.ncopy]
             # seq_lens / positions are written before the step, never by the
-            # kernel just before a decode: it may plan while that one finishes
+            # kernel just before a decode, and the caches rotate, so no kernel
+            # that may still run writes the cache a call reads: it may plan and
+            # start its first cache tiles while that one finishes
             gq.attn_decode_append(d["q"], d["k_new"], d["v_new"], d["slots"], c, d["seq"],
                                   d["pos"], self.max_seq, 0, self.scale, out=d["out"],
-                                  workspace=self.ws, err=self.err, tables_early=True)
+                                  workspace=self.ws, err=self.err, tables_early=True,
+                                  cache_early=True)
             if e2e:
                 self.h["dec"][i]["out"].copy_(d["out"], non_blocking=True)
 
@@ -484,7 +487,7 @@ class DecodeOnlyWorkload(Workload):
             self.gq.attn_decode_append(c.q, c.k_new, c.v_new, c.slot_mapping, cache,
                                        c.seq_lens, c.positions, self.max_seq, c.window,
                                        c.scale, out=self.out, workspace=self.ws,
-                                       err=self.err, tables_early=True)
+                                       err=self.err, tables_early=True, cache_early=True)
 
     def capture(self, stream, e2e=False):
         torch = self.torch

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_
                 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_ALIGN"}
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
-ATTN_DECODE_TABLES_EARLY = 1  # attn_decode_append flag (include/attn_kv.h)
+ATTN_DECODE_TABLES_EARLY = 1  # attn_decode_append flags (include/attn_kv.h)
+ATTN_DECODE_CACHE_EARLY = 2
 ATTN_KV_BF16, ATTN_KV_FP8_E4M3 = 0, 1  # cache element types (attn_kv_dtype)
 ATTN_LAYOUT_BSHD, ATTN_LAYOUT_BHSD = 0, 1  # cache layouts (attn_kv_layout)
 
@@ -236,7 +237,7 @@ def attn_decode(q, cache: KVCache, seq_lens, positions, max_seq_len, window, sca
 
 def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, positions,
                        max_seq_len, window, scale, out=None, workspace=None, err=None,
-                       stream=None, rope_inv_freq=None, tables_early=False):
+                       stream=None, rope_inv_freq=None, tables_early=False, cache_early=False):
     """The step's KV append and its decode in one launch: same result as
     attn_kv_append(k_new, v_new, slot_mapping, cache) then attn_decode(...)
     when new row b*R + r is the key at position seq_lens[b] - R + r.
@@ -244,7 +245,8 @@ def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, 
     rope_inv_freq (float32 [D/2] on the device), q and k_new are first rotated
     at their positions (interleaved pairs).  tables_early: seq_lens,
     positions and the block table were not written by the kernel launched
-    just before on this stream (ATTN_DECODE_TABLES_EARLY)."""
+    just before on this stream (ATTN_DECODE_TABLES_EARLY); cache_early: nor
+    are the cache's other rows (ATTN_DECODE_CACHE_EARLY, implies tables_early)."""
     import torch
 
     B, R, Hq, D = q.shape
@@ -260,7 +262,8 @@ def attn_decode_append(q, k_new, v_new, slot_mapping, cache: KVCache, seq_lens, 
         _ptr(positions), B, R, int(max_seq_len), int(window), Hq, cache.n_kv_heads, D,
         float(scale), _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(err),
-        ATTN_DECODE_TABLES_EARLY if tables_early else 0, _stream(stream))
+        (ATTN_DECODE_TABLES_EARLY if tables_early else 0) |
+        (ATTN_DECODE_CACHE_EARLY if cache_early else 0), _stream(stream))
     _check(rc, "attn_decode_append")
     return out
 

@@ -197,7 +197,7 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,
                                 int n_kv_heads, int head_dim, int max_seq_len, int window,
                                 int with_append, int with_rope, unsigned flags) {
-    if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return -1;
+    if ((flags & ~(ATTN_DECODE_TABLES_EARLY | ATTN_DECODE_CACHE_EARLY)) != 0) return -1;
     if (check_decode_shape(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len,
                            window) != ATTN_OK)
         return -1;
@@ -267,7 +267,8 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
                                 max_seq_len, window);
     if (rc != ATTN_OK) return rc;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
-    if ((flags & ~ATTN_DECODE_TABLES_EARLY) != 0) return ATTN_ERR_UNSUPPORTED;
+    if ((flags & ~(ATTN_DECODE_TABLES_EARLY | ATTN_DECODE_CACHE_EARLY)) != 0)
+        return ATTN_ERR_UNSUPPORTED;
     // FP8 caches: the rows are encoded as attn_kv_append encodes them; the
     // rotary embedding is not combined with them here
     if (cache->dtype == ATTN_KV_FP8_E4M3 && rope_inv_freq) return ATTN_ERR_UNSUPPORTED;
@@ -292,7 +293,8 @@ int attn_decode_append(const void *q, const void *k_new, const void *v_new,
     return gqa::launch_decode(plan, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
                               window, n_q_heads, n_kv_heads, scale, out, workspace, err_word,
                               reinterpret_cast<cudaStream_t>(stream), k_new, v_new, slot_mapping,
-                              rope_inv_freq, (flags & ATTN_DECODE_TABLES_EARLY) != 0);
+                              rope_inv_freq, (flags & ATTN_DECODE_TABLES_EARLY) != 0,
+                              (flags & ATTN_DECODE_CACHE_EARLY) != 0);
 }
 
 int attn_prefill(const void *q, const void *k, const void *v, int batch, int seq_len, int window,

@@ -119,6 +119,10 @@ struct Params {
     // seq_lens, positions and block_table may be read before the previous
     // kernel completes (ATTN_DECODE_TABLES_EARLY)
     bool tables_early;
+    // ... and the cache too (ATTN_DECODE_CACHE_EARLY): the producer issues the
+    // first tiles of its share that hold none of the step's new rows before
+    // it waits for the previous kernel
+    bool cache_early;
     int32_t *err;
 };
 
@@ -559,12 +563,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 }
             }
         }
-        pdl_wait();
+        // with the cache final too, the producer waits inside its loop, after
+        // issuing the first tiles that need nothing from the previous kernel
+        if (!(p.cache_early && warp == kProducerWarp)) pdl_wait();
     }
     pdl_launch_dependents();
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == 0 && warp != kProducerWarp) {
         // units with no valid key get zeros (no CTA visits them)
-        for (int i = threadIdx.x; i < B * RBc; i += kThreads) {
+        for (int i = threadIdx.x; i < B * RBc; i += kWarps * 32) {
             if (tb.cnt[i] != 0) continue;
             const int b = i / RBc, rb = i - (i / RBc) * RBc;
             for (int row = rb * RB; row < min(p.rows, (rb + 1) * RB); ++row) {
@@ -595,7 +601,65 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         int tile = 0;  // tiles issued by this CTA (stage / phase counter)
         int seg = 0;   // segments started (q staging buffer / phase counter)
         bool ok = true;
+        bool waited = !p.cache_early;  // passed pdl_wait (the consumers have)
         while (ok && walk.next(p, tb, sg)) {
+            const int bg = p.b_base + sg.b;  // request index in the whole cache
+            const int seq_len = tb.seqlen[sg.b];
+            const int new_lo = seq_len - p.q_rows;  // first of the step's new keys
+            const int n_tiles = (sg.c_end - sg.c_begin + kCPT - 1) / kCPT;
+            // Fast path: a linear or ring tile of four present chunks whose 64
+            // positions sit in 64 consecutive slots and hold none of the
+            // step's new rows is one box per tensor.  Every lane reaches the
+            // same decision with a few integer operations: no ballots, so
+            // the producer keeps ahead of the stream (its general path costs
+            // ~1,000 cycles a tile).  Returns false for a tile it cannot take.
+            auto whole_tile_fast = [&](int it, int st) -> bool {
+                const int chunk0 = sg.c_begin + it * kCPT;
+                if (paged || chunk0 + kCPT > sg.c_end) return false;
+                constexpr int kRows = G::kTileRows;
+                const int T0 = chunk0 * kChunk;
+                const bool no_new = !fused || T0 + kRows <= new_lo || T0 >= seq_len;
+                int j0 = T0;
+                bool fits = !bhsd || T0 + kRows <= p.slots_per_seq;
+                if (p.kind == ATTN_CACHE_RING) {
+                    j0 = T0 % p.slots_per_seq;
+                    fits = j0 + kRows <= p.slots_per_seq;
+                }
+                const int64_t s00 = (int64_t)bg * p.slots_per_seq + j0;
+                if (!(no_new && fits && s00 + kRows <= p.num_slots)) return false;
+                uint8_t *kst = stages + st * G::kStageBytes;
+                uint8_t *vst = kst + G::kTileBytes;
+                if (lane == 0) info_whole[st] = 1;
+                if (lane < kCPT) {
+                    info_t0[st * kCPT + lane] = T0 + lane * kChunk;
+                    info_mask[st * kCPT + lane] = 0xFFFFu;
+                }
+                if (lane == 0) mbar_expect_tx(&full[st], 2 * G::kTileBytes);
+                __syncwarp();
+                if (lane < 2) {
+                    if (bhsd)  // block = request, row = position in its window
+                        tma_load_4d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, j0, 0,
+                                         bg * p.n_kv_heads + sg.kvh, &full[st], kv_policy);
+                    else
+                        tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, (int)s00,
+                                         sg.kvh * G::kHalves, &full[st], kv_policy);
+                }
+                __syncwarp();
+                mbar_arrive(&full[st]);
+                return true;
+            };
+            int it0 = 0;
+            if (!waited) {
+                // the first tiles of the share, into fresh stages, before the
+                // previous kernel completes (the cache is final: the step's new
+                // rows, which it may still be writing, are never among them)
+                while (it0 < n_tiles && tile < kStages && whole_tile_fast(it0, tile)) {
+                    ++it0;
+                    ++tile;
+                }
+                pdl_wait();
+                waited = true;
+            }
             {
                 // stage the segment's q rows and row positions for the consumers
                 const int qi = seg & 1;
@@ -619,7 +683,6 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 cp_async_arrive_noinc(&q_full[qi]);
                 ++seg;
             }
-            const int bg = p.b_base + sg.b;  // request index in the whole cache
             const int32_t *bt = paged ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
             // raw table entry at page index pi (range-checked when used)
             auto table_at = [&](int pi) -> int { return pi < p.max_blocks ? bt[pi] : -1; };
@@ -636,59 +699,17 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 }
                 return (s >= 0 && s < p.num_slots) ? s : -1;
             };
-            const int seq_len = tb.seqlen[sg.b];
-            const int new_lo = seq_len - p.q_rows;  // first of the step's new keys
-            const int n_tiles = (sg.c_end - sg.c_begin + kCPT - 1) / kCPT;
             // page ids of two consecutive 32-page windows, one per lane; the
             // second is fetched a window ahead of its use
             int win = -1, pg_cur = -1, pg_next = -1;
-            for (int it = 0; it < n_tiles && ok; ++it, ++tile) {
+            for (int it = it0; it < n_tiles && ok; ++it, ++tile) {
                 const int st = tile % kStages;
                 if (tile >= kStages) ok = mbar_wait(&empty[st], ((tile / kStages) - 1) & 1, p.err);
                 if (!ok) break;
                 uint8_t *kst = stages + st * G::kStageBytes;
                 uint8_t *vst = kst + G::kTileBytes;
                 const int chunk0 = sg.c_begin + it * kCPT;
-                // Fast path: a linear or ring tile of four present chunks whose 64
-                // positions sit in 64 consecutive slots and hold none of the
-                // step's new rows is one box per tensor.  Every lane reaches the
-                // same decision with a few integer operations: no ballots, so
-                // the producer keeps ahead of the stream (its general path costs
-                // ~1,000 cycles a tile).
-                if (!paged && chunk0 + kCPT <= sg.c_end) {
-                    constexpr int kRows = G::kTileRows;
-                    const int T0 = chunk0 * kChunk;
-                    const bool no_new = !fused || T0 + kRows <= new_lo || T0 >= seq_len;
-                    int j0 = T0;
-                    bool fits = !bhsd || T0 + kRows <= p.slots_per_seq;
-                    if (p.kind == ATTN_CACHE_RING) {
-                        j0 = T0 % p.slots_per_seq;
-                        fits = j0 + kRows <= p.slots_per_seq;
-                    }
-                    const int64_t s00 = (int64_t)bg * p.slots_per_seq + j0;
-                    if (no_new && fits && s00 + kRows <= p.num_slots) {
-                        if (lane == 0) info_whole[st] = 1;
-                        if (lane < kCPT) {
-                            info_t0[st * kCPT + lane] = T0 + lane * kChunk;
-                            info_mask[st * kCPT + lane] = 0xFFFFu;
-                        }
-                        if (lane == 0) mbar_expect_tx(&full[st], 2 * G::kTileBytes);
-                        __syncwarp();
-                        if (lane < 2) {
-                            if (bhsd)  // block = request, row = position in its window
-                                tma_load_4d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0, j0,
-                                                 0, bg * p.n_kv_heads + sg.kvh, &full[st],
-                                                 kv_policy);
-                            else
-                                tma_load_3d_hint(lane ? vst : kst, lane ? &tm_v64 : &tm_k64, 0,
-                                                 (int)s00, sg.kvh * G::kHalves, &full[st],
-                                                 kv_policy);
-                        }
-                        __syncwarp();
-                        mbar_arrive(&full[st]);
-                        continue;
-                    }
-                }
+                if (whole_tile_fast(it, st)) continue;
                 const int chunk = chunk0 + c;
                 const int t0 = chunk * kChunk;
                 // slot0 >= 0: first of 16 consecutive slots (TMA box); -1: a
@@ -911,6 +932,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                 }
             }
         }
+        if (!waited) pdl_wait();
         // the gathered rows of this thread must land before it leaves
         asm volatile("cp.async.wait_all;" ::: "memory");
         // No box may still be landing when the CTA exits: the last tile of
@@ -1946,7 +1968,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   int max_seq_len, int window, int n_q_heads, int n_kv_heads, float scale,
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
-                  const float *rope_inv_freq, bool tables_early) {
+                  const float *rope_inv_freq, bool tables_early, bool cache_early) {
     if (plan.chunk && rope_inv_freq == nullptr) {
         // the step's rows first (every CTA of the chunk kernel may read them)
         if (k_new) {
@@ -2030,7 +2052,12 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
         p.slot_mapping = slot_mapping ? slot_mapping + (int64_t)b0 * q_rows : nullptr;
         p.rope_inv_freq = rope_inv_freq;
         p.k_ref = fp8 ? cache->k_ref : nullptr;
-        p.tables_early = tables_early;
+        p.tables_early = tables_early || cache_early;
+        // Early tile loads are left out when the merge kernel follows (few
+        // units over long contexts): measured, they slowed those calls by 5%
+        // (their DRAM traffic delays the previous call's merge, which gates
+        // this call's start), while calls without it gained 5-8%.
+        p.cache_early = cache_early && !plan.merge_kernel;
         p.batch = nb;
         p.b_base = b0;
         p.q_rows = q_rows;

@@ -137,7 +137,7 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   void *out, void *workspace, int32_t *err, cudaStream_t stream,
                   const void *k_new = nullptr, const void *v_new = nullptr,
                   const int64_t *slot_mapping = nullptr, const float *rope_inv_freq = nullptr,
-                  bool tables_early = false);
+                  bool tables_early = false, bool cache_early = false);
 
 int launch_prefill(const void *q, const void *k, const void *v, int batch, int seq_len,
                    int window, int n_q_heads, int n_kv_heads, int head_dim, float scale,

@@ -301,12 +301,22 @@ int attn_decode(const void *q, const attn_kv_cache *cache, const int32_t *seq_le
  *                  programmatic dependent launch, and bring the first tiles
  *                  of its cache reads into L2 meanwhile.  Everything else is
  *                  still read after the previous kernel completes.
+ *                  ATTN_DECODE_CACHE_EARLY (implies TABLES_EARLY): in
+ *                  addition, no cache slot other than the ones this call
+ *                  appends is written by a kernel that may still be running,
+ *                  so the call may also start loading the first cache tiles
+ *                  of its work into shared memory before the previous kernel
+ *                  completes (the step's own rows are taken from k_new /
+ *                  v_new after it).  Normal in a decode loop whose previous
+ *                  kernel produces q, k_new and v_new; wrong if that kernel
+ *                  wrote other rows of this cache.
  *   Every other argument, the workspace and the statuses are attn_decode's.
  *   An FP8 cache receives the rows encoded exactly as attn_kv_append encodes
  *   them (K minus k_ref), and the decode reads those codes; rope_inv_freq must
  *   then be NULL (ATTN_ERR_UNSUPPORTED otherwise).
  */
 #define ATTN_DECODE_TABLES_EARLY 1u
+#define ATTN_DECODE_CACHE_EARLY 2u
 int attn_decode_append(const void *q, const void *k_new, const void *v_new,
                        const int64_t *slot_mapping, const float *rope_inv_freq,
                        const attn_kv_cache *cache,

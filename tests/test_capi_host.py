@@ -141,7 +141,8 @@ def test_decode_kernel_launches(lib):
     # ATTN_DECODE_TABLES_EARLY plans the same kernels
     assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 1) == 2
     assert f(ctypes.byref(bs), 300, 1, 8, 2, 128, 64, 0, 1, 0, 1) == 2
-    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 2) == -1  # unknown flag
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 3) == 2  # both early flags
+    assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 4) == -1  # unknown flag
     # a 29-row chunk of a 28/4 group (203 rows) over a linear cache: the chunk
     # kernel (+ its merge: 2 x 4 groups split over the key range; + the
     # append for attn_decode_append); with a rotary embedding the split kernel
@@ -202,7 +203,7 @@ def test_decode_append_validation(lib):
     assert f(*args(ws_bytes=need - 1)) == gq.ATTN_ERR_WORKSPACE
     assert f(*args(hq=30)) == gq.ATTN_ERR_SHAPE
     assert f(*args(scale=0.0)) == gq.ATTN_ERR_SHAPE
-    assert f(*args(flags=2)) == gq.ATTN_ERR_UNSUPPORTED
+    assert f(*args(flags=4)) == gq.ATTN_ERR_UNSUPPORTED
 
 
 def test_fp8_cache_validation(lib):

@@ -150,3 +150,33 @@ def test_tables_early_same_result():
         outs[early] = res
     for a, b in zip(outs[False], outs[True]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kind,B,seq,window", [(LINEAR, 2, [8192, 5000], 0),
+                                               (LINEAR, 1, [512], 0),
+                                               (RING, 4, [9000, 20000, 4100, 16400], 4096),
+                                               (PAGED, 4, [3000, 64, 1029, 2048], 0)])
+def test_cache_early_same_result(kind, B, seq, window):
+    """ATTN_DECODE_CACHE_EARLY lets the first cache tiles be loaded before the
+    previous kernel completes; it changes when they are read, not what is
+    computed: back-to-back calls give the bits of calls without it, and match
+    the oracle."""
+    dev = "cuda"
+    case = synth.decode_case(9510 + B, kind, B, 1, 28 if kind == LINEAR else 32,
+                             4 if kind == LINEAR else 8, 128, seq, window=window, block_size=16)
+    outs = {}
+    for early in (False, True):
+        cache = to_device(case, dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = (case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev),
+                case.slot_mapping.to(dev), cache, case.seq_lens.to(dev), case.positions.to(dev),
+                case.max_seq_len(), window, case.scale)
+        res = [gq.attn_decode_append(*args, err=err, tables_early=True, cache_early=early)
+               for _ in range(4)]
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs[early] = res
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
+    ref, _, _ = oracle_decode(case)
+    compare(outs[True][-1], ref, f"cache early {kind}")
