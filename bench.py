@@ -59,13 +59,13 @@ def load_peaks():
 # --------------------------------------------------------------------------
 
 # DRAM bytes (read + write) of one full-size Qwen2-7B prompt prefill launch,
-# T = 14,449, from ncu (profiles/prefill_kernel_qwen14449_dram.md).  They
+# T = 14,449, from ncu (profiles/prefill_kernel_qwen14449.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 199703040,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 200430080,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "a0030926e3b8099c1e3768bc9c16390a7c1ef3e1dd6c4b14721784449382ce50"}
+                   "sha256": "de67403b3be0c0e68c568807fc946e4bc3688d9b435e73b99e66be2ab52c7800"}
 
 
 def prefill_traffic(T):
