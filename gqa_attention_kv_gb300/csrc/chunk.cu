@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(s_tmem + 64, *reinterpret_cast<uint32_t(*)[32]>(u + 64));
                 tmem_ld_32x32b_x32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 96));
                 tmem_wait_ld();
+                tmem_regs_after_wait(u);
             }
             const int key0 = (kt0 + j) * kBN;
             const bool needs_mask =
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t orow[32];
                     tmem_ld_32x32b_x32(o_tmem + c0, orow);
                     tmem_wait_ld();
+                    tmem_regs_after_wait(orow);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
@@ -474,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n_kt > 0) {  // CTA-uniform: the TMEM rows were accumulated into
                 tmem_ld_32x32b_x32(o_tmem + c0, orow);
                 tmem_wait_ld();
+                tmem_regs_after_wait(orow);
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) orow[e] = 0u;

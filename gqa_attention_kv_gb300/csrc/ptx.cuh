@@ -490,6 +490,17 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Registers a tcgen05.ld writes are valid only after tcgen05.wait::ld, and
+// nothing ties their later uses to that wait: the compiler may schedule an
+// arithmetic use of them above it.  An empty asm that "modifies" each of them,
+// issued after the wait (volatile asms keep their order), makes every later
+// use depend on it.
+template <int N>
+__device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
