@@ -24,7 +24,9 @@
 //               positions, so the swizzle is unchanged) before P V reads it.
 //   warps 4..7  softmax for Q0, warps 8..11 for Q1.  Thread = query row = TMEM
 //               lane.  tcgen05.ld of its S row, mask (only on tiles that
-//               cross the diagonal or the window edge), running max / sum in
+//               cross the diagonal or the window edge; a tile none of the
+//               query tile's rows sees is skipped by the MMA issuer and the
+//               softmax alike), running max / sum in
 //               fp32, P written back over its S columns rounded once to f16
 //               (vibevoice.c, "Attention backends": P V takes its operands in
 //               FP16, because one bf16 rounding of P is too coarse; f16 keeps
@@ -131,8 +133,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not all ask L2 for the same lines at once.
     const int rot = n_kt > 0 ? (int)(((int64_t)(h % p.group) * n_kt) / p.group) : 0;
     auto tile_of = [&](int j) { const int t = j + rot; return kt0 + (t >= n_kt ? t - n_kt : t); };
+    // Tile j is dead for query tile a when no row of a may see any of its
+    // keys: all keys after a's last row, all before the window of a's first
+    // row, or a's rows all past the sequence.  Its S and P V are never
+    // computed: the MMA issuer and the softmax warps both skip it.
+    auto live = [&](int a, int j) -> bool {
+        const int qa = q0 + a * kBM, key0 = tile_of(j) * kBN;
+        return qa < p.seq_len && key0 <= qa + kBM - 1 &&
+               (p.window <= 0 || qa - (key0 + kBN - 1) < p.window);
+    };
 
+    // The next kernel may start its own prologue on SMs this grid leaves
+    // free; it reads nothing of ours before its programmatic-launch wait.
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
+        // kernel parameters, not written by the previous kernel
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_o);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -167,9 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
             mbar_arrive_expect_tx(q_full, 2 * C::kQBytes);
             for (int a = 0; a < 2; ++a)
                 for (int hf = 0; hf < C::kHalves; ++hf)
@@ -248,12 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
             if (ok && n_kt > 0) {
                 tc_fence_after();
-                issue_qk(0, 0);
-                issue_qk(1, 0);
+                if (live(0, 0)) issue_qk(0, 0);
+                if (live(1, 0)) issue_qk(1, 0);
                 tc_commit(&k_empty[0]);
             }
             // stage indices and phases of the K and V rings, stepped without division
             int vst = 0, vph = 0, kst = 0, kph = 0;
+            // live tiles of query tile 0 / 1 whose P V is issued (two scalars:
+            // an array indexed by a would live in local memory)
+            int n_pv0 = 0, n_pv1 = 0;
             for (int j = 0; j < n_kt && ok; ++j) {
                 ok = mbar_wait(&v_conv[vst], vph, p.err);  // V(j) landed and is f16
                 const bool more = j + 1 < n_kt;
@@ -262,14 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kph ^= 1;
                 }
                 for (int a = 0; a < 2 && ok; ++a) {
-                    // each half of P as soon as the softmax has written it
-                    for (int hh = 0; hh < 2 && ok; ++hh) {
-                        ok = mbar_wait(&p_full[a * 2 + hh], j & 1, p.err);
+                    if (live(a, j)) {
+                        const int n_pv = a ? n_pv1 : n_pv0;
+                        // each half of P as soon as the softmax has written it
+                        for (int hh = 0; hh < 2 && ok; ++hh) {
+                            ok = mbar_wait(&p_full[a * 2 + hh], n_pv & 1, p.err);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv_half(a, vst, hh, n_pv == 0 && hh == 0);
+                        }
+                        if (a) ++n_pv1; else ++n_pv0;
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_pv_half(a, vst, hh, j == 0 && hh == 0);
                     }
-                    if (!ok) break;
                     if (a == 1) tc_commit(&v_empty[vst]);
                     if (more) {
                         if (a == 0) {
@@ -277,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        issue_qk(a, kst);
+                        if (live(a, j + 1)) issue_qk(a, kst);
                         if (a == 1) tc_commit(&k_empty[kst]);
                     }
                 }
@@ -336,15 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;            // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;     // row inside the tile
         const int qa0 = q0 + a * kBM;
-        const int qi = qa0 + row;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const uint32_t s_tmem = tmem + a * 128 + lane_base;
         const uint32_t o_tmem = tmem + 256 + a * HD + lane_base;
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        int n_s = 0;  // live tiles whose S this warp has read
         for (int j = 0; j < n_kt; ++j) {
-            ok = mbar_wait(&s_full[a], j & 1, p.err);
+            if (!live(a, j)) continue;
+            ok = mbar_wait(&s_full[a], n_s & 1, p.err);
             __syncwarp();  // reconverge before the warp-collective tcgen05.ld
             if (!ok) break;
             tc_fence_after();
@@ -362,11 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool needs_mask =
                 key0 + kBN - 1 > qa0 || (p.window > 0 && qa0 + kBM - 1 - key0 >= p.window);
             if (needs_mask) {
+                // row sees columns lo <= c <= hi (c = key - key0): per element
+                // one compare with an immediate (two with a window) and a select
+                const int hi = qa0 + row - key0;
+                if (p.window > 0) {
+                    const int lo = hi - p.window + 1;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int t = key0 + c;
-                    const bool valid = t <= qi && (p.window <= 0 || qi - t < p.window);
-                    s[c] = valid ? s[c] : -INFINITY;
+                    for (int c = 0; c < kBN; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
                 }
             }
             // row max of the raw scores: three-input max, four independent chains
@@ -387,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = m_new;
             }
             // O_a += P V of the previous tile is complete (covered by s_full)
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (n_s > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t orow[32];
@@ -424,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             l_run = l_run * alpha + (sum0 + sum1);
+            ++n_s;
         }
         // epilogue: wait for the last PV, normalise, store through shared memory
         if (ok) ok = mbar_wait(o_done, 0, p.err);

@@ -53,6 +53,18 @@ def test_window(T, W):
     compare(out, ref, f"T={T} W={W}")
 
 
+@pytest.mark.parametrize("T,W,Hq,Hkv,D", [(1100, 130, 28, 4, 128), (900, 64, 12, 2, 128),
+                                          (1300, 257, 7, 1, 64), (520, 255, 4, 2, 64)])
+def test_window_gqa(T, W, Hq, Hkv, D):
+    """Windows with grouped heads, whose CTAs walk their key tiles from
+    different starting tiles: key tiles that one query tile of a CTA sees and
+    the other does not (before the window or after the diagonal), at any
+    position of the walk."""
+    p = synth.prefill_case(350 + W + Hq, 1, T, Hq, Hkv, D, window=W)
+    out, ref = run(p)
+    compare(out, ref, f"T={T} W={W} {Hq}/{Hkv} D={D}")
+
+
 def test_encoder_prefill_full():
     """The speech-encoder shape at full size: T=750, 32 heads, D=64."""
     p = synth.encoder_prefill()
@@ -124,3 +136,13 @@ def test_v_beyond_f16_is_reported():
     rc, ref = oracle.prefill(bits(p.q), bits(p.k), bits(p.v), 0, p.scale, rows=list(range(150)))
     assert rc == 0
     compare(out[:, :150], ref, "rows before the large value")
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [(2, 513, 8, 2, 128, 0), (1, 1100, 4, 4, 64, 300),
+                                            (3, 900, 6, 3, 128, 0), (1, 640, 2, 1, 64, 129)])
+def test_small_launches(B, T, Hq, Hkv, D, W):
+    """Launches that leave SMs idle (fewer CTAs than SMs, long last pairs):
+    batches, GQA, both head dims and windows."""
+    p = synth.prefill_case(500 + T + D + W, B, T, Hq, Hkv, D, window=W)
+    out, ref = run(p)
+    compare(out, ref, f"B={B} T={T} {Hq}/{Hkv} D={D} W={W}")
