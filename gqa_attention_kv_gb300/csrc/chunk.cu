@@ -41,11 +41,12 @@ namespace chk {
 constexpr int kBM = 128;       // rows per tile (two tiles per CTA)
 constexpr int kBN = 128;       // keys per tile
 constexpr int kThreads = 384;  // 3 warpgroups
-// Registers as in the prefill kernel: launched at 168 a thread, the TMA / MMA
-// / V-conversion warpgroup drops to 88 and the two softmax warpgroups rise to
-// 208 (4x32x88 + 8x32x208 = 384x168).
-constexpr uint32_t kRegsControl = 88;
-constexpr uint32_t kRegsSoftmax = 208;
+// Registers: launched at 168 a thread, the TMA / MMA / V-conversion warpgroup
+// drops to 96 and the two softmax warpgroups rise to 200 (4x32x96 + 8x32x200 =
+// 63,488 <= 384x168; 96 + 200 + 200 <= 512 per sub-partition lane slot).  This
+// split spills the least of those measured (88 / 208 reloaded 224 bytes).
+constexpr uint32_t kRegsControl = 96;
+constexpr uint32_t kRegsSoftmax = 200;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMergeWarps = 8;
@@ -397,11 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool needs_mask =
                 key0 + kBN - 1 > key_cap || (p.window > 0 && qi - key0 >= p.window);
             if (needs_mask) {
+                // the row sees columns lo <= c <= hi (c = key - key0): one
+                // compare with an immediate (two with a window) and a select
+                const int hi = key_cap - key0;
+                if (p.window > 0) {
+                    const int lo = qi - p.window + 1 - key0;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int t = key0 + c;
-                    const bool valid = t <= key_cap && (p.window <= 0 || qi - t < p.window);
-                    s[c] = valid ? s[c] : -INFINITY;
+                    for (int c = 0; c < kBN; ++c) s[c] = (c <= hi && c >= lo) ? s[c] : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) s[c] = c <= hi ? s[c] : -INFINITY;
                 }
             }
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
