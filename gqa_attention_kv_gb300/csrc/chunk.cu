@@ -117,7 +117,8 @@ __device__ __forceinline__ void split_range(const Params &p, int p_lo, int p_hi,
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
+                 const Params p) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -476,6 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = row < used && r < r_end;
         __nv_bfloat16 *dst =
             p.out + (((int64_t)b * R + r) * (p.n_kv_heads * G) + kvh * G + gh) * HD;
+        // A split's partial O goes through shared memory (the K ring for tile
+        // 0, the V ring for tile 1: the last MMA has read them) as 128-byte
+        // swizzled rows of 32 columns, and TMA writes whole lines of it; a
+        // row per thread stored straight to global memory would write 16
+        // bytes into each of 32 lines per instruction.
+        uint8_t *stage = a == 0 ? sK : sV;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
             uint32_t orow[32];
@@ -500,14 +507,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        pack_bf16x2(v(8 * q4 + 6), v(8 * q4 + 7)));
                 }
             } else {
-                float *o = p.ws_o + (slot * 2 * kBM + m) * HD + c0;
+                const uint32_t base = smem_u32(stage + (c0 / 32) * (kBM * 128) + row * 128);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)
-                    *reinterpret_cast<float4 *>(o + 4 * q4) =
-                        make_float4(v(4 * q4), v(4 * q4 + 1), v(4 * q4 + 2), v(4 * q4 + 3));
+                    st_shared_v4(base + ((q4 ^ (row & 7)) << 4),
+                                 make_uint4(__float_as_uint(v(4 * q4)), __float_as_uint(v(4 * q4 + 1)),
+                                            __float_as_uint(v(4 * q4 + 2)),
+                                            __float_as_uint(v(4 * q4 + 3))));
             }
         }
-        if (p.n_split > 1) p.ws_lse[slot * 2 * kBM + m] = any ? m_run + __log2f(l_run) : -INFINITY;
+        if (p.n_split > 1) {
+            p.ws_lse[slot * 2 * kBM + m] = any ? m_run + __log2f(l_run) : -INFINITY;
+            fence_proxy_async_smem();
+            if (a == 0)
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            else
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (quad == 0 && lane == 0) {
+                for (int t = 0; t < HD / 32; ++t)
+                    tma_store_2d(&tm_ws, stage + t * (kBM * 128), t * 32,
+                                 (int)(slot * 2 * kBM + a * kBM));
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        }
     }
     __syncwarp();  // lanes 1..31 of the TMA and MMA warps wait here for lane 0
     tc_fence_before();
@@ -601,7 +624,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
 
 template <int HD>
 int launch(const Params &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-           cudaStream_t stream) {
+           const CUtensorMap &tw, cudaStream_t stream) {
     auto kern = chunk_kernel<HD>;
     static int configured_device = -1;
     int dev = 0;
@@ -617,7 +640,7 @@ int launch(const Params &p, const CUtensorMap &tq, const CUtensorMap &tk, const 
     }
     const int64_t groups = (int64_t)p.batch * p.n_kv_heads * p.n_pairs;
     const unsigned grid = (unsigned)(groups * p.n_split);
-    if (launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg<HD>::kSmem, stream, tq, tk, tv, p) !=
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg<HD>::kSmem, stream, tq, tk, tv, tw, p) !=
         cudaSuccess)
         return ATTN_ERR_CUDA;
     if (p.n_split > 1) {
@@ -696,8 +719,21 @@ int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cach
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
-    return head_dim == 128 ? chk::launch<128>(p, tq, tk, tv, stream)
-                           : chk::launch<64>(p, tq, tk, tv, stream);
+    // the splits' partial O viewed as {head_dim, slot * 256 + row} fp32: a
+    // box of {32, 128} is one staged 128-row tile of 32 columns (unused, and
+    // the K map passed in its place, when the key range is not split)
+    CUtensorMap tw = tk;
+    if (plan.n_split > 1) {
+        const uint64_t dw[2] = {(uint64_t)head_dim, groups * plan.n_split * 2 * chk::kBM};
+        const uint64_t sw[1] = {(uint64_t)head_dim * 4};
+        const uint32_t bw[2] = {32, (uint32_t)chk::kBM};
+        if (!encode_tensor_map_f32(&tw, p.ws_o, 2, dw, sw, bw)) {
+            note_cuda_error(cudaErrorInvalidValue);
+            return ATTN_ERR_CUDA;
+        }
+    }
+    return head_dim == 128 ? chk::launch<128>(p, tq, tk, tv, tw, stream)
+                           : chk::launch<64>(p, tq, tk, tv, tw, stream);
 }
 
 }  // namespace gqa
