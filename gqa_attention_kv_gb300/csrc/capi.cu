@@ -74,7 +74,7 @@ bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint6
     return r == CUDA_SUCCESS;
 }
 
-bool encode_tensor_map_f32(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+bool encode_tensor_map_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                            const uint64_t *strides_bytes, const uint32_t *box) {
     auto fn = get_encode_fn();
     if (!fn) return false;
@@ -87,7 +87,7 @@ bool encode_tensor_map_f32(CUtensorMap *map, const void *base, int rank, const u
         es[i] = 1;
         if (i + 1 < rank) gs[i] = strides_bytes[i];
     }
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void *>(base), gd,
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd,
               gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -27,6 +27,7 @@
 // the softmax of one tile row per thread.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -76,8 +77,8 @@ struct Params {
     const int32_t *seq_lens;   // [batch]
     const int32_t *positions;  // [batch * q_rows]
     float scale_log2;
-    float *ws_o;    // n_split > 1: [slot][256][HD] fp32, slot = ((b*Hkv + kvh)*pairs + pair)*splits + s
-    float *ws_lse;  // [slot][256]
+    uint16_t *ws_o;  // n_split > 1: [slot][256][HD] f16, slot = ((b*Hkv + kvh)*pairs + pair)*splits + s
+    float *ws_lse;   // [slot][256]
     __nv_bfloat16 *out;  // [batch, q_rows, n_q_heads, HD]
     int32_t *err;
 };
@@ -477,11 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = row < used && r < r_end;
         __nv_bfloat16 *dst =
             p.out + (((int64_t)b * R + r) * (p.n_kv_heads * G) + kvh * G + gh) * HD;
-        // A split's partial O goes through shared memory (the K ring for tile
-        // 0, the V ring for tile 1: the last MMA has read them) as 128-byte
-        // swizzled rows of 32 columns, and TMA writes whole lines of it; a
-        // row per thread stored straight to global memory would write 16
-        // bytes into each of 32 lines per instruction.
+        // A split's partial O (normalised by its own sum, so |O| <= max |v|,
+        // inside f16's range as the V conversion requires) is kept in f16:
+        // 2^-11 relative, a quarter of the output's bf16 step, for half the
+        // bytes written here and read by the merge.  It goes through shared
+        // memory (the K ring for tile 0, the V ring for tile 1: the last MMA
+        // has read them) as 128-byte swizzled rows of 64 columns, and TMA
+        // writes whole lines of it; a row per thread stored straight to
+        // global memory would write into 32 lines per instruction.
         uint8_t *stage = a == 0 ? sK : sV;
 #pragma unroll
         for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -507,13 +511,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        pack_bf16x2(v(8 * q4 + 6), v(8 * q4 + 7)));
                 }
             } else {
-                const uint32_t base = smem_u32(stage + (c0 / 32) * (kBM * 128) + row * 128);
+                // columns c0 .. c0 + 31: four 16-byte pieces of box c0 / 64
+                const uint32_t base = smem_u32(stage + (c0 / 64) * (kBM * 128) + row * 128);
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    st_shared_v4(base + ((q4 ^ (row & 7)) << 4),
-                                 make_uint4(__float_as_uint(v(4 * q4)), __float_as_uint(v(4 * q4 + 1)),
-                                            __float_as_uint(v(4 * q4 + 2)),
-                                            __float_as_uint(v(4 * q4 + 3))));
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int piece = ((c0 & 63) >> 3) + q4;
+                    st_shared_v4(base + ((piece ^ (row & 7)) << 4),
+                                 make_uint4(pack_f16x2(v(8 * q4), v(8 * q4 + 1)),
+                                            pack_f16x2(v(8 * q4 + 2), v(8 * q4 + 3)),
+                                            pack_f16x2(v(8 * q4 + 4), v(8 * q4 + 5)),
+                                            pack_f16x2(v(8 * q4 + 6), v(8 * q4 + 7))));
+                }
             }
         }
         if (p.n_split > 1) {
@@ -524,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 asm volatile("bar.sync 2, 128;" ::: "memory");
             if (quad == 0 && lane == 0) {
-                for (int t = 0; t < HD / 32; ++t)
-                    tma_store_2d(&tm_ws, stage + t * (kBM * 128), t * 32,
+                for (int t = 0; t < HD / 64; ++t)
+                    tma_store_2d(&tm_ws, stage + t * (kBM * 128), t * 64,
                                  (int)(slot * 2 * kBM + a * kBM));
                 tma_store_commit();
                 tma_store_wait_all();
@@ -562,7 +570,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
     const int r = pair * 2 * p.rt + a * p.rt + row / G, gh = row % G;
     if (row >= p.rt * G || r >= p.q_rows) return;
     const float *lse = p.ws_lse + grp * p.n_split * 2 * kBM + m;  // split s at s * 2 kBM
-    const float *o = p.ws_o + (grp * p.n_split * 2 * kBM + m) * HD + lane * PER;
+    const uint16_t *o = p.ws_o + (grp * p.n_split * 2 * kBM + m) * HD + lane * PER;
     float M = -INFINITY;
     for (int s0 = 0; s0 < p.n_split; s0 += 32)
         if (s0 + lane < p.n_split) M = fmaxf(M, __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM));
@@ -587,13 +595,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
 #pragma unroll
                     for (int e = 0; e < PER; ++e) v[k][e] = 0.f;
                     if (k0 + k < n) {
-                        const float *src = o + (int64_t)(s0 + k0 + k) * 2 * kBM * HD;
+                        const uint16_t *src = o + (int64_t)(s0 + k0 + k) * 2 * kBM * HD;
                         if constexpr (PER == 4) {
-                            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-                            v[k][0] = t.x, v[k][1] = t.y, v[k][2] = t.z, v[k][3] = t.w;
+                            const uint2 t = __ldcg(reinterpret_cast<const uint2 *>(src));
+                            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
+                            const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
+                            v[k][0] = lo.x, v[k][1] = lo.y, v[k][2] = hi.x, v[k][3] = hi.y;
                         } else {
-                            const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-                            v[k][0] = t.x, v[k][1] = t.y;
+                            const uint32_t t = __ldcg(reinterpret_cast<const unsigned int *>(src));
+                            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&t));
+                            v[k][0] = lo.x, v[k][1] = lo.y;
                         }
                     }
                 }
@@ -670,8 +681,9 @@ void plan_chunk(int batch, int q_rows, int n_q_heads, int n_kv_heads, int head_d
     int64_t split = std::max<int64_t>(1, device_sm_count() / std::max<int64_t>(groups, 1));
     split = std::min<int64_t>(split, std::max<int64_t>(1, tiles / 2));
     plan->n_split = (int)split;
+    // per split and packed row: head_dim f16 of O, one fp32 log-sum-exp
     plan->workspace = plan->n_split > 1 ? (size_t)groups * plan->n_split * 2 * chk::kBM *
-                                              ((size_t)head_dim + 1) * sizeof(float)
+                                              ((size_t)head_dim * 2 + sizeof(float))
                                         : 0;
 }
 
@@ -695,8 +707,10 @@ int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cach
     p.positions = positions;
     p.scale_log2 = scale * 1.4426950408889634f;
     const size_t groups = (size_t)batch * n_kv_heads * plan.n_pairs;
-    p.ws_o = static_cast<float *>(workspace);
-    p.ws_lse = p.ws_o ? p.ws_o + groups * plan.n_split * 2 * chk::kBM * head_dim : nullptr;
+    p.ws_o = static_cast<uint16_t *>(workspace);
+    p.ws_lse = p.ws_o ? reinterpret_cast<float *>(p.ws_o + groups * plan.n_split * 2 * chk::kBM *
+                                                               head_dim)
+                      : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.err = err;
     // q viewed as {head_dim, n_q_heads, q_rows, batch}: a box of {64, G, rt, 1}
@@ -719,15 +733,15 @@ int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cach
         note_cuda_error(cudaErrorInvalidValue);
         return ATTN_ERR_CUDA;
     }
-    // the splits' partial O viewed as {head_dim, slot * 256 + row} fp32: a
-    // box of {32, 128} is one staged 128-row tile of 32 columns (unused, and
+    // the splits' partial O viewed as {head_dim, slot * 256 + row} f16: a
+    // box of {64, 128} is one staged 128-row tile of 64 columns (unused, and
     // the K map passed in its place, when the key range is not split)
     CUtensorMap tw = tk;
     if (plan.n_split > 1) {
         const uint64_t dw[2] = {(uint64_t)head_dim, groups * plan.n_split * 2 * chk::kBM};
-        const uint64_t sw[1] = {(uint64_t)head_dim * 4};
-        const uint32_t bw[2] = {32, (uint32_t)chk::kBM};
-        if (!encode_tensor_map_f32(&tw, p.ws_o, 2, dw, sw, bw)) {
+        const uint64_t sw[1] = {(uint64_t)head_dim * 2};
+        const uint32_t bw[2] = {64, (uint32_t)chk::kBM};
+        if (!encode_tensor_map_f16(&tw, p.ws_o, 2, dw, sw, bw)) {
             note_cuda_error(cudaErrorInvalidValue);
             return ATTN_ERR_CUDA;
         }

@@ -41,8 +41,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 bool encode_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                        const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128,
                        bool bytes = false);
-// The same over fp32 elements, 128-byte swizzled (boxes of 32 columns).
-bool encode_tensor_map_f32(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+// The same over f16 elements, 128-byte swizzled (boxes of 64 columns).
+bool encode_tensor_map_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                            const uint64_t *strides_bytes, const uint32_t *box);
 
 // Where head h's row of cache slot s starts, in bytes (attn_kv_cache's layouts):
