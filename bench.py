@@ -62,10 +62,10 @@ def load_peaks():
 # T = 14,449, from ncu (profiles/prefill_kernel_qwen14449.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 200430080,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 198478080,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "de67403b3be0c0e68c568807fc946e4bc3688d9b435e73b99e66be2ab52c7800"}
+                   "sha256": "64deabd02f1b96d26995ade49049e8b175b525c83d5e97cb1183314abe0fcd13"}
 
 
 def prefill_traffic(T):
