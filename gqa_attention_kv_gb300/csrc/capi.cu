@@ -223,8 +223,7 @@ int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_row
     gqa::DecodePlan plan;
     gqa::plan_decode(cache, batch, q_rows, n_q_heads, n_kv_heads, head_dim, max_seq_len, window,
                      &plan);
-    if (plan.chunk && !with_rope)
-        return (with_append ? 1 : 0) + 1 + (plan.cp.n_split > 1 ? 1 : 0);
+    if (plan.chunk && !with_rope) return 1 + (plan.cp.n_split > 1 ? 1 : 0);
     const int splits = (batch + plan.batch_per_launch - 1) / plan.batch_per_launch;
     return splits * (plan.merge_kernel ? 2 : 1);
 }

@@ -80,6 +80,12 @@ struct Params {
     uint16_t *ws_o;  // n_split > 1: [slot][256][HD] f16, slot = ((b*Hkv + kvh)*pairs + pair)*splits + s
     float *ws_lse;   // [slot][256]
     __nv_bfloat16 *out;  // [batch, q_rows, n_q_heads, HD]
+    // The step's own rows (fused append), or null: row b * q_rows + r is the
+    // key at position seq_lens[b] - q_rows + r; its slot is slot_mapping[row].
+    const __nv_bfloat16 *k_new, *v_new;  // [batch * q_rows, Hkv, HD]
+    const int64_t *slot_mapping;
+    int64_t num_slots;
+    __nv_bfloat16 *k_cache, *v_cache;  // linear slot-major: slot s, head h at (s * Hkv + h) * HD
     int32_t *err;
 };
 
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_done = p_full + 4;
     uint64_t *mma_done = o_done + 1;
     uint64_t *v_conv = mma_done + 1;  // [kVStages]: V tile now f16
+    uint64_t *k_patch = v_conv + C::kVStages;  // a K tile holding the step's rows is patched
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
     __shared__ int s_pos[2];  // min and max position of the CTA's rows
 
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 128);
         mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
+        mbar_init(k_patch, 64);  // every thread of warps 2 and 3
         fence_barrier_init();
         s_pos[0] = INT32_MAX;
         s_pos[1] = -1;
@@ -205,6 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kt0, n_kt;
     split_range(p, s_pos[0], s_pos[1], n_keys, split, kt0, n_kt);
     const uint32_t tmem = *tmem_slot;
+    // With the step's rows fused in, the keys at positions new_lo .. n_keys - 1
+    // come from k_new / v_new: a K or V tile holding any of them is patched in
+    // shared memory after its copy lands (the cache may still hold older rows
+    // there: this launch writes them for later steps).
+    const bool fused = p.k_new != nullptr;
+    const int new_lo = n_keys - R;
+    auto tile_new = [&](int j) {
+        const int key0 = (kt0 + j) * kBN;
+        return fused && key0 < n_keys && key0 + kBN > new_lo;
+    };
 
     if (warp < 4) {
     setmaxnreg_dec<kRegsControl>();
@@ -285,7 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                               idesc_pv, (!first || k4 > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || mbar_wait(&k_full[0], 0, p.err));
+            // K tile j is ready when its copy lands or, holding the step's
+            // rows, when warps 2 and 3 have patched them in (k_patch completes
+            // once per such tile, in tile order)
+            int n_patched = 0;
+            auto k_ready = [&](int j, int st, int ph) -> bool {
+                if (!tile_new(j)) return mbar_wait(&k_full[st], ph, p.err);
+                return mbar_wait(k_patch, (n_patched++) & 1, p.err);
+            };
+            bool ok = mbar_wait(q_full, 0, p.err) && (n_kt == 0 || k_ready(0, 0, 0));
             if (ok && n_kt > 0) {
                 tc_fence_after();
                 issue_qk(0, 0);
@@ -311,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (a == 1) tc_commit(&v_empty[vst]);
                     if (more) {
                         if (a == 0) {
-                            ok = mbar_wait(&k_full[kst], kph, p.err);
+                            ok = k_ready(j + 1, kst, kph);
                             if (!ok) break;
                             tc_fence_after();
                         }
@@ -331,11 +357,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------- V to f16
         // as in the prefill kernel: each V tile rewritten in place, a
-        // magnitude of 2^16 or more saturated and reported
+        // magnitude of 2^16 or more saturated and reported.  A tile holding
+        // the step's rows takes them from k_new / v_new: K as soon as its
+        // copy lands (every thread patches its share, fences and arrives on
+        // k_patch, which the MMA warp waits for instead), V after the
+        // conversion, each thread over the pieces it has just converted
+        // itself (piece i of a tile is thread i % 64's), so no thread waits
+        // for another.
         const int ct = threadIdx.x - 64;  // 0 .. 63
+        if (fused) {
+            // The step's rows into the cache for later steps (this launch
+            // reads them from k_new / v_new), before the first V tile lands:
+            // rows blockIdx.x, + gridDim.x, ..., each tensor's row a run of
+            // 16-byte pieces at its slot.
+            const int64_t n_new = (int64_t)p.batch * R;
+            const int pieces = p.n_kv_heads * HD / 8;
+            for (int64_t row = blockIdx.x; row < n_new; row += gridDim.x) {
+                const int64_t slot = p.slot_mapping[row];
+                if (slot < 0 || slot >= p.num_slots) {
+                    if (ct == 0) report_error(p.err, ATTN_ERR_BOUNDS);
+                    continue;
+                }
+                const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new) + row * pieces;
+                const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new) + row * pieces;
+                uint4 *kd = reinterpret_cast<uint4 *>(p.k_cache) + slot * pieces;
+                uint4 *vd = reinterpret_cast<uint4 *>(p.v_cache) + slot * pieces;
+                for (int pc = ct; pc < pieces; pc += 64) {
+                    kd[pc] = __ldg(ks + pc);
+                    vd[pc] = __ldg(vs + pc);
+                }
+            }
+        }
         int vst = 0, vph = 0;
         bool ok = true;
+        // the step's row at key t (new_lo <= t < n_keys) as 16-byte pieces
+        auto new_row = [&](const __nv_bfloat16 *rows, int t) {
+            return reinterpret_cast<const uint4 *>(
+                rows + (((int64_t)b * R + (t - new_lo)) * p.n_kv_heads + kvh) * HD);
+        };
         for (int j = 0; j < n_kt && ok; ++j) {
+            const bool nw = tile_new(j);
+            const int key0 = (kt0 + j) * kBN;
+            if (nw) {
+                // K(j) is issued before V(j); its stage is not refilled before
+                // the MMA warp, which waits for this patch, has read it
+                const int kst = j % C::kKStages;
+                ok = mbar_wait(&k_full[kst], (j / C::kKStages) & 1, p.err);
+                __syncwarp();
+                if (!ok) break;
+                // rows r0 .. r1 - 1 of the [half][128 rows][128 B] swizzled tile
+                const uint32_t kb = smem_u32(sK + kst * C::kKBytes);
+                const int r0 = max(key0, new_lo) - key0, r1 = min(key0 + kBN, n_keys) - key0;
+                constexpr int kPieces = HD / 8;  // 16-byte pieces of a head row
+                for (int i = ct; i < (r1 - r0) * kPieces; i += 64) {
+                    const int r = r0 + i / kPieces, pc = i % kPieces;
+                    st_shared_v4(kb + (pc >> 3) * (kBN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4),
+                                 __ldg(new_row(p.k_new, key0 + r) + pc));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(k_patch);
+            }
             ok = mbar_wait(&v_full[vst], vph, p.err);
             __syncwarp();
             if (!ok) break;
@@ -353,6 +434,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     u[e] = pack_f16x2_sat(x0, x1);
                 }
                 st_shared_v4(base + i * 16, w);
+            }
+            if (nw) {
+                // the step's rows of this tile, converted the same way: this
+                // thread's pieces of row r are those of rows r = ct / 8 mod 8,
+                // swizzled position ct % 8 (logical piece (ct % 8) ^ (r % 8))
+                const int r0 = max(key0, new_lo) - key0, r1 = min(key0 + kBN, n_keys) - key0;
+                const int rr = ct >> 3, c = (ct & 7) ^ rr;
+                for (int r = r0 + ((rr - r0) & 7); r < r1; r += 8) {
+                    const uint4 *src = new_row(p.v_new, key0 + r);
+                    for (int hf = 0; hf < C::kHalves; ++hf) {
+                        uint4 w = __ldg(src + hf * 8 + c);
+                        uint32_t *u = &w.x;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = __uint_as_float(u[e] << 16);
+                            const float x1 = __uint_as_float(u[e] & 0xFFFF0000u);
+                            amax = max3(amax, fabsf(x0), fabsf(x1));
+                            u[e] = pack_f16x2_sat(x0, x1);
+                        }
+                        st_shared_v4(base + (hf * (kBN * 8) + r * 8 + (ct & 7)) * 16, w);
+                    }
+                }
             }
             if (!(amax < 65536.f)) report_error(p.err, ATTN_ERR_UNSUPPORTED);
             fence_proxy_async_smem();
@@ -690,7 +793,8 @@ void plan_chunk(int batch, int q_rows, int n_q_heads, int n_kv_heads, int head_d
 int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cache,
                  const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                  int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
-                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream) {
+                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream,
+                 const void *k_new, const void *v_new, const int64_t *slot_mapping) {
     chk::Params p;
     p.batch = batch;
     p.q_rows = q_rows;
@@ -712,6 +816,13 @@ int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cach
                                                                head_dim)
                       : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(out);
+    const bool fused = k_new != nullptr && v_new != nullptr && slot_mapping != nullptr;
+    p.k_new = fused ? static_cast<const __nv_bfloat16 *>(k_new) : nullptr;
+    p.v_new = fused ? static_cast<const __nv_bfloat16 *>(v_new) : nullptr;
+    p.slot_mapping = fused ? slot_mapping : nullptr;
+    p.num_slots = cache->num_slots;
+    p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+    p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
     p.err = err;
     // q viewed as {head_dim, n_q_heads, q_rows, batch}: a box of {64, G, rt, 1}
     // lands as rt x G rows of 128 bytes, the packed tile rows.

@@ -1970,17 +1970,12 @@ int launch_decode(const DecodePlan &plan, const void *q, const attn_kv_cache *ca
                   const void *k_new, const void *v_new, const int64_t *slot_mapping,
                   const float *rope_inv_freq, bool tables_early, bool cache_early) {
     if (plan.chunk && rope_inv_freq == nullptr) {
-        // the step's rows first (every CTA of the chunk kernel may read them)
-        if (k_new) {
-            const KvPlace place = kv_place(cache, n_kv_heads, plan.head_dim, 2);
-            const int rc = launch_kv_append(k_new, v_new, slot_mapping, (int64_t)batch * q_rows,
-                                            cache->k, cache->v, cache->num_slots, place, err,
-                                            stream);
-            if (rc != ATTN_OK) return rc;
-        }
+        // the step's rows, when given, are fused into the chunk kernel: taken
+        // from k_new / v_new and written to the cache by the same launch
         return launch_chunk(plan.cp, q, cache, seq_lens, positions, batch, q_rows, max_seq_len,
                             window, n_q_heads, n_kv_heads, plan.head_dim, scale, out,
-                            static_cast<uint8_t *>(workspace) + plan.chunk_offset, err, stream);
+                            static_cast<uint8_t *>(workspace) + plan.chunk_offset, err, stream,
+                            k_new, v_new, slot_mapping);
     }
     // TMA maps over the caches viewed as [n_kv_heads * halves][num_slots][cols]
     // (a half is 128 bytes of one head's row: 64 bf16 or 128 E4M3 columns): a

@@ -85,8 +85,8 @@ int launch_kv_reference(const void *k, int64_t n, int row_elems, float *ref,
 
 // Chunk plan (many query rows per KV group over a linear slot-major bf16
 // cache, chunk.cu): rt chunk rows per 128-row tcgen05 tile, n_pairs tile
-// pairs, n_split CTAs along each key range, and the fp32 partial states
-// (n_split > 1) the merge combines.
+// pairs, n_split CTAs along each key range, and the partial states (n_split >
+// 1: f16 O, fp32 log-sum-exp) the merge combines.
 struct ChunkPlan {
     int rt, n_pairs, n_split;
     size_t workspace;
@@ -95,10 +95,14 @@ struct ChunkPlan {
 void plan_chunk(int batch, int q_rows, int n_q_heads, int n_kv_heads, int head_dim,
                 int max_seq_len, int window, ChunkPlan *plan);
 
+// k_new / v_new / slot_mapping non-null: the step's rows are taken from
+// k_new / v_new and written to the cache by the same launch (attn_decode_append).
 int launch_chunk(const ChunkPlan &plan, const void *q, const attn_kv_cache *cache,
                  const int32_t *seq_lens, const int32_t *positions, int batch, int q_rows,
                  int max_seq_len, int window, int n_q_heads, int n_kv_heads, int head_dim,
-                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream);
+                 float scale, void *out, void *workspace, int32_t *err, cudaStream_t stream,
+                 const void *k_new = nullptr, const void *v_new = nullptr,
+                 const int64_t *slot_mapping = nullptr);
 
 // Decode plan: a persistent grid of one CTA per SM; requests are processed
 // in launches of at most batch_per_launch (the per-request tables live in

@@ -205,9 +205,10 @@ size_t attn_decode_workspace_size(const attn_kv_cache *cache, int batch, int q_r
  * tables hold, each followed by the merge kernel when units of this shape may
  * be split over enough CTAs to need it.  A group of 64 or more query rows (q_rows x
  * n_q_heads / n_kv_heads) over a linear slot-major bf16 cache, without a
- * rotary embedding, is a prefill chunk: the append kernel (attn_decode_append
- * only), the tcgen05 chunk kernel, and its merge kernel when the key range is
- * split over CTAs.  Returns -1 for arguments attn_decode would reject, 0 for
+ * rotary embedding, is a prefill chunk: the tcgen05 chunk kernel (which, for
+ * attn_decode_append, also takes the step's rows from k_new / v_new and writes
+ * them to the cache), and its merge kernel when the key range is split over
+ * CTAs.  Returns -1 for arguments attn_decode would reject, 0 for
  * batch 0.
  */
 int attn_decode_kernel_launches(const attn_kv_cache *cache, int batch, int q_rows, int n_q_heads,

@@ -144,12 +144,13 @@ def test_decode_kernel_launches(lib):
     assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 3) == 2  # both early flags
     assert f(ctypes.byref(cs), 2, 1, 32, 8, 128, 8192, 0, 1, 0, 4) == -1  # unknown flag
     # a 29-row chunk of a 28/4 group (203 rows) over a linear cache: the chunk
-    # kernel (+ its merge: 2 x 4 groups split over the key range; + the
-    # append for attn_decode_append); with a rotary embedding the split kernel
+    # kernel (+ its merge: 2 x 4 groups split over the key range; the append of
+    # attn_decode_append is inside the chunk kernel); with a rotary embedding
+    # the split kernel
     ch = cache(slots=14464 * 2, sps=14464, Hkv=4)
     hs = ch.struct()
     assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 0, 0, 0) == 2
-    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 0, 0) == 3
+    assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 0, 0) == 2
     assert f(ctypes.byref(hs), 2, 29, 28, 4, 128, 14449, 0, 1, 1, 0) == 1
 
 

@@ -78,13 +78,33 @@ def test_chunk_kernel_window():
 
 
 def test_chunk_kernel_fused_append_and_rope_fallback():
-    """attn_decode_append on a chunk: the append kernel, then the chunk
-    kernel (and its merge); with a rotary embedding the split kernel."""
+    """attn_decode_append on a chunk: the chunk kernel takes the step's rows
+    from k_new / v_new and writes them to the cache (then its merge); with a
+    rotary embedding the split kernel."""
     from test_gpu_decode_append import _run
 
     case = synth.decode_case(8500, synth.LINEAR, 2, 29, 28, 4, 128, [14449, 3000])
-    assert launches(case, with_append=True) == 3
+    assert launches(case, with_append=True) == 2
     assert launches(case, with_append=True, with_rope=True) == 1
     fused, _ = _run(case, fused=True)
     ref, _, _ = oracle_decode(case)
     compare(fused, ref, "fused chunk")
+
+
+@pytest.mark.parametrize("seq", [[14480, 1030], [14449, 3000], [200, 64]])
+def test_chunk_fused_append_equals_append_then_decode(seq):
+    """The chunk kernel with the step's rows fused in (taken from k_new / v_new,
+    written to the cache by the same launch) equals the append kernel followed
+    by the chunk kernel, output and cache bit for bit: new rows straddling a
+    key-tile boundary (14,451..14,479 over 14,464; 1,001..1,029 over 1,024),
+    inside one tile, and a short request."""
+    from test_gpu_decode_append import _run
+
+    case = synth.decode_case(8600 + seq[1], synth.LINEAR, 2, 29, 28, 4, 128, seq)
+    assert launches(case, with_append=True) <= 2  # the chunk kernel (+ its merge)
+    out_f, cache_f = _run(case, fused=True)
+    out_u, cache_u = _run(case, fused=False)
+    assert torch.equal(out_f, out_u), "fused chunk differs from append + chunk"
+    assert torch.equal(cache_f.k, cache_u.k) and torch.equal(cache_f.v, cache_u.v)
+    ref, _, _ = oracle_decode(case)
+    compare(out_f, ref, f"fused chunk {seq}")
