@@ -279,9 +279,10 @@ class QwenWorkload(Workload):
         gq = self.gq
         for i, d in enumerate(self.dec):
             if e2e:
-                hd = self.h["dec"][i]
-                for key in ("q", "k_new", "v_new", "slots", "seq", "pos"):
-                    d[key].copy_(hd[key], non_blocking=True)
+                # this call's inputs, packed in one pinned buffer: one transfer
+                pk = self.h["dec"][i]
+                pk["dev"].copy_(pk["host"], non_blocking=True)
+                d = pk["views"] | {"out": d["out"]}
             c = self.caches[(s * 6 + 1 + i) % self.ncopy]
             # seq_lens / positions are written before the step, never by the
             # kernel just before a decode, and the caches rotate, so no kernel
@@ -329,19 +330,37 @@ class QwenWorkload(Workload):
         ev("end")
 
     # end to end through host buffers ---------------------------------------
+    def _packed(self, d):
+        """A decode call's inputs (q, k_new, v_new, slot_mapping, seq_lens,
+        positions) at 256-byte offsets of one pinned host buffer, with views of
+        the same offsets into one device buffer: the call copies them with one
+        transfer, as a serving engine stages a step's inputs."""
+        torch = self.torch
+        keys = ("q", "k_new", "v_new", "slots", "seq", "pos")
+        offs, n = [], 0
+        for k in keys:
+            offs.append(n)
+            n += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
+        host = torch.empty(n, dtype=torch.uint8).pin_memory()
+        dev = torch.empty(n, dtype=torch.uint8, device=d["q"].device)
+        views = {}
+        for k, o in zip(keys, offs):
+            t = d[k]
+            nb = t.numel() * t.element_size()
+            host[o:o + nb].view(t.dtype).view(t.shape).copy_(t.detach().cpu())
+            views[k] = dev[o:o + nb].view(t.dtype).view(t.shape)
+        return {"host": host, "dev": dev, "views": views,
+                "out": torch.empty(d["q"].shape, dtype=d["q"].dtype).pin_memory()}
+
     def setup_host(self):
         torch = self.torch
         pin = lambda t: t.detach().to("cpu").pin_memory()
         self.h = {"q": pin(self.q), "k": pin(self.k), "v": pin(self.v),
                   "out": torch.empty(self.q.shape, dtype=self.q.dtype).pin_memory(),
-                  "dec": [{k: pin(v) for k, v in d.items() if k in
-                           ("q", "k_new", "v_new", "slots", "seq", "pos")} |
-                          {"out": torch.empty(d["q"].shape, dtype=d["q"].dtype).pin_memory()}
-                          for d in self.dec]}
+                  "dec": [self._packed(d) for d in self.dec]}
         self.h2d_prefill = sum(self.h[k].numel() * self.h[k].element_size() for k in "qkv")
         self.d2h_prefill = self.h["out"].numel() * self.h["out"].element_size()
-        self.h2d_decode = sum(t.numel() * t.element_size() for d in self.h["dec"]
-                              for k, t in d.items() if k != "out")
+        self.h2d_decode = sum(d["host"].numel() for d in self.h["dec"])
         self.d2h_decode = sum(d["out"].numel() * d["out"].element_size() for d in self.h["dec"])
 
     def run_step_e2e(self, ev):
