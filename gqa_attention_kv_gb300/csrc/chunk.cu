@@ -16,9 +16,11 @@
 // G positions per tile, the remaining rows padding).  A CTA takes two such
 // tiles and a range of key tiles: the key range of a (request, KV head) is
 // split over CTAs so that the few groups of a chunk still fill the GPU; each
-// CTA leaves a partial state per row (O / l in fp32 and the base-2 log-sum-
-// exp), and chunk_merge_kernel combines the splits in a fixed order.  One
-// split writes the bf16 rows itself.
+// CTA leaves a partial state per row (O / l in f16 and the base-2 log-sum-
+// exp in fp32), and chunk_merge_kernel combines the splits in a fixed order.
+// One split writes the bf16 rows itself.  Under attn_decode_append the step's
+// own rows are taken from k_new / v_new and written to the cache by the same
+// launch.
 //
 // The warp roles, rings, TMEM columns and the ping-pong of the two tiles are
 // those of the prefill kernel (prefill.cu): warp 0 issues TMA, warp 1 the
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run = l_run * alpha + (sum0 + sum1);
         }
         // epilogue: the row's O / l (bf16 when the key range is not split,
-        // else an fp32 partial state with its base-2 log-sum-exp)
+        // else an f16 partial state with its fp32 base-2 log-sum-exp)
         if (ok) ok = mbar_wait(o_done, 0, p.err);
         __syncwarp();
         tc_fence_after();

@@ -178,8 +178,8 @@ int attn_kv_reference(const void *k, int64_t n, int n_kv_heads, int head_dim, fl
 
 /*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
- * this shape: merge counters, then fp32 partial softmax states of the key
- * pieces different CTAs handle.  A call accepts any workspace at least this
+ * this shape: merge counters, then partial softmax states of the key pieces
+ * different CTAs handle (fp32; a prefill chunk's partial O in f16).  A call accepts any workspace at least this
  * large.  Returns (size_t)-1 for arguments attn_decode would reject.
  *
  * The workspace must be zero-filled before its first use; every call that
