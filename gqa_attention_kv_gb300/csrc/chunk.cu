@@ -654,12 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // One warp per packed row of a (request, KV head, pair): the splits' partial
 // states in split order, weights from the log-sum-exps, one bf16 rounding.
-// The lanes read 32 splits' log-sum-exps at once; the output pieces of eight
-// splits are in flight together.
+// Up to 32 splits are read in one round (each lane one split's log-sum-exp,
+// every lane its columns of all of them, f16): no load waits for another.
+// More splits go 32 at a time, the running sums rescaled to the new maximum.
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Params p) {
     constexpr int PER = HD / 32;
-    constexpr int kBatch = 8;
     pdl_wait();  // the partial states come from the chunk kernel
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -676,51 +676,53 @@ __global__ void __launch_bounds__(kMergeWarps * 32) chunk_merge_kernel(const Par
     if (row >= p.rt * G || r >= p.q_rows) return;
     const float *lse = p.ws_lse + grp * p.n_split * 2 * kBM + m;  // split s at s * 2 kBM
     const uint16_t *o = p.ws_o + (grp * p.n_split * 2 * kBM + m) * HD + lane * PER;
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < p.n_split; s0 += 32)
-        if (s0 + lane < p.n_split) M = fmaxf(M, __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM));
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
-    float L = 0.f, acc[PER];
+    constexpr int kRound = 32;
+    float M = -INFINITY, L = 0.f, acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    if (M != -INFINITY) {
-        for (int s0 = 0; s0 < p.n_split; s0 += 32) {
-            // this lane's split weight (0 for an empty split or past the end)
-            float w = 0.f;
-            if (s0 + lane < p.n_split) {
-                const float l = __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM);
-                w = l == -INFINITY ? 0.f : fast_exp2(l - M);
-            }
-            const int n = min(32, p.n_split - s0);
-            for (int k0 = 0; k0 < n; k0 += kBatch) {
-                float v[kBatch][PER];
+    for (int s0 = 0; s0 < p.n_split; s0 += kRound) {
+        const int n = min(kRound, p.n_split - s0);
+        // every load of the round issued before any is used
+        const float l = lane < n ? __ldcg(lse + (int64_t)(s0 + lane) * 2 * kBM) : -INFINITY;
+        uint32_t raw[kRound][PER / 2];
 #pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
+        for (int k = 0; k < kRound; ++k) {
 #pragma unroll
-                    for (int e = 0; e < PER; ++e) v[k][e] = 0.f;
-                    if (k0 + k < n) {
-                        const uint16_t *src = o + (int64_t)(s0 + k0 + k) * 2 * kBM * HD;
-                        if constexpr (PER == 4) {
-                            const uint2 t = __ldcg(reinterpret_cast<const uint2 *>(src));
-                            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
-                            const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
-                            v[k][0] = lo.x, v[k][1] = lo.y, v[k][2] = hi.x, v[k][3] = hi.y;
-                        } else {
-                            const uint32_t t = __ldcg(reinterpret_cast<const unsigned int *>(src));
-                            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&t));
-                            v[k][0] = lo.x, v[k][1] = lo.y;
-                        }
-                    }
+            for (int e = 0; e < PER / 2; ++e) raw[k][e] = 0u;
+            if (k < n) {
+                const uint16_t *src = o + (int64_t)(s0 + k) * 2 * kBM * HD;
+                if constexpr (PER == 4) {
+                    const uint2 t = __ldcg(reinterpret_cast<const uint2 *>(src));
+                    raw[k][0] = t.x;
+                    raw[k][1] = t.y;
+                } else {
+                    raw[k][0] = __ldcg(reinterpret_cast<const unsigned int *>(src));
                 }
+            }
+        }
+        float mr = l;
 #pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
-                    const float f = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                    if (k0 + k < n) {
-                        L += f;
+        for (int d = 16; d > 0; d >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, d));
+        const float Mn = fmaxf(M, mr);
+        if (Mn == -INFINITY) continue;  // no split so far saw a key
+        if (M != -INFINITY && Mn != M) {
+            const float rs = fast_exp2(M - Mn);
+            L *= rs;
 #pragma unroll
-                        for (int e = 0; e < PER; ++e) acc[e] += f * v[k][e];
-                    }
+            for (int e = 0; e < PER; ++e) acc[e] *= rs;
+        }
+        M = Mn;
+        const float w = l == -INFINITY ? 0.f : fast_exp2(l - M);  // this lane's split
+#pragma unroll
+        for (int k = 0; k < kRound; ++k) {
+            const float f = __shfl_sync(0xffffffffu, w, k);
+            if (k < n) {
+                L += f;
+#pragma unroll
+                for (int e = 0; e < PER / 2; ++e) {
+                    const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&raw[k][e]));
+                    acc[2 * e] += f * v.x;
+                    acc[2 * e + 1] += f * v.y;
                 }
             }
         }
