@@ -392,68 +392,111 @@ struct SegmentWalker {
 // slots s0, s0 + stride, ... (in that order, the order that fixes the
 // result), either into the bf16 output (final) or, as one partial state, back
 // into slot s0.  Partial states hold O / l and the base-2 log-sum-exp.  Run by
-// the four consumer warps; sl: shared staging of parts x RB floats.
+// the four consumer warps, each thread two output pieces (row, 4 columns) at
+// a time; for each it reads the log-sum-exps and pieces of up to kGroupParts
+// parts in one round (more parts go kGroupParts at a time, the running sums
+// rescaled to the new maximum).  Slot s0's log-sum-exps, which every thread
+// of a row reads, are overwritten only after the consumer barrier.  Ends with
+// that barrier.
 template <int HD, int RB>
 __device__ __forceinline__ void merge_partials(const Params &p, const Segment &u, int64_t s0,
-                                               int stride, int parts, bool final, float *sl,
-                                               int ctid) {
+                                               int stride, int parts, bool final, int ctid) {
+    constexpr int kItems = RB * (HD / 4) / (kWarps * 32);  // output pieces per thread
+    constexpr int kPair = (kItems >= 2 && RB <= 8) ? 2 : 1;  // registers: pairs for 8-row units
+    static_assert(kItems * kWarps * 32 == RB * (HD / 4) && kItems % kPair == 0, "whole items");
     const int row0 = u.rb * RB, row1 = min(p.rows, row0 + RB);
-    for (int i = ctid; i < parts * RB; i += kWarps * 32) {
-        const int c = i / RB, row = i - (i / RB) * RB;
-        sl[i] = __ldcg(p.ws_lse + (s0 + (int64_t)c * stride) * RB + row);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-    for (int idx = ctid; idx < RB * (HD / 4); idx += kWarps * 32) {
-        const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
-        const int i = row0 + row;
-        if (i >= row1) continue;
-        float M = -INFINITY;
-        for (int c = 0; c < parts; ++c) M = fmaxf(M, sl[c * RB + row]);
-        float Lsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-            // kGroupParts loads in flight at a time
-            for (int c0 = 0; c0 < parts; c0 += kGroupParts) {
-                float f[kGroupParts];
-                float4 v[kGroupParts];
+    float lse_out[kItems];
+#pragma unroll
+    for (int q0 = 0; q0 < kItems; q0 += kPair) {
+        float M[kPair], Lsum[kPair];
+        float4 acc[kPair];
+#pragma unroll
+        for (int q = 0; q < kPair; ++q) {
+            M[q] = -INFINITY;
+            Lsum[q] = 0.f;
+            acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int c0 = 0; c0 < parts; c0 += kGroupParts) {
+            float l[kPair][kGroupParts];
+            float4 v[kPair][kGroupParts];
+#pragma unroll
+            for (int q = 0; q < kPair; ++q) {
+                const int idx = ctid + (q0 + q) * (kWarps * 32);
+                const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+                const bool live = row0 + row < row1;
 #pragma unroll
                 for (int k = 0; k < kGroupParts; ++k) {
                     const int c = c0 + k;
-                    f[k] = 0.f;
-                    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (c < parts) {
-                        f[k] = fast_exp2(sl[c * RB + row] - M);  // -inf gives 0
-                        v[k] = __ldcg(reinterpret_cast<const float4 *>(
-                            p.ws_o + ((s0 + (int64_t)c * stride) * RB + row) * HD + d));
+                    l[q][k] = -INFINITY;
+                    v[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (live && c < parts) {
+                        const int64_t slot = s0 + (int64_t)c * stride;
+                        l[q][k] = __ldcg(p.ws_lse + slot * RB + row);
+                        v[q][k] = __ldcg(
+                            reinterpret_cast<const float4 *>(p.ws_o + (slot * RB + row) * HD + d));
                     }
                 }
+            }
+#pragma unroll
+            for (int q = 0; q < kPair; ++q) {
+                float Mn = M[q];
+#pragma unroll
+                for (int k = 0; k < kGroupParts; ++k) Mn = fmaxf(Mn, l[q][k]);
+                if (Mn == -INFINITY) continue;  // no part so far holds a key
+                if (M[q] != -INFINITY && Mn != M[q]) {
+                    const float rs = fast_exp2(M[q] - Mn);
+                    Lsum[q] *= rs;
+                    acc[q].x *= rs;
+                    acc[q].y *= rs;
+                    acc[q].z *= rs;
+                    acc[q].w *= rs;
+                }
+                M[q] = Mn;
 #pragma unroll
                 for (int k = 0; k < kGroupParts; ++k) {
-                    Lsum += f[k];
-                    acc.x += f[k] * v[k].x;
-                    acc.y += f[k] * v[k].y;
-                    acc.z += f[k] * v[k].z;
-                    acc.w += f[k] * v[k].w;
+                    const float f = fast_exp2(l[q][k] - Mn);  // -inf gives 0
+                    Lsum[q] += f;
+                    acc[q].x += f * v[q][k].x;
+                    acc[q].y += f * v[q][k].y;
+                    acc[q].z += f * v[q][k].z;
+                    acc[q].w += f * v[q][k].w;
                 }
             }
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        if (final) {
-            const int r = i / p.group, g = i - (i / p.group) * p.group;
-            __nv_bfloat16 *dst =
-                p.out + (((int64_t)u.b * p.q_rows + r) * p.n_q_heads + u.kvh * p.group + g) * HD + d;
-            uint2 packed;
-            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2 *>(dst) = packed;
-        } else {
-            // this thread read (row, d) of slot s0 itself: the overwrite is safe
-            *reinterpret_cast<float4 *>(p.ws_o + (s0 * RB + row) * HD + d) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (d == 0) p.ws_lse[s0 * RB + row] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kPair; ++q) {
+            const int idx = ctid + (q0 + q) * (kWarps * 32);
+            const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+            const int i = row0 + row;
+            lse_out[q0 + q] = Lsum[q] > 0.f ? M[q] + __log2f(Lsum[q]) : -INFINITY;
+            if (i >= row1) continue;
+            const float inv = Lsum[q] > 0.f ? 1.f / Lsum[q] : 0.f;
+            if (final) {
+                const int r = i / p.group, g = i - (i / p.group) * p.group;
+                __nv_bfloat16 *dst =
+                    p.out + (((int64_t)u.b * p.q_rows + r) * p.n_q_heads + u.kvh * p.group + g) * HD +
+                    d;
+                uint2 packed;
+                packed.x = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
+                packed.y = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
+                *reinterpret_cast<uint2 *>(dst) = packed;
+            } else {
+                // this thread alone reads (row, d) of slot s0: the overwrite is safe
+                *reinterpret_cast<float4 *>(p.ws_o + (s0 * RB + row) * HD + d) =
+                    make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+            }
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // staging free again
+    if (!final) {
+        asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // all reads of slot s0 done
+#pragma unroll
+        for (int q = 0; q < kItems; ++q) {
+            const int idx = ctid + q * (kWarps * 32);
+            const int row = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+            if (d == 0 && row0 + row < row1) p.ws_lse[s0 * RB + row] = lse_out[q];
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 }
 
 // ROPE: the fused append's rotary embedding (its code is compiled only into
@@ -1669,14 +1712,12 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
     // merges the group, in CTA order, into that slot; the CTA that completes
     // a unit's last group (per-unit counter) merges the groups in order into
     // the bf16 output.  A unit of at most kGroupParts parts is one group
-    // merged straight to the output.  The ring is drained, so the stages
-    // are free for staging.  Ordering: the consumer barrier puts every
+    // merged straight to the output.  Ordering: the consumer barrier puts every
     // thread's partial stores before thread 0's counter update, whose release
     // (gpu scope, cumulative) publishes them; the CTA whose update completes a
     // group acquires the others' by the same update, and the barrier after it
     // orders its threads' loads after that acquire.
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-    float *sl = reinterpret_cast<float *>(stages);  // [parts][RB] log-sum-exps
     for (int k = 0; k < n_pend; ++k) {
         const Segment &u = k == 0 ? pend0 : pend1;
         const int n = u.last - u.first + 1;
@@ -1692,11 +1733,11 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         if (!s_last[2 * k]) continue;  // uniform across the consumer warps
         if (n <= kGroupParts) {
-            merge_partials<HD, RB>(p, u, gslot, 1, n, true, sl, ctid);
+            merge_partials<HD, RB>(p, u, gslot, 1, n, true, ctid);
             if (ctid == 0) p.ws_count[u.unit] = 0;  // ready for the next call
             continue;
         }
-        merge_partials<HD, RB>(p, u, gslot, 1, gl - gf + 1, false, sl, ctid);
+        merge_partials<HD, RB>(p, u, gslot, 1, gl - gf + 1, false, ctid);
         // (merge_partials ends with the consumer barrier: its stores precede
         // the release below)
         const int groups = (n + kGroupParts - 1) / kGroupParts;
@@ -1706,8 +1747,7 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
         if (!s_last[2 * k + 1]) continue;
-        merge_partials<HD, RB>(p, u, (int64_t)u.unit + u.first, kGroupParts, groups, true, sl,
-                               ctid);
+        merge_partials<HD, RB>(p, u, (int64_t)u.unit + u.first, kGroupParts, groups, true, ctid);
         if (ctid == 0) p.ws_count[u.unit] = 0;
     }
 }
