@@ -91,16 +91,19 @@ def test_chunk_kernel_fused_append_and_rope_fallback():
     compare(fused, ref, "fused chunk")
 
 
-@pytest.mark.parametrize("seq", [[14480, 1030], [14449, 3000], [200, 64]])
-def test_chunk_fused_append_equals_append_then_decode(seq):
+@pytest.mark.parametrize("R,Hq,Hkv,D,seq", [(29, 28, 4, 128, [14480, 1030]),
+                                             (29, 28, 4, 128, [14449, 3000]),
+                                             (29, 28, 4, 128, [200, 64]),
+                                             (16, 32, 8, 64, [700, 136])])
+def test_chunk_fused_append_equals_append_then_decode(R, Hq, Hkv, D, seq):
     """The chunk kernel with the step's rows fused in (taken from k_new / v_new,
     written to the cache by the same launch) equals the append kernel followed
     by the chunk kernel, output and cache bit for bit: new rows straddling a
-    key-tile boundary (14,451..14,479 over 14,464; 1,001..1,029 over 1,024),
-    inside one tile, and a short request."""
+    key-tile boundary (14,451..14,479 over 14,464; 1,001..1,029 over 1,024;
+    120..135 over 128 at head_dim 64), inside one tile, and a short request."""
     from test_gpu_decode_append import _run
 
-    case = synth.decode_case(8600 + seq[1], synth.LINEAR, 2, 29, 28, 4, 128, seq)
+    case = synth.decode_case(8600 + seq[1] + D, synth.LINEAR, 2, R, Hq, Hkv, D, seq)
     assert launches(case, with_append=True) <= 2  # the chunk kernel (+ its merge)
     out_f, cache_f = _run(case, fused=True)
     out_u, cache_u = _run(case, fused=False)
