@@ -84,7 +84,8 @@ struct Cfg {
 
 struct Params {
     int batch, seq_len, window, n_q_heads, n_kv_heads, group;
-    int n_pairs;  // CTAs along the sequence (256 query rows each)
+    int n_pairs;  // CTAs along the sequence (256 query rows each, 128 when single)
+    int single;   // 1: one Q tile per CTA (the second tile is absent)
     float scale_log2;
     int32_t *err;
 };
@@ -122,8 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = rest % p.n_q_heads;
     const int b = rest / p.n_q_heads;
     const int g = h / p.group;
-    const int q0 = pair * 2 * kBM;
-    const int key_hi = min(p.seq_len, q0 + 2 * kBM);  // exclusive
+    const int rows = p.single ? kBM : 2 * kBM;  // query rows of this CTA
+    const int q0 = pair * rows;
+    const int key_hi = min(p.seq_len, q0 + rows);  // exclusive
     const int key_lo = p.window > 0 ? max(0, q0 - p.window + 1) : 0;
     const int kt0 = key_lo / kBN;
     const int n_kt = (key_hi + kBN - 1) / kBN - kt0;
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // computed: the MMA issuer and the softmax warps both skip it.
     auto live = [&](int a, int j) -> bool {
         const int qa = q0 + a * kBM, key0 = tile_of(j) * kBN;
-        return qa < p.seq_len && key0 <= qa + kBM - 1 &&
+        return (a == 0 || !p.single) && qa < p.seq_len && key0 <= qa + kBM - 1 &&
                (p.window <= 0 || qa - (key0 + kBN - 1) < p.window);
     };
 
@@ -186,8 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 2 * C::kQBytes);
-            for (int a = 0; a < 2; ++a)
+            const int n_q = p.single ? 1 : 2;
+            mbar_arrive_expect_tx(q_full, n_q * C::kQBytes);
+            for (int a = 0; a < n_q; ++a)
                 for (int hf = 0; hf < C::kHalves; ++hf)
                     tma_load_3d(sQ + a * C::kQBytes + hf * (kBM * 128), &tm_q, h * HD + hf * 64,
                                 q0 + a * kBM, b, q_full);
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("bar.sync 1, 128;" ::: "memory");
         else
             asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (quad == 0 && lane == 0 && ok && qa0 < p.seq_len) {
+        if (quad == 0 && lane == 0 && ok && qa0 < p.seq_len && (a == 0 || !p.single)) {
             for (int hf = 0; hf < C::kHalves; ++hf)
                 tma_store_3d(&tm_o, stage + hf * (kBM * 128), h * HD + hf * 64, qa0, b);
             tma_store_commit();
@@ -536,7 +539,15 @@ int launch_prefill(const void *q, const void *k, const void *v, int batch, int s
     p.n_q_heads = n_q_heads;
     p.n_kv_heads = n_kv_heads;
     p.group = n_q_heads / n_kv_heads;
-    p.n_pairs = (seq_len + 2 * pre::kBM - 1) / (2 * pre::kBM);
+    // Two Q tiles per CTA share every K/V tile and ping-pong on the tensor
+    // core; when those CTAs would not fill the SMs (short sequences), each CTA
+    // takes one tile instead: twice the CTAs, and the longest CTA's chain of
+    // key tiles runs alone (~1 us a tile instead of ~1.5 for the pair).
+    const int64_t pair_ctas =
+        (int64_t)((seq_len + 2 * pre::kBM - 1) / (2 * pre::kBM)) * n_q_heads * batch;
+    p.single = pair_ctas < device_sm_count() ? 1 : 0;
+    p.n_pairs = p.single ? (seq_len + pre::kBM - 1) / pre::kBM
+                         : (seq_len + 2 * pre::kBM - 1) / (2 * pre::kBM);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     CUtensorMap tq, tk, tv, to;
