@@ -62,10 +62,10 @@ def load_peaks():
 # T = 14,449, from ncu (profiles/prefill_kernel_qwen14449.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 198478080,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 198134272,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "64deabd02f1b96d26995ade49049e8b175b525c83d5e97cb1183314abe0fcd13"}
+                   "sha256": "b71c0f0c22d0a85c0c1979b2f2488211eb5a2fbc948df1f8934ffe7d89c41ba3"}
 
 
 def prefill_traffic(T):
