@@ -57,8 +57,10 @@ constexpr int kMergeWarps = 8;
 template <int HD>
 struct Cfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kKStages = HD == 128 ? 2 : 4;
-    static constexpr int kVStages = HD == 128 ? 3 : 4;
+    // rings: three K stages, two V (measured 1.4% faster than two and three at
+    // D = 128; K's depth gates how far ahead the tiles are requested)
+    static constexpr int kKStages = HD == 128 ? 3 : 4;
+    static constexpr int kVStages = HD == 128 ? 2 : 4;
     static constexpr int kQBytes = kBM * HD * 2;  // one Q tile
     static constexpr int kKBytes = kBN * HD * 2;
     static constexpr int kVBytes = kBN * HD * 2;
