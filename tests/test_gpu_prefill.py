@@ -65,6 +65,21 @@ def test_window_gqa(T, W, Hq, Hkv, D):
     compare(out, ref, f"T={T} W={W} {Hq}/{Hkv} D={D}")
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [(3, 1500, 16, 4, 128, 0), (2, 2333, 32, 8, 64, 700)])
+def test_two_tile_ctas_batched(B, T, Hq, Hkv, D, W):
+    """Launches large enough for two Q tiles per CTA (pairs x heads x batch at
+    least the SM count) with several sequences, a ragged length and a window,
+    checked on sampled rows: every tile edge of the first and last sequence's
+    pairs, the first and last rows, and seeded random rows."""
+    p = synth.prefill_case(700 + T + W, B, T, Hq, Hkv, D, window=W)
+    edges = [r for t in range(128, T, 128) for r in (t - 1, t)]
+    g = np.random.default_rng(T)
+    rows = sorted(set(list(range(8)) + list(range(T - 8, T)) + edges[::3] +
+                      g.integers(0, T, 24).tolist()))
+    out, ref = run(p, rows=rows)
+    compare(out, ref, f"B={B} T={T} {Hq}/{Hkv} D={D} W={W} (sampled rows)")
+
+
 def test_encoder_prefill_full():
     """The speech-encoder shape at full size: T=750, 32 heads, D=64."""
     p = synth.encoder_prefill()
@@ -141,8 +156,8 @@ def test_v_beyond_f16_is_reported():
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [(2, 513, 8, 2, 128, 0), (1, 1100, 4, 4, 64, 300),
                                             (3, 900, 6, 3, 128, 0), (1, 640, 2, 1, 64, 129)])
 def test_small_launches(B, T, Hq, Hkv, D, W):
-    """Launches that leave SMs idle (fewer CTAs than SMs, long last pairs):
-    batches, GQA, both head dims and windows."""
+    """Launches of fewer Q-tile pairs than SMs (one Q tile per CTA): batches,
+    GQA, both head dims and windows."""
     p = synth.prefill_case(500 + T + D + W, B, T, Hq, Hkv, D, window=W)
     out, ref = run(p)
     compare(out, ref, f"B={B} T={T} {Hq}/{Hkv} D={D} W={W}")
