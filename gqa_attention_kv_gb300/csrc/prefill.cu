@@ -11,6 +11,8 @@
 // one head; both walk the same key tiles, so every K/V tile is loaded once for
 // 256 query rows, and the two tiles ping-pong: while one softmax warpgroup
 // works on its scores the tensor core computes the other tile's QK^T and PV.
+// When such pairs would not fill the SMs (short sequences), a CTA takes one
+// tile (Q0) and its critical chain of key tiles runs alone, faster per tile.
 //
 //   warp 0      TMA producer: Q0, Q1 once; then K tiles (2-stage ring) and V
 //               tiles (3-stage ring) of 128 keys, 128-byte swizzled, through
