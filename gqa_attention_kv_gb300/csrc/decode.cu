@@ -69,6 +69,11 @@ constexpr int kMinChunksPerCta = 8;          // smallest share of key chunks per
 // much less real work.
 constexpr int kUnitGapChunks = 12;
 constexpr int kGroupParts = 8;               // partial states merged by one CTA at a time
+// Lazy rescale of the running output: a row's reference maximum moves only
+// when a chunk's scores pass it by more than this (log2 units), so P stays
+// <= 2^8 (exact range of f16 and of the bf16 hi + lo split) and the warp
+// skips the rescale of O whenever none of its rows moved.
+constexpr float kRescaleLog2 = 8.0f;
 // merge kernel CTA: four warps.  Beside two split CTAs (165 registers, three
 // warps on two of the SM's four sub-partitions) one no longer fits, so merge
 // CTAs take SMs as split CTAs leave them.
@@ -247,6 +252,16 @@ __device__ __forceinline__ int park_unit(int row, int u) {
     if constexpr (!FP8) return u;
     else if constexpr (MT == 0) return u ^ ((row >> 1) & 3);
     else return u ^ ((2 * (u >> 3) + (row & 1)) & 7);
+}
+
+// Whether every key t0 .. t0 + 15 of a chunk is visible to query rows at
+// positions pmin .. pmax: all present (mask16), inside the sequence and the
+// ring, causal for the earliest row and inside the window of the latest.
+__device__ __forceinline__ bool chunk_open(uint32_t mask16, int t0, int seq_len, int ring_lo,
+                                           int window, int pmin, int pmax) {
+    const int t1 = t0 + kChunk - 1;
+    return mask16 == 0xFFFFu && t1 < seq_len && t1 <= pmin && t0 >= ring_lo &&
+           (window <= 0 || pmax - t0 < window);
 }
 
 // Key chunk range of unit (request b, row block rb): chunk c covers positions
@@ -1228,28 +1243,41 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+                    // the whole chunk visible to every row of the warp: no mask (a
+                    // padding row repeats the unit's first row and position; its
+                    // results are never stored)
+                    if (__all_sync(0xffffffffu,
+                                   chunk_open(mask16, t0, seq_len, ring_lo, window,
+                                              min(cpos[0], cpos[1]), max(cpos[0], cpos[1])))) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sacc[e] *= p.scale_log2;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)  // row 2tq + e: elements e (key gq), e+2 (key gq+8)
+#pragma unroll
+                            for (int hk = 0; hk < 2; ++hk) {
+                                const int n = gq + hk * 8;
+                                const int t = t0 + n, pos = cpos[e];
+                                const bool valid = cvalid[e] && ((mask16 >> n) & 1u) &&
+                                                   t < seq_len && t <= pos && t >= ring_lo &&
+                                                   (window <= 0 || pos - t < window);
+                                sacc[e + 2 * hk] =
+                                    valid ? sacc[e + 2 * hk] * p.scale_log2 : -INFINITY;
+                            }
+                    }
                     float alpha[2];
+                    bool moved = false;
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {  // row 2tq + e: elements e (key gq), e+2 (key gq+8)
-                        const int pos = cpos[e];
-                        float mx = -INFINITY;
-#pragma unroll
-                        for (int hk = 0; hk < 2; ++hk) {
-                            const int n = gq + hk * 8;
-                            const int t = t0 + n;
-                            const bool valid = cvalid[e] && ((mask16 >> n) & 1u) && t < seq_len &&
-                                               t <= pos && t >= ring_lo &&
-                                               (window <= 0 || pos - t < window);
-                            const float v = valid ? sacc[e + 2 * hk] * p.scale_log2 : -INFINITY;
-                            sacc[e + 2 * hk] = v;
-                            mx = fmaxf(mx, v);
-                        }
+                    for (int e = 0; e < 2; ++e) {
+                        float mx = fmaxf(sacc[e], sacc[e + 2]);
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float m_new = fmaxf(m_run[e], mx);
+                        const float m_old = m_run[e];
+                        const float m_new = mx > m_old + kRescaleLog2 ? mx : m_old;
                         const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                        alpha[e] = fast_exp2(m_run[e] - m_use);
+                        alpha[e] = m_new == m_old ? 1.f : fast_exp2(m_old - m_use);
+                        moved |= m_new != m_old;
                         const float p0 = fast_exp2(sacc[e] - m_use);
                         const float p1 = fast_exp2(sacc[e + 2] - m_use);
                         sacc[e] = p0;
@@ -1257,12 +1285,14 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                         l_run[e] = l_run[e] * alpha[e] + (p0 + p1);
                         m_run[e] = m_new;
                     }
+                    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-                    for (int n = 0; n < HD / 16; ++n) {
-                        o[n][0] *= alpha[0];
-                        o[n][1] *= alpha[1];
-                        o[n][2] *= alpha[0];
-                        o[n][3] *= alpha[1];
+                        for (int n = 0; n < HD / 16; ++n) {
+                            o[n][0] *= alpha[0];
+                            o[n][1] *= alpha[1];
+                            o[n][2] *= alpha[0];
+                            o[n][3] *= alpha[1];
+                        }
                     }
                     if constexpr (FP8) {
                         // P^T in f16 (one rounding: 11 significant bits)
@@ -1479,32 +1509,52 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                             }
                         }
                     }
+                    // the whole chunk visible to every row of the warp: no mask
+                    int pmin = rpos[0][0], pmax = rpos[0][0];
+    #pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+    #pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            pmin = min(pmin, rpos[mt][hr]);
+                            pmax = max(pmax, rpos[mt][hr]);
+                        }
+                    const bool open = __all_sync(
+                        0xffffffffu, chunk_open(mask16, t0, seq_len, ring_lo, window, pmin, pmax));
                     uint32_t pa[MT][4], pl[MT][4];  // P as bf16 hi + lo
     #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
-    #pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const int pos = rpos[mt][hr];
-                            float mx = -INFINITY;
+                        if (open) {
     #pragma unroll
                             for (int j = 0; j < 2; ++j)
     #pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int n = j * 8 + tq * 2 + e;
-                                    const int t = t0 + n;
-                                    const bool valid = rvalid[mt][hr] && ((mask16 >> n) & 1u) &&
-                                                       t < seq_len && t <= pos && t >= ring_lo &&
-                                                       (window <= 0 || pos - t < window);
-                                    const float v =
-                                        valid ? s[mt][j][hr * 2 + e] * p.scale_log2 : -INFINITY;
-                                    s[mt][j][hr * 2 + e] = v;
-                                    mx = fmaxf(mx, v);
-                                }
+                                for (int e = 0; e < 4; ++e) s[mt][j][e] *= p.scale_log2;
+                        } else {
+    #pragma unroll
+                            for (int hr = 0; hr < 2; ++hr)
+    #pragma unroll
+                                for (int j = 0; j < 2; ++j)
+    #pragma unroll
+                                    for (int e = 0; e < 2; ++e) {
+                                        const int n = j * 8 + tq * 2 + e;
+                                        const int t = t0 + n, pos = rpos[mt][hr];
+                                        const bool valid =
+                                            rvalid[mt][hr] && ((mask16 >> n) & 1u) &&
+                                            t < seq_len && t <= pos && t >= ring_lo &&
+                                            (window <= 0 || pos - t < window);
+                                        s[mt][j][hr * 2 + e] =
+                                            valid ? s[mt][j][hr * 2 + e] * p.scale_log2
+                                                  : -INFINITY;
+                                    }
+                        }
+    #pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            float mx = fmaxf(fmaxf(s[mt][0][hr * 2], s[mt][0][hr * 2 + 1]),
+                                             fmaxf(s[mt][1][hr * 2], s[mt][1][hr * 2 + 1]));
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                            const float m_new = fmaxf(m_run[mt][hr], mx);
+                            const float m_old = m_run[mt][hr];
+                            const float m_new = mx > m_old + kRescaleLog2 ? mx : m_old;
                             const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                            const float alpha = fast_exp2(m_run[mt][hr] - m_use);
                             float sum = 0.f;
     #pragma unroll
                             for (int j = 0; j < 2; ++j)
@@ -1514,13 +1564,18 @@ __global__ void __launch_bounds__(kThreads, Geo<HD, MT, FP8>::kCtasPerSm)
                                     s[mt][j][hr * 2 + e] = pv;
                                     sum += pv;
                                 }
-                            l_run[mt][hr] = l_run[mt][hr] * alpha + sum;
-                            m_run[mt][hr] = m_new;
+                            if (__any_sync(0xffffffffu, m_new != m_old)) {
+                                const float alpha =
+                                    m_new == m_old ? 1.f : fast_exp2(m_old - m_use);
+                                l_run[mt][hr] *= alpha;
     #pragma unroll
-                            for (int n = 0; n < HD / 8; ++n) {
-                                o[mt][n][hr * 2] *= alpha;
-                                o[mt][n][hr * 2 + 1] *= alpha;
+                                for (int n = 0; n < HD / 8; ++n) {
+                                    o[mt][n][hr * 2] *= alpha;
+                                    o[mt][n][hr * 2 + 1] *= alpha;
+                                }
                             }
+                            l_run[mt][hr] += sum;
+                            m_run[mt][hr] = m_new;
                         }
                         if constexpr (FP8) {  // P in f16, one rounding
                             pa[mt][0] = pack_f16x2(s[mt][0][0], s[mt][0][1]);
