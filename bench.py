@@ -62,10 +62,10 @@ def load_peaks():
 # T = 14,449, from ncu (profiles/prefill_kernel_qwen14449.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 198134272,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 198432768,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "b71c0f0c22d0a85c0c1979b2f2488211eb5a2fbc948df1f8934ffe7d89c41ba3"}
+                   "sha256": "4fad6952aff5432a1a18a4c7333d431d6cdfc35eb7b840176029c2b63bcae141"}
 
 
 def prefill_traffic(T):
