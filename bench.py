@@ -62,10 +62,10 @@ def load_peaks():
 # T = 14,449, from ncu (profiles/prefill_kernel_qwen14449.md).  They
 # describe the kernel built from these exact sources and are dropped (null)
 # once either file changes.
-PREFILL_TRAFFIC = {"T": 14449, "bytes": 198432768,
+PREFILL_TRAFFIC = {"T": 14449, "bytes": 198099200,
                    "sources": ("gqa_attention_kv_gb300/csrc/prefill.cu",
                                "gqa_attention_kv_gb300/csrc/ptx.cuh"),
-                   "sha256": "4fad6952aff5432a1a18a4c7333d431d6cdfc35eb7b840176029c2b63bcae141"}
+                   "sha256": "115c6fa0c9008eea39e7d09d55a27d44c520a44b4e1242a749e24f57669c3c27"}
 
 
 def prefill_traffic(T):

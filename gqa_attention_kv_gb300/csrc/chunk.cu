@@ -521,12 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-            for (int c = 4; c < kBN; c += 8) {
+            for (int c = 4; c + 8 <= kBN; c += 8) {  // columns 4 .. kBN - 5
                 mx0 = max3(mx0, s[c], s[c + 1]);
                 mx1 = max3(mx1, s[c + 2], s[c + 3]);
                 mx2 = max3(mx2, s[c + 4], s[c + 5]);
                 mx3 = max3(mx3, s[c + 6], s[c + 7]);
             }
+            mx0 = max3(mx0, s[kBN - 4], s[kBN - 3]);  // the last four columns
+            mx1 = max3(mx1, s[kBN - 2], s[kBN - 1]);
             const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
             float alpha = 1.f;
             if (mx > m_run + kRescaleThreshold || m_run == -INFINITY) {
