@@ -14,7 +14,10 @@ every row's scores follow a chosen level s(t) (log2 units) plus small noise:
           7.5 step half way (no rescale: P near 2^7.5 on that half);
 * saw:    alternates 0 / 7.5 every 160 keys: the reference never moves after
           the first chunk, and split partial states of comparable weight
-          carry references below their true maxima into the merges.
+          carry references below their true maxima into the merges;
+* spike:  the last four keys of every 128-key tile 20 above the rest: a row
+          maximum that missed a tile's last columns would leave P near 2^20,
+          past f16's range (the prefill and chunk kernels).
 
 The output is checked against the fp64 oracle at the stated tolerance, for
 the decode split kernel (8-row and 16-row tilings, bf16 and E4M3 caches, one
@@ -45,6 +48,8 @@ def level(profile, t):
         return 8.5 * np.floor(t / 320.0) + 7.5 * ((t % 320) >= 160)
     if profile == "saw":
         return 7.5 * (np.floor(t / 160.0) % 2)
+    if profile == "spike":
+        return 20.0 * ((t % 128) >= 124)
     raise ValueError(profile)
 
 
@@ -127,7 +132,7 @@ def test_decode_one_unit_over_many_ctas(profile):
     compare(out, ref, f"{profile} one unit, 14,449 keys")
 
 
-@pytest.mark.parametrize("profile", ["ramp", "stairs", "saw"])
+@pytest.mark.parametrize("profile", ["ramp", "stairs", "saw", "spike"])
 def test_chunk_kernel(profile):
     """29-row chunks of 28/4 heads (203 rows a KV group: the tcgen05 chunk kernel)."""
     case = synth.decode_case(9400, LINEAR, 2, 29, 28, 4, 128, [3029, 1529])
@@ -137,7 +142,7 @@ def test_chunk_kernel(profile):
     compare(out, ref, f"{profile} chunk")
 
 
-@pytest.mark.parametrize("profile", ["ramp", "stairs", "saw"])
+@pytest.mark.parametrize("profile", ["ramp", "stairs", "saw", "spike"])
 @pytest.mark.parametrize("B,T,Hq,Hkv,D", [(1, 1500, 28, 4, 128), (2, 750, 32, 32, 64)])
 def test_prefill(profile, B, T, Hq, Hkv, D):
     p = synth.prefill_case(9500 + T + D, B, T, Hq, Hkv, D)
