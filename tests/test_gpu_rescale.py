@@ -6,7 +6,9 @@ reference by more than 2^8 (the lazy rescale of the prefill, chunk and decode
 kernels).  Seeded N(0, 1) inputs settle the maximum within the first tiles,
 so these cases shape q and K instead: q of every head near a fixed +-1
 direction u of its KV head, and the key at position t near a(t) u, so that
-every row's scores follow a chosen level s(t) (log2 units) plus small noise:
+every row's scores follow a chosen level s(t) (log2 units, scaled by a factor
+of the head within 10% of 1) plus small noise (pinned on the CPU in
+`test_rescale_inputs.py`):
 
 * ramp:   s rises by 0.5 per 16 keys: the reference moves every ~16 chunks,
           and P approaches 2^8 just before each move;
